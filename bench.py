@@ -1,0 +1,341 @@
+"""Benchmark: draft-tree builds per second at the Qwen3-4B shape (B=64).
+
+One step = one whole round of the hot path (LM head + Top-M, the 15-depth
+batched expansion, global Top-B, tree + mask) on one batch of synthetic input,
+replayed as one CUDA graph through the C ABI.  Inputs are resident in HBM when
+the timed region starts; the LM head streams 778 MB of weights per round, more
+than the 129 MB L2, so no explicit L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(no data-path collective); value = rounds of all ranks / max elapsed.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft-tree builds/sec & us/round (Qwen3-4B shape, B=64); HBM GB/s vs peak"
+WORKLOAD = "qwen3_4b"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _config_dict(cfg, n_inputs):
+    return {
+        "workload": f"{cfg.name}: d={cfg.d} V={cfg.V} block={cfg.block} g={cfg.g} r={cfg.r} "
+                    f"M={cfg.M} K={cfg.K} W={cfg.W} B={cfg.B} beta={cfg.beta} T={cfg.T} n_req={cfg.n_req}",
+        "n_req": cfg.n_req, "depth": cfg.block - 1, "B": cfg.B, "distinct_inputs": n_inputs,
+        "l2": "inputs larger than L2 (778 MB LM head streamed per round), no flush",
+    }
+
+
+def algorithmic_bytes(cfg):
+    """HBM bytes one round must move (roofline)."""
+    D = cfg.block - 1
+    lm = cfg.V * cfg.d * 2
+    w1h = cfg.r * cfg.d * 2
+    h = cfg.n_req * cfg.block * cfg.d * 2
+    logits_out = cfg.n_req * D * cfg.V * 4 + cfg.n_req * D * cfg.r * 4
+    kernel = lm + w1h + h + logits_out
+    w_hh = 3 * cfg.g * cfg.g * 2
+    w1s = cfg.r * cfg.g * 2
+    w2 = cfg.n_req * D * cfg.M * cfg.r * 2
+    xrows = cfg.n_req * (1 + (D - 1) * cfg.W) * 3 * cfg.g * 4
+    round_bytes = lm + w1h + h + w_hh + w1s + w2 + xrows
+    return kernel, round_bytes
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_oracle_rounds(cfg, w, seeds):
+    from oracle.dartree import Oracle
+    from workloads import make_round_inputs
+    orc = Oracle(w, cfg)
+    trees, times = [], []
+    for s in seeds:
+        H, root = make_round_inputs(cfg, s)
+        t0 = time.perf_counter()
+        trees.append(orc.build_round(H, root))
+        times.append(time.perf_counter() - t0)
+    return orc, trees, times
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def bench_reference(args):
+    """The fp64 oracle as it stands, on the host cores, same workload and metric."""
+    from workloads import get_config, make_weights
+    cfg = get_config(WORKLOAD)
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = make_weights(cfg)
+    _, _, tw = run_oracle_rounds(cfg, w, range(1000, 1000 + args.warmup))
+    _, _, times = run_oracle_rounds(cfg, w, range(args.steps))
+    total = sum(times)
+    value = args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "builds/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config_dict(cfg, args.steps),
+        "cpu_baseline": {"value": value, "unit": "builds/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{args.steps} whole rounds (seeds 0..{args.steps - 1}) of the fp64 oracle"},
+        "e2e": {"value": value, "unit": "builds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_gpu(args):
+    import numpy as np
+    import torch
+
+    from conditional_draft_tree_lm_gb300 import DraftTreeBuilder, bf16_tensor
+    from conditional_draft_tree_lm_gb300.build import build_library
+    from workloads import get_config, make_round_inputs, make_weights
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    build_library()
+    cfg = get_config(WORKLOAD)
+    w = make_weights(cfg)
+    wd = {k: bf16_tensor(v) for k, v in w.items()}
+    builder = DraftTreeBuilder(cfg, wd)
+    n_inputs = args.inputs
+    seeds = [rank * 100000 + s for s in range(n_inputs)]
+    Hs, roots = [], []
+    for s in seeds:
+        H, root = make_round_inputs(cfg, s)
+        Hs.append(bf16_tensor(H))
+        roots.append(torch.from_numpy(root.astype(np.int32)).cuda())
+    outs = [builder.new_tree() for _ in range(n_inputs)]
+    stream = torch.cuda.current_stream()
+
+    def step(k):
+        j = k % n_inputs
+        builder.build_round(Hs[j], roots[j], outs[j])
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    # per-round latency distribution (one event pair per round)
+    lat = []
+    for k in range(min(args.steps, 200)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step(k)
+        b.record(stream)
+        b.synchronize()
+        lat.append(a.elapsed_time(b) * 1e3)
+    # dominant kernel (LM head GEMM) timed alone with events on its stream
+    logits = torch.empty(cfg.n_req, cfg.block - 1, cfg.V, dtype=torch.float32, device="cuda")
+    for k in range(3):
+        builder.base_logits(Hs[k % n_inputs], logits)
+    nk = max(10, min(args.steps, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(nk):
+        builder.base_logits(Hs[k % n_inputs], logits)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    lm_ms = e0.elapsed_time(e1) / nk
+    clk = clocks.stop()
+    # end to end through the public API with host buffers (pinned)
+    Hh = [torch.from_numpy(np.ascontiguousarray(make_round_inputs(cfg, s)[0]).view(np.int16))
+          .view(torch.bfloat16).pin_memory() for s in seeds[:4]]
+    rh = [torch.from_numpy(make_round_inputs(cfg, s)[1].astype(np.int32)).pin_memory() for s in seeds[:4]]
+    out_h = {k: v.cpu().pin_memory() for k, v in builder.new_tree().items()}
+    for k in range(3):
+        builder.build_round_host(Hh[k % 4], rh[k % 4], out_h)
+    n_e2e = max(10, min(args.steps, 200))
+    t0 = time.perf_counter()
+    for k in range(n_e2e):
+        builder.build_round_host(Hh[k % 4], rh[k % 4], out_h)
+    e2e_s = time.perf_counter() - t0
+    h2d = Hh[0].numel() * 2 + rh[0].numel() * 4
+    d2h = sum(v.numel() * v.element_size() for v in out_h.values())
+
+    status = builder.device_status()
+    elapsed = ms / 1e3
+    if dist:
+        t = torch.tensor([elapsed, e2e_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed, e2e_s = float(t[0]), float(t[1])
+    rounds = args.steps * world
+    value = rounds / elapsed
+    kbytes, rbytes = algorithmic_bytes(cfg)
+    peak, peak_kind = _peaks()
+    achieved = kbytes / (lm_ms / 1e3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "lm_head_gemm_qwen3_4b_traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                pj = json.load(f)
+            if pj.get("kernel_source_hash") == _kernel_hash():
+                traffic = pj.get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    us_round = 1e6 * elapsed / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "builds/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "us_per_round": us_round,
+        "us_per_round_p10_p50_p90": [float(np.percentile(lat, q)) for q in (10, 50, 90)],
+        "round_hbm_gbs": rbytes / (us_round * 1e-6) / 1e9,
+        "round_hbm_frac": rbytes / (us_round * 1e-6) / 1e9 / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1/fan_in) weights, N(0,1) hidden states)",
+        "config": _config_dict(cfg, n_inputs),
+        "roofline": {"bound": "hbm", "kernel": "k_gemm_tc (LM head + W1_H, tcgen05/TMA)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": lm_ms * 1e3},
+        "e2e": {"value": n_e2e * world / e2e_s, "unit": "builds/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": builder.round_kernel_count() * args.steps,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        t_budget = args.cpu_seconds
+        seeds_cpu, times = [], []
+        from oracle.dartree import Oracle
+        orc = Oracle(w, cfg)
+        t_start = time.perf_counter()
+        k = 0
+        while time.perf_counter() - t_start < t_budget and k < 16:
+            H, root = make_round_inputs(cfg, seeds[k % n_inputs])
+            t0 = time.perf_counter()
+            orc.build_round(H, root)
+            times.append(time.perf_counter() - t0)
+            seeds_cpu.append(seeds[k % n_inputs])
+            k += 1
+        line["cpu_baseline"] = {"value": len(times) / sum(times), "unit": "builds/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"{len(times)} whole rounds of the fp64 oracle (~{t_budget:.0f} s budget)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    builder.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "conditional_draft_tree_lm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--inputs", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

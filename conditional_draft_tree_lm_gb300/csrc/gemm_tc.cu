@@ -1,0 +1,261 @@
+// Skinny "TN" GEMM on the 5th-generation tensor cores: D[m, n] = sum_k A[m, k] B[n, k]
+// with A and B bf16 K-major, fp32 accumulation in tensor memory.
+//
+// Uses:
+//  * base logits (Domino page, Columna Vertebral, Salida): A = the frozen LM head
+//    [V, d] (tiles 0..ceil(V/128)-1) followed by the H half of W1, W1[:, :d]
+//    ([r, d], row stride d+g; the remaining tiles), B = H viewed as
+//    [n_req*block, d].  The roles are swapped (A = weights) so that the MMA's
+//    M dimension is 128 vocabulary rows and its N dimension the few H rows; the
+//    kernel is bound by streaming A from HBM.  The epilogue scatters columns of
+//    block position i >= 1 to logits[q, i-1, v] (or h1[q, i-1, j]).
+//  * the GRU input table (create time): A = E [V, d], B = W_ih [3g, d],
+//    D + b_ih -> X [V, 3g] fp32.
+//
+// Structure: one persistent CTA per SM, 6 warps.  Warp 0 issues TMA loads of
+// A/B k-blocks (64 bf16 = one 128-byte swizzle row) into a ring of shared-memory
+// stages; warp 1 owns the tensor memory and issues tcgen05.mma (M=128, N<=256,
+// K=16) from one thread, committing each stage back to the producer and each
+// finished tile to the epilogue; warps 2..5 drain the accumulator with
+// tcgen05.ld (one TMEM lane quarter each) while the next tile accumulates into
+// the other half of tensor memory.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dt {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = 128 * 128;  // 128 rows x 64 bf16
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a2,
+              const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
+  uint64_t* empty = full + p.stages;
+  uint64_t* tfull = empty + p.stages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = p.m_tiles_a + p.m_tiles_a2;
+  const int num_tiles = m_tiles * p.n_tiles;
+  const int num_kb = (p.K + 63) / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_a = p.a_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_last();
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+        const bool second = mt >= p.m_tiles_a;
+        const void* ta = second ? static_cast<const void*>(&tm_a2) : static_cast<const void*>(&tm_a);
+        const int row_a = (second ? mt - p.m_tiles_a : mt) * 128;
+        const int row_b = nt * p.BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], p.stage_bytes);
+          uint8_t* sa = smem + stage * p.stage_bytes;
+          uint8_t* sb = sa + kABytes;
+          tma_load_2d(sa, ta, &full[stage], kb * 64, row_a, pol_a);
+          for (int h = 0; h < p.BN; h += 256)
+            tma_load_2d(sb + h * 128, &tm_b, &full[stage], kb * 64, row_b + h, pol_b);
+          if (++stage == static_cast<uint32_t>(p.stages)) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        const int acc = p.acc_bufs == 2 ? (local & 1) : 0;
+        const uint32_t use = p.acc_bufs == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = sdesc_k_sw128(sa + k * 32);
+            for (int h = 0; h < p.BN; h += 256) {
+              const uint32_t n = min(256, p.BN - h);
+              const uint64_t bd = sdesc_k_sw128(sb + h * 128 + k * 32);
+              tc_mma_bf16(d_tmem + h, ad, bd, idesc_bf16_f32(128, n), (kb | k) != 0);
+            }
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == static_cast<uint32_t>(p.stages)) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    // epilogue: warps 2..5; TMEM lanes [32*(warp%4), +32)
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int acc = p.acc_bufs == 2 ? (local & 1) : 0;
+      const uint32_t use = p.acc_bufs == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
+      if (!mbar_wait(&tfull[acc], use & 1u, p.status)) break;
+      tc_fence_after();
+      const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * p.BN);
+      if (p.mode == GEMM_LOGITS) {
+        const bool second = mt >= p.m_tiles_a;
+        const int row = (second ? mt - p.m_tiles_a : mt) * 128 + row_in_tile;
+        const int nrows = second ? p.rows_a2 : p.rows_a;
+        float* dst = second ? p.h1 : p.logits;
+        const bool valid = row < nrows;
+        for (int c0 = 0; c0 < p.BN; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tbase + c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = c0 + j;
+            if (n >= p.n_valid) break;
+            const int q = n / p.block, i = n - q * p.block;
+            if (i > 0 && valid)
+              dst[static_cast<size_t>(q * p.D + i - 1) * nrows + row] = __uint_as_float(v[j]);
+          }
+        }
+      } else {
+        const int row = mt * 128 + row_in_tile;
+        const bool valid = row < p.rows_a;
+        for (int c0 = 0; c0 < p.BN; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tbase + c0, v);
+          const int col0 = nt * p.BN + c0;
+          if (valid) {
+            float* o = p.out + static_cast<size_t>(row) * p.ldo + col0;
+            if (col0 + 16 <= p.n_valid) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 4) {
+                float4 f;
+                f.x = __uint_as_float(v[j]) + bf16_to_f32(p.bias[col0 + j]);
+                f.y = __uint_as_float(v[j + 1]) + bf16_to_f32(p.bias[col0 + j + 1]);
+                f.z = __uint_as_float(v[j + 2]) + bf16_to_f32(p.bias[col0 + j + 2]);
+                f.w = __uint_as_float(v[j + 3]) + bf16_to_f32(p.bias[col0 + j + 3]);
+                *reinterpret_cast<float4*>(o + j) = f;
+              }
+            } else {
+              for (int j = 0; j < 16 && col0 + j < p.n_valid; ++j)
+                o[j] = __uint_as_float(v[j]) + bf16_to_f32(p.bias[col0 + j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t row_stride_bytes, uint32_t box_rows) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (row_stride_bytes & 15u) != 0) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Fill the launch-shape fields of p for a tile width BN (16..256 or 512).
+void gemm_plan(GemmParams& p, int BN) {
+  p.BN = BN;
+  p.b_bytes = static_cast<uint32_t>(BN) * 128u;
+  p.stage_bytes = kABytes + p.b_bytes;
+  const uint32_t budget = 200u * 1024u;
+  int st = static_cast<int>(budget / p.stage_bytes);
+  p.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
+  p.acc_bufs = (2 * BN <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < p.acc_bufs * BN) cols <<= 1;
+  p.tmem_cols = cols;
+}
+
+size_t gemm_smem_bytes(const GemmParams& p) {
+  return 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (2 * p.stages + 4) * 8 + 16;
+}
+
+cudaError_t gemm_prepare() {
+  return cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_a2, const CUtensorMap& tm_b,
+                           const GemmParams& p, int num_sms, cudaStream_t stream) {
+  const size_t smem = gemm_smem_bytes(p);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  const int tiles = (p.m_tiles_a + p.m_tiles_a2) * p.n_tiles;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  k_gemm_tc<<<grid, kThreads, smem, stream>>>(tm_a, tm_a2, tm_b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dt

@@ -1,0 +1,128 @@
+// Launch interfaces of the libdtree kernels (host side).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dt {
+
+constexpr int kMaxDepth = 64;
+
+// ---------------------------------------------------------------- tcgen05 GEMM
+enum GemmMode { GEMM_LOGITS = 0, GEMM_TABLE = 1 };
+
+struct GemmParams {
+  int mode;
+  int K;           // inner dimension
+  int m_tiles_a;   // 128-row tiles taken from the first A tensor
+  int m_tiles_a2;  // 128-row tiles taken from the second A tensor (logits mode: W1[:, :d])
+  int n_tiles;     // BN-wide tiles of B
+  int BN;          // tile width: 16..256 (multiple of 16) or 512
+  int n_valid;     // valid B rows
+  int stages;
+  uint32_t stage_bytes, b_bytes;
+  int tmem_cols;
+  int acc_bufs;
+  int a_evict_first;
+  int rows_a, rows_a2;  // valid rows of the two A tensors
+  // logits mode
+  int block, D;
+  float* logits;  // [n_req*D, rows_a]
+  float* h1;      // [n_req*D, rows_a2]
+  // table mode
+  float* out;
+  int ldo;
+  const uint16_t* bias;
+  int* status;
+};
+
+bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t row_stride_bytes, uint32_t box_rows);
+void gemm_plan(GemmParams& p, int BN);
+size_t gemm_smem_bytes(const GemmParams& p);
+cudaError_t gemm_prepare();
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_a2, const CUtensorMap& tm_b,
+                           const GemmParams& p, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- Top-M
+struct TopmParams {
+  const float* logits;  // [rows, V]
+  int V, rows, M, S, chunk;
+  float T;
+  int* part_id;     // [rows, S, M]
+  float* part_val;  // [rows, S, M]
+  float* part_max;  // [rows, S]   max of logit/T over the chunk
+  float* part_sum;  // [rows, S]   sum over the chunk's non-candidates of exp(logit/T - max)
+  int* part_cnt;    // [rows, S]
+  int* cand_tok;    // [rows, M]
+  float* cand_base; // [rows, M]
+  float* rest_lse;  // [rows]
+  int* status;
+};
+void topm_plan(TopmParams& p, int num_sms);
+size_t topm_partial_smem(const TopmParams& p);
+size_t topm_merge_smem(const TopmParams& p);
+cudaError_t topm_prepare();
+cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- depth chain
+struct ChainParams {
+  int n_req, D, g, r, M, K, W, V, ldw1, d;
+  int N1;  // nodes per request including the root
+  float T;
+  const uint16_t* w_hh;  // [3g, g]
+  const uint16_t* w1;    // [r, d+g]
+  const uint16_t* w2;    // [V, r]
+  const float* xtab;     // [V, 3g]
+  const float* h1;       // [n_req*D, r]
+  const int* cand_tok;   // [n_req*D, M]
+  const float* cand_base;
+  const float* rest_lse;  // [n_req*D]
+  const int* root_tok;    // [n_req]
+  float* S;      // [2, n_req*W, g]
+  float* uW1;    // [n_req*W, r]
+  int* live;     // [2, n_req, W]
+  int* node_tok;
+  int* node_parent;
+  float* node_logp;
+  float* node_score;  // [n_req, N1]
+  int* live_out;      // [n_req, W] or null
+  unsigned* bar;      // grid-barrier counter, zero at launch
+  int* status;
+  int depth_first, depth_last;
+  int jper, rper;     // S / r columns owned per CTA
+  int cpad;           // padded owned-column count (multiple of 32)
+  int off[kMaxDepth + 1];  // first node index of depth i
+  int nn[kMaxDepth + 1];   // nodes created at depth i
+  int L[kMaxDepth + 1];    // branches that live after depth i (L[0] = 1)
+};
+int chain_grid(const ChainParams& p, int num_sms);
+size_t chain_smem_bytes(const ChainParams& p);
+void chain_plan(ChainParams& p, int grid);
+cudaError_t chain_prepare();
+cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream);
+
+// ---------------------------------------------------------------- Top-B and tree
+struct PruneParams {
+  int n_req, N1, B, D;
+  float beta;
+  const float* node_score;  // [n_req, N1]
+  int* sel;                 // [n_req, B]
+  const int* node_tok;
+  const int* node_parent;
+  int* tok;
+  int* parent;
+  int* depth;
+  float* logp_cum;
+  uint8_t* mask;
+  int* status;
+  int off[kMaxDepth + 2];   // off[i] first node of depth i; off[D+1] = N1
+};
+size_t prune_smem_bytes(const PruneParams& p);
+cudaError_t prune_prepare();
+cudaError_t launch_prune(const PruneParams& p, cudaStream_t stream);
+cudaError_t launch_tree_mask(const PruneParams& p, cudaStream_t stream);
+
+}  // namespace dt

@@ -1,0 +1,226 @@
+/*
+ * libdtree — path-conditioned draft-tree construction, built depth by depth in
+ * batches, for a Domino-style drafter (parallel backbone + GRU low-rank logit
+ * correction), on NVIDIA GB300 (sm_103a).
+ *
+ * The method (sources are three technical summaries):
+ *   "Resumen Técnico: Domino" (Metodología): base logits L^base_i = H_i W_lm
+ *     from the frozen LM head; a light GRU summarises the preceding draft
+ *     tokens into S_{i-1}; a rank-r bottleneck maps [H_i ; S_{i-1}] to a logit
+ *     correction Delta L_i; final logits L_i = L^base_i + Delta L_i.
+ *   "Resumen Técnico: DominoTree" (Componentes Principales, 2. Top-M): the
+ *     correction is evaluated only on the Top-M base candidates of each depth.
+ *   "DARTree: Speculative Diffusion Decoding with Autoregressive Draft Trees"
+ *     (Metodología 1, depth-wise parallel expansion; 2, deferred pruning and
+ *     Lemma 1): all live branches of a depth are corrected in one batch, the W
+ *     best children live on, and one global Top-B over score + beta*depth
+ *     (beta <= 0) picks the tree handed to tree-attention verification.
+ *
+ * Conventions of every entry point:
+ *   - All device pointers are plain CUDA device addresses owned by the caller
+ *     unless stated; bf16 data is passed as `const void*` (IEEE bfloat16).
+ *   - Weights use the out-by-in row-major layout of torch.nn.Linear weights.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  They never synchronise except dt_get_device_status and
+ *     dt_build_round_host.
+ *   - Errors are returned as dt_status; nothing is thrown across the ABI.
+ *     Faults detected on the device (an index out of range, a bounded wait that
+ *     gave up) are recorded in the context's device status word and reported
+ *     by dt_get_device_status.
+ *   - Depth i = 1..D (D = block - 1) uses block position i of H; position 0 is
+ *     the last verified token (the root) and its hidden state is not used.
+ *   - Super-tree node numbering (per request): node 0 is the root; the nodes
+ *     created at depth i follow all nodes of depth i-1, ordered by (parent
+ *     index, token id).  Node arrays hold dt_node_count(cfg) + 1 entries per
+ *     request.
+ *   - Tie rules: Top-M and per-branch top-K prefer the lower token id; top-W and
+ *     Top-B prefer the lower node index.
+ */
+#ifndef DTREE_H_
+#define DTREE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dt_status {
+  DT_OK = 0,
+  DT_ERR_INVALID_ARG = 1,   /* null pointer, out-of-range scalar, calls out of order */
+  DT_ERR_SHAPE = 2,         /* sizes the kernels do not support (see dt_check_config) */
+  DT_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+  DT_ERR_OOM = 4,           /* device allocation failed */
+  DT_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up */
+  DT_ERR_UNIMPLEMENTED = 6, /* entry point or mode not built */
+  DT_ERR_DEVICE = 7         /* device-side check failed (bad index, non-closed tree) */
+} dt_status;
+
+/* Round configuration.  D = block - 1 depths. */
+typedef struct dt_config {
+  int d;      /* backbone hidden size; multiple of 8 */
+  int V;      /* vocabulary size */
+  int block;  /* block length (root + D masked positions), 2..64 */
+  int g;      /* GRU hidden size */
+  int r;      /* correction bottleneck rank */
+  int M;      /* Top-M candidates per depth, K <= M <= min(V, 512) */
+  int K;      /* children kept per branch, 1..32 */
+  int W;      /* live branches kept per depth, 1..64 */
+  int B;      /* node budget of the emitted tree (root excluded), B <= N */
+  int n_req;  /* independent requests per round; n_req * block <= 512 */
+  float beta; /* depth bonus of the Top-B key (score + beta * depth); <= 0 */
+  float T;    /* temperature dividing the corrected logits; > 0 */
+  unsigned flags; /* reserved, must be 0 */
+} dt_config;
+
+/* Frozen weights (device pointers, borrowed: they must outlive the context).
+ * All bf16, row-major, torch.nn.Linear out-by-in layout.  GRU gate blocks are
+ * ordered (r, z, n); the GRU has one input-side bias and no hidden bias. */
+typedef struct dt_weights {
+  const void* lm_head; /* [V, d]   row v = output vector of token v (L^base = H lm_head^T) */
+  const void* emb;     /* [V, d]   token embeddings E (GRU input) */
+  const void* w_ih;    /* [3g, d]  GRU input weights */
+  const void* b_ih;    /* [3g]     GRU input bias */
+  const void* w_hh;    /* [3g, g]  GRU hidden weights */
+  const void* w1;      /* [r, d+g] bottleneck over [H_i ; S_{i-1}] */
+  const void* w2;      /* [V, r]   up-projection (row c = column c of W2) */
+} dt_weights;
+
+typedef struct dt_ctx dt_ctx;
+
+/* --------------------------------------------------------------------------
+ * Host-only helpers (no CUDA calls).
+ * ------------------------------------------------------------------------ */
+
+/* Validate a configuration: K <= M <= V, M <= 512, 1 <= K <= 32,
+ * 1 <= W <= 64, 2 <= block <= 64, d % 8 == 0, g % 8 == 0, r % 8 == 0,
+ * r <= 1024, g <= 4096, n_req * block <= 512, 1 <= B <= N, T > 0, beta <= 0,
+ * flags == 0.  Returns DT_OK, DT_ERR_INVALID_ARG or DT_ERR_SHAPE. */
+dt_status dt_check_config(const dt_config* cfg);
+
+/* N: super-tree nodes of one request without the root (n_1 = K,
+ * n_i = min(W, n_{i-1}) K; DARTree page, fixed-width super-tree).  -1 if cfg
+ * is NULL. */
+int64_t dt_node_count(const dt_config* cfg);
+
+/* Device bytes that dt_create allocates for this configuration (workspace,
+ * GRU input table, captured-round buffers).  0 if the configuration is invalid. */
+size_t dt_workspace_bytes(const dt_config* cfg);
+
+/* Static description of a status code. */
+const char* dt_status_string(dt_status s);
+
+/* --------------------------------------------------------------------------
+ * Context.
+ * ------------------------------------------------------------------------ */
+
+/* Validate cfg, borrow the weights, allocate the workspace on the current
+ * device and build the GRU input table X[v] = E[v] W_ih^T + b_ih ([V, 3g]
+ * fp32, an exact regrouping of the GRU input projection; Domino page,
+ * Codificador Causal) on `stream`.  *out receives the context.  Errors:
+ * INVALID_ARG / SHAPE (bad cfg or null weight), OOM, CUDA. */
+dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_ctx** out);
+
+/* Synchronise the context's work, free everything it owns.  NULL is a no-op. */
+dt_status dt_destroy(dt_ctx* ctx);
+
+/* --------------------------------------------------------------------------
+ * Steps of one round (call in this order; each reads what the previous wrote
+ * into the context's workspace).
+ * ------------------------------------------------------------------------ */
+
+/* Step 1 — base logits (Domino page, Columna Vertebral, Salida; DominoTree
+ * page, Hecho Estructural: H is shared by all paths).
+ *   H:      [n_req, block, d] bf16 hidden states of the parallel backbone.
+ *   logits: [n_req, D, V] fp32 output, logits[q, i-1, v] = H[q, i] . lm_head[v];
+ *           NULL keeps them only in the workspace.
+ * Also computes H[q, i] W1[:, :d]^T (the H half of the bottleneck) into the
+ * workspace for dt_expand_depth.  One tcgen05/TMA kernel. */
+dt_status dt_base_logits(dt_ctx* ctx, const void* H, float* logits, void* stream);
+
+/* Step 2 — Top-M candidates and rest log-partition per (request, depth)
+ * (DominoTree page, Top-M restriction; the M corrected entries are
+ * substituted into the base log-partition).
+ *   logits:    [n_req, D, V] fp32 input, or NULL for the workspace copy.
+ *   cand_tok:  [n_req, D, M] int32 out (NULL = workspace only), ordered by
+ *              logit descending, token id ascending.
+ *   cand_base: [n_req, D, M] fp32 out: base logits of those tokens (not / T).
+ *   rest_lse:  [n_req, D] fp32 out: log sum_{v not in C} exp(logit_v / T),
+ *              -inf when M == V. */
+dt_status dt_topm(dt_ctx* ctx, const float* logits, int32_t* cand_tok, float* cand_base,
+                  float* rest_lse, void* stream);
+
+/* Step 3 — one depth of the batched expansion (DARTree page, Metodología 1;
+ * Domino page, Cabeza de Domino).  For every live branch p of depth-1:
+ * z = SiLU([H_i ; S(p)] W1^T), lambda_c = (L^base_{i,c} + z . W2[c]) / T on the
+ * Top-M candidates c, logp = lambda - log(e^rest_lse + sum_c e^lambda_c); the K
+ * best children per branch get score(p) + logp; the W best children of the
+ * depth keep a GRU state S = GRU(E[token], S(p)).
+ *   depth:     1..D; depths must be called in order 1, 2, ..., D.
+ *   root_tok:  [n_req] int32, read at depth 1 (the last verified token).
+ *   node_*:    [n_req, N+1] outputs (N = dt_node_count); depth i writes the
+ *              entries of its own nodes (depth 1 also writes the root, node 0:
+ *              token root_tok, parent -1, logp 0, score 0).
+ *              node_tok int32, node_parent int32 (node index), node_logp fp32
+ *              (the node's conditional log-prob), node_score fp32 (cumulative).
+ *   live:      [n_req, W] int32 out or NULL: node indices of the branches that
+ *              live on after this depth, ascending, padded with -1.
+ * The same node buffers must be passed at every depth of a round. */
+dt_status dt_expand_depth(dt_ctx* ctx, int depth, const int32_t* root_tok, int32_t* node_tok,
+                          int32_t* node_parent, float* node_logp, float* node_score,
+                          int32_t* live, void* stream);
+
+/* Step 4 — deferred pruning (DARTree page, Poda Diferida: Selección Global,
+ * Equivalencia Teórica).
+ *   node_score: [n_req, N+1] fp32 (from dt_expand_depth).
+ *   sel:        [n_req, B] int32 out: the B non-root nodes with the largest
+ *               node_score + beta * depth, ties to the lower index, ascending. */
+dt_status dt_prune_topB(dt_ctx* ctx, const float* node_score, int32_t* sel, void* stream);
+
+/* Step 5 — compact tree and ancestor-only attention mask (DominoTree page,
+ * Verificación; DARTree page, Verificación).  Tree slot 0 is the root, slots
+ * 1..B the selected nodes in ascending node order.
+ *   sel, node_tok, node_parent, node_score: inputs from steps 3-4.
+ *   tok, parent, depth: [n_req, B+1] int32 out (parent = slot of the parent,
+ *   -1 for the root); logp_cum: [n_req, B+1] fp32 out (cumulative score);
+ *   mask: [n_req, B+1, B+1] uint8 out, mask[a][b] = 1 iff slot b is slot a or
+ *   one of its ancestors.  A parent missing from the selection (impossible for
+ *   beta <= 0) is recorded in the device status word. */
+dt_status dt_tree_mask(dt_ctx* ctx, const int32_t* sel, const int32_t* node_tok,
+                       const int32_t* node_parent, const float* node_score, int32_t* tok,
+                       int32_t* parent, int32_t* depth, float* logp_cum, uint8_t* mask,
+                       void* stream);
+
+/* --------------------------------------------------------------------------
+ * Whole round.
+ * ------------------------------------------------------------------------ */
+
+/* Steps 1-5 for one round as one CUDA-graph replay on `stream`.  The graph is
+ * captured on the first call with a given set of pointer arguments; the
+ * context keeps up to 16 captured rounds (least recently used is replaced).
+ * H and root_tok as above; outputs as dt_tree_mask.  Intermediate arrays stay
+ * in the workspace. */
+dt_status dt_build_round(dt_ctx* ctx, const void* H, const int32_t* root_tok, int32_t* tok,
+                         int32_t* parent, int32_t* depth, float* logp_cum, uint8_t* mask,
+                         void* stream);
+
+/* dt_build_round with HOST buffers: copies H (bf16, [n_req, block, d]) and
+ * root_tok to the device, replays the round, copies the outputs back and
+ * synchronises `stream`.  Host buffers should be pinned for full speed. */
+dt_status dt_build_round_host(dt_ctx* ctx, const void* H_host, const int32_t* root_host,
+                              int32_t* tok_host, int32_t* parent_host, int32_t* depth_host,
+                              float* logp_cum_host, uint8_t* mask_host, void* stream);
+
+/* Synchronise the context's last stream and read (and clear) its device status
+ * word: DT_OK, DT_ERR_TIMEOUT or DT_ERR_DEVICE. */
+dt_status dt_get_device_status(dt_ctx* ctx);
+
+/* Number of kernel launches one dt_build_round replay performs. */
+int dt_round_kernel_count(const dt_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTREE_H_ */
