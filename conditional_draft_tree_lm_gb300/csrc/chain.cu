@@ -8,22 +8,25 @@
 // columns, and keeps in shared memory, for the whole launch, the bf16 weight
 // columns that produce them: the three GRU gate rows of W_hh for each j in J
 // and the S-half of W1 for each row in R.  Per depth:
-//   A  u = S(p) [W_hh(J gates) | W1_S(R)]^T for every live branch p (fp32 SIMT
-//      from shared-memory weights); the W1_S part goes to global memory.
-//   -- grid barrier --
-//   B  every CTA (identically): z = SiLU(h1_i + u_W1), lambda_c = (base_c +
-//      z . W2[c]) / T on the Top-M candidates, logp = lambda - logsumexp(rest,
-//      lambda), per-branch top-K (ties to the lower token id), children sorted
-//      by token id, top-W of the depth by cumulative score (ties to the lower
-//      node index).  CTA 0 writes the node arrays and the live list.
-//   C  GRU update of the survivors' state columns J:
-//      r = sigmoid(x_r + u_r), z = sigmoid(x_z + u_z), n = tanh(x_n + r u_n),
-//      h' = (1 - z) n + z h, with x = X[token] (the precomputed E W_ih^T + b_ih).
-//   -- grid barrier --
+//   pre  the depth's Top-M candidate tokens are read, and their base logits, W2
+//        rows, GRU-input slices X[token][gates of J] and the H-half h1_i of the
+//        bottleneck are copied to shared memory with cp.async, overlapping A.
+//   A    u = S(p) [W_hh(J gates) | W1_S(R)]^T for every live branch p: mma.sync
+//        m16n8k16 on the resident K-major bf16 weight columns, with each fp32
+//        state split into bf16 high + low parts (two products, fp32
+//        accumulation); the W1_S part goes to global memory.
+//   --   grid barrier
+//   B    every CTA (identically): z = SiLU(h1_i + u_W1), lambda_c = (base_c +
+//        z . W2[c]) / T on the Top-M candidates, logp = lambda - logsumexp(rest,
+//        lambda), per-branch top-K (ties to the lower token id), children
+//        sorted by token id, top-W of the depth by cumulative score (ties to the
+//        lower node index).  CTA 0 writes the node arrays and the live list.
+//   C    GRU update of the survivors' state columns J:
+//        r = sigmoid(x_r + u_r), z = sigmoid(x_z + u_z), n = tanh(x_n + r u_n),
+//        h' = (1 - z) n + z h, with x = X[token] = E[token] W_ih^T + b_ih.
+//   --   grid barrier
 // Every wait is bounded; on a timeout the kernel records DT_DEV_TIMEOUT and
 // returns.
-#include <cooperative_groups.h>
-
 #include "common.cuh"
 #include "kernels.h"
 
@@ -33,13 +36,44 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPC = 8;  // state rows per GEMM chunk
+constexpr int kPC = 8;           // state rows per projection chunk
+constexpr int kRankMax = 256;    // top-W by rank counting up to this many children
+constexpr int kMaxNTiles = 8;    // owned columns per CTA <= 64 (8-wide MMA tiles)
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16
+// mantissa bits, so two bf16 MMAs reproduce an fp32 operand to ~2^-17.
+DT_DEVINL uint32_t split_hi_lo(float a, float b, uint32_t& lo) {
+  const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
+  const __nv_bfloat16 al = __float2bfloat16_rn(a - __bfloat162float(ah));
+  const __nv_bfloat16 bl = __float2bfloat16_rn(b - __bfloat162float(bh));
+  lo = static_cast<uint32_t>(__bfloat16_as_ushort(al)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bl)) << 16);
+  return static_cast<uint32_t>(__bfloat16_as_ushort(ah)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bh)) << 16);
+}
+
+// D += A B for one m16n8k16 tile, bf16 inputs, fp32 accumulators.
+DT_DEVINL void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 DT_DEVINL unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+
+DT_DEVINL void cp_async16(void* s, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(s)), "l"(g) : "memory");
+}
+DT_DEVINL void cp_async4(void* s, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s)), "l"(g) : "memory");
+}
+DT_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+DT_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Grid-wide barrier on a monotonically increasing counter.  Returns false on
 // timeout (the status word is set).
@@ -72,21 +106,132 @@ DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_
 DT_DEVINL float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 struct Smem {
-  uint16_t* w;      // [g][cpad] bf16 owned weight columns
-  float* st;        // [g][kPC] transposed state chunk
+  uint16_t* w;      // [cpad][gp] bf16 owned weight columns, K-major
+  uint16_t* sh;     // [kPC][gp] bf16 high part of the state chunk
+  uint16_t* sl;     // [kPC][gp] bf16 low part (S - high)
   float* red;       // [kWarps][kPC][cpad]
   float* uu;        // [n_req*W][3*jper] owned GRU hidden projections
   float* z;         // [kWarps][r]
-  float* lam;       // [kWarps][M]
+  uint16_t* w2s;    // [M][r+8] staged W2 rows of the current request's candidates
+  float* xs;        // [M][3*jper] staged GRU-input slices of the candidates
+  int* ctk;         // [M] candidate tokens
+  float* cbs;       // [M] candidate base logits
+  float* h1s;       // [r]
+  float* rest;      // [1]
   int* ctok;        // [W*K] children of the current request: token
+  int* cslot;       // [W*K] candidate index of each child
   float* clogp;     // [W*K]
   float* cscore;    // [W*K]
   int* crank;       // [W*K]
+  uint64_t* wkey;   // [npad] top-W sort keys (wide trees)
   int* surv;        // [n_req][W] survivor child slot
   float* pscore;    // [W] parent scores of the current request
   int* pnode;       // [W] parent node indices of the current request
 };
 
+struct SmemSizes {
+  size_t off[20];
+  size_t total;
+};
+
+DT_HOST_DEVICE_INLINE size_t al16(size_t b) { return (b + 15) & ~static_cast<size_t>(15); }
+
+DT_HOST_DEVICE_INLINE int pow2_at_least(int n) {
+  int v = 1;
+  while (v < n) v <<= 1;
+  return v;
+}
+
+// Row stride (bf16 elements) of the K-major weight columns and of the state
+// rows in shared memory: g rounded up to whole k16 steps, plus 8 elements so
+// that consecutive rows start 4 banks apart (conflict-free fragment loads).
+DT_HOST_DEVICE_INLINE int kstride(int g) { return (g + 15) / 16 * 16 + 8; }
+
+DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const ChainParams& p) {
+  const size_t WK = static_cast<size_t>(p.W) * p.K;
+  const size_t gp = static_cast<size_t>(kstride(p.g));
+  const size_t sz[20] = {
+      gp * p.cpad * 2,
+      gp * kPC * 2 * 2,
+      static_cast<size_t>(kWarps) * kPC * p.cpad * 4,
+      static_cast<size_t>(p.n_req) * p.W * 3 * p.jper * 4,
+      static_cast<size_t>(kWarps) * p.r * 4,
+      p.stage_w2 ? static_cast<size_t>(p.M) * (p.r + 8) * 2 : 0,
+      static_cast<size_t>(p.M) * 3 * p.jper * 4,
+      static_cast<size_t>(p.M) * 4,
+      static_cast<size_t>(p.M) * 4,
+      static_cast<size_t>(p.r) * 4,
+      16,
+      WK * 4,
+      WK * 4,
+      WK * 4,
+      WK * 4,
+      WK * 4,
+      WK > static_cast<size_t>(kRankMax) ? static_cast<size_t>(pow2_at_least(static_cast<int>(WK))) * 8 : 0,
+      static_cast<size_t>(p.n_req) * p.W * 4,
+      static_cast<size_t>(p.W) * 4,
+      static_cast<size_t>(p.W) * 4,
+  };
+  SmemSizes s;
+  size_t o = 0;
+  for (int i = 0; i < 20; ++i) {
+    s.off[i] = o;
+    o += al16(sz[i]);
+  }
+  s.total = o;
+  return s;
+}
+
+// Read the candidate tokens of one (request, depth) row into shared memory.
+DT_DEVINL void load_cand_tokens(const ChainParams& p, const Smem& s, size_t qrow) {
+  for (int c = threadIdx.x; c < p.M; c += kThreads) {
+    int t = p.cand_tok[qrow * p.M + c];
+    if (t < 0 || t >= p.V) {
+      dt_report(p.status, DT_DEV_BOUNDS);
+      t = 0;
+    }
+    s.ctk[c] = t;
+  }
+}
+
+// Asynchronous copies of everything phase B/C read for one (request, depth) row.
+DT_DEVINL void stage_row(const ChainParams& p, const Smem& s, size_t qrow, int j0, int nj, bool want_x) {
+  const int r = p.r, M = p.M, g = p.g;
+  if (p.stage_w2) {
+    const int c8 = r / 8;
+    for (int idx = threadIdx.x; idx < M * c8; idx += kThreads) {
+      const int c = idx / c8, k = idx - c * c8;
+      cp_async16(s.w2s + static_cast<size_t>(c) * (r + 8) + k * 8,
+                 p.w2 + static_cast<size_t>(s.ctk[c]) * r + k * 8);
+    }
+  }
+  if (want_x && nj > 0) {
+    const int per = 3 * nj;
+    for (int idx = threadIdx.x; idx < M * per; idx += kThreads) {
+      const int c = idx / per, rem = idx - c * per;
+      const int gate = rem / nj, jj = rem - gate * nj;
+      cp_async4(s.xs + static_cast<size_t>(c) * 3 * p.jper + gate * nj + jj,
+                p.xtab + static_cast<size_t>(s.ctk[c]) * 3 * g + gate * g + j0 + jj);
+    }
+  }
+  for (int c = threadIdx.x; c < M; c += kThreads) cp_async4(s.cbs + c, p.cand_base + qrow * M + c);
+  for (int k = threadIdx.x; k < r; k += kThreads) cp_async4(s.h1s + k, p.h1 + qrow * r + k);
+  if (threadIdx.x == 0) cp_async4(s.rest, p.rest_lse + qrow);
+  cp_async_commit();
+}
+
+DT_DEVINL void fma8(float& acc, const float4& za, const float4& zb, const uint4& w8) {
+  acc = fmaf(za.x, __uint_as_float(w8.x << 16), acc);
+  acc = fmaf(za.y, __uint_as_float(w8.x & 0xFFFF0000u), acc);
+  acc = fmaf(za.z, __uint_as_float(w8.y << 16), acc);
+  acc = fmaf(za.w, __uint_as_float(w8.y & 0xFFFF0000u), acc);
+  acc = fmaf(zb.x, __uint_as_float(w8.z << 16), acc);
+  acc = fmaf(zb.y, __uint_as_float(w8.z & 0xFFFF0000u), acc);
+  acc = fmaf(zb.z, __uint_as_float(w8.w << 16), acc);
+  acc = fmaf(zb.w, __uint_as_float(w8.w & 0xFFFF0000u), acc);
+}
+
+template <int MPL>
 __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int s_abort;
@@ -102,39 +247,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
 
   Smem s;
   {
-    uint8_t* q = smem_raw;
-    auto take = [&](size_t bytes) {
-      uint8_t* o = q;
-      q += (bytes + 15) & ~static_cast<size_t>(15);
-      return o;
-    };
-    s.w = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(g) * cpad * 2));
-    s.st = reinterpret_cast<float*>(take(static_cast<size_t>(g) * kPC * 4));
-    s.red = reinterpret_cast<float*>(take(static_cast<size_t>(kWarps) * kPC * cpad * 4));
-    s.uu = reinterpret_cast<float*>(take(static_cast<size_t>(p.n_req) * W * 3 * p.jper * 4));
-    s.z = reinterpret_cast<float*>(take(static_cast<size_t>(kWarps) * r * 4));
-    s.lam = reinterpret_cast<float*>(take(static_cast<size_t>(kWarps) * M * 4));
-    s.ctok = reinterpret_cast<int*>(take(static_cast<size_t>(W) * K * 4));
-    s.clogp = reinterpret_cast<float*>(take(static_cast<size_t>(W) * K * 4));
-    s.cscore = reinterpret_cast<float*>(take(static_cast<size_t>(W) * K * 4));
-    s.crank = reinterpret_cast<int*>(take(static_cast<size_t>(W) * K * 4));
-    s.surv = reinterpret_cast<int*>(take(static_cast<size_t>(p.n_req) * W * 4));
-    s.pscore = reinterpret_cast<float*>(take(static_cast<size_t>(W) * 4));
-    s.pnode = reinterpret_cast<int*>(take(static_cast<size_t>(W) * 4));
+    const SmemSizes L = smem_sizes(p);
+    s.w = reinterpret_cast<uint16_t*>(smem_raw + L.off[0]);
+    s.sh = reinterpret_cast<uint16_t*>(smem_raw + L.off[1]);
+    s.sl = s.sh + static_cast<size_t>(kPC) * kstride(g);
+    s.red = reinterpret_cast<float*>(smem_raw + L.off[2]);
+    s.uu = reinterpret_cast<float*>(smem_raw + L.off[3]);
+    s.z = reinterpret_cast<float*>(smem_raw + L.off[4]);
+    s.w2s = reinterpret_cast<uint16_t*>(smem_raw + L.off[5]);
+    s.xs = reinterpret_cast<float*>(smem_raw + L.off[6]);
+    s.ctk = reinterpret_cast<int*>(smem_raw + L.off[7]);
+    s.cbs = reinterpret_cast<float*>(smem_raw + L.off[8]);
+    s.h1s = reinterpret_cast<float*>(smem_raw + L.off[9]);
+    s.rest = reinterpret_cast<float*>(smem_raw + L.off[10]);
+    s.ctok = reinterpret_cast<int*>(smem_raw + L.off[11]);
+    s.cslot = reinterpret_cast<int*>(smem_raw + L.off[12]);
+    s.clogp = reinterpret_cast<float*>(smem_raw + L.off[13]);
+    s.cscore = reinterpret_cast<float*>(smem_raw + L.off[14]);
+    s.crank = reinterpret_cast<int*>(smem_raw + L.off[15]);
+    s.wkey = reinterpret_cast<uint64_t*>(smem_raw + L.off[16]);
+    s.surv = reinterpret_cast<int*>(smem_raw + L.off[17]);
+    s.pscore = reinterpret_cast<float*>(smem_raw + L.off[18]);
+    s.pnode = reinterpret_cast<int*>(smem_raw + L.off[19]);
   }
 
-  // ---- load the owned weight columns (transposed: s.w[k][c]) ----
-  for (int idx = tid; idx < cpad * g; idx += kThreads) {
-    const int c = idx / g, k = idx - c * g;
-    uint16_t v = 0;
-    if (c < 3 * nj) {
-      const int gate = c / nj, jj = c - gate * nj;
-      v = p.w_hh[static_cast<size_t>(gate * g + j0 + jj) * g + k];
-    } else if (c < ncol) {
-      const int rr = r0 + (c - 3 * nj);
-      v = p.w1[static_cast<size_t>(rr) * p.ldw1 + p.d + k];
+  // ---- the owned weight columns, K-major: s.w[c][k] (zero padded) ----
+  const int gp = kstride(g);
+  {
+    const int g8 = gp / 8;  // 16-byte chunks per padded row
+    for (int idx = tid; idx < cpad * g8; idx += kThreads) {
+      const int c = idx / g8, k8 = idx - c * g8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (8 * k8 < g) {
+        if (c < 3 * nj) {
+          const int gate = c / nj, jj = c - gate * nj;
+          v = *reinterpret_cast<const uint4*>(p.w_hh + static_cast<size_t>(gate * g + j0 + jj) * g + 8 * k8);
+        } else if (c < ncol) {
+          const int rr = r0 + (c - 3 * nj);
+          v = *reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(rr) * p.ldw1 + p.d + 8 * k8);
+        }
+      }
+      *reinterpret_cast<uint4*>(s.w + static_cast<size_t>(c) * gp + 8 * k8) = v;
     }
-    s.w[k * cpad + c] = v;
   }
 
   unsigned epoch = 0;
@@ -144,7 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     for (int idx = tid; idx < p.n_req * nj; idx += kThreads) {
       const int q = idx / nj, jj = j0 + (idx - q * nj);
       int tok = p.root_tok[q];
-      if (tok < 0 || tok >= p.V) { dt_report(p.status, DT_DEV_BOUNDS); tok = 0; }
+      if (tok < 0 || tok >= p.V) {
+        dt_report(p.status, DT_DEV_BOUNDS);
+        tok = 0;
+      }
       const float* x = p.xtab + static_cast<size_t>(tok) * 3 * g;
       const float zg = sigmoidf_(x[g + jj]);
       const float ng = tanhf(x[2 * g + jj]);
@@ -164,51 +321,78 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   }
 
   for (int i = p.depth_first; i <= p.depth_last; ++i) {
-    const int Lp = p.L[i - 1];          // live branches entering this depth
-    const int Li = p.L[i];              // branches that live on
+    const int Lp = p.L[i - 1];  // live branches entering this depth
+    const int Li = p.L[i];      // branches that live on
     const int P = p.n_req * Lp;
+    const bool last = i == p.D;
     const float* Sprev = p.S + static_cast<size_t>((i - 1) & 1) * p.n_req * W * g;
     float* Snext = p.S + static_cast<size_t>(i & 1) * p.n_req * W * g;
     const int* live_prev = p.live + static_cast<size_t>((i - 1) & 1) * p.n_req * W;
     int* live_next = p.live + static_cast<size_t>(i & 1) * p.n_req * W;
 
+    // ---- pre: stage request 0 of this depth (overlaps phase A) ----
+    __syncthreads();
+    load_cand_tokens(p, s, static_cast<size_t>(i - 1));
+    __syncthreads();
+    stage_row(p, s, static_cast<size_t>(i - 1), j0, nj, !last);
+
     // ================= phase A: projections of the live states ==============
     for (int p0 = 0; p0 < P; p0 += kPC) {
       const int pc = min(kPC, P - p0);
       __syncthreads();
-      for (int idx = tid; idx < kPC * g; idx += kThreads) {
-        const int pp = idx / g, k = idx - pp * g;
-        float v = 0.0f;
-        if (pp < pc) {
+      // state rows -> bf16 high + low parts (S = hi + lo to ~16 mantissa bits)
+      const int gp4 = gp / 4;
+      for (int idx = tid; idx < kPC * gp4; idx += kThreads) {
+        const int pp = idx / gp4, k4 = idx - pp * gp4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (pp < pc && 4 * k4 < g) {
           const int pr = p0 + pp;
           const int q = pr / Lp, b = pr - q * Lp;
-          v = Sprev[static_cast<size_t>(q * W + b) * g + k];
+          v = *reinterpret_cast<const float4*>(Sprev + static_cast<size_t>(q * W + b) * g + 4 * k4);
         }
-        s.st[k * kPC + pp] = v;
+        uint2 hi, lo;
+        hi.x = split_hi_lo(v.x, v.y, lo.x);
+        hi.y = split_hi_lo(v.z, v.w, lo.y);
+        *reinterpret_cast<uint2*>(s.sh + static_cast<size_t>(pp) * gp + 4 * k4) = hi;
+        *reinterpret_cast<uint2*>(s.sl + static_cast<size_t>(pp) * gp + 4 * k4) = lo;
       }
       __syncthreads();
-      const int kper = (g + kWarps - 1) / kWarps;
-      const int k0 = warp * kper, k1 = min(g, k0 + kper);
-      for (int cg = 0; cg < cpad; cg += 32) {
-        float acc[kPC];
+      // u[pp][c] = sum_k S[pp][k] W[c][k]: mma.sync m16n8k16 (rows 8..15 zero),
+      // k16 steps split over the warps, two products (hi, lo) per step
+      {
+        const int gid = lane >> 2, tig = lane & 3;
+        const int nk16 = (g + 15) / 16;
+        float acc[kMaxNTiles][4];
 #pragma unroll
-        for (int j = 0; j < kPC; ++j) acc[j] = 0.0f;
-        const int c = cg + lane;
-        for (int k = k0; k < k1; ++k) {
-          const float wv = bf16_to_f32(s.w[k * cpad + c]);
-          const float4 a = *reinterpret_cast<const float4*>(&s.st[k * kPC]);
-          const float4 b = *reinterpret_cast<const float4*>(&s.st[k * kPC + 4]);
-          acc[0] = fmaf(wv, a.x, acc[0]);
-          acc[1] = fmaf(wv, a.y, acc[1]);
-          acc[2] = fmaf(wv, a.z, acc[2]);
-          acc[3] = fmaf(wv, a.w, acc[3]);
-          acc[4] = fmaf(wv, b.x, acc[4]);
-          acc[5] = fmaf(wv, b.y, acc[5]);
-          acc[6] = fmaf(wv, b.z, acc[6]);
-          acc[7] = fmaf(wv, b.w, acc[7]);
+        for (int nt = 0; nt < kMaxNTiles; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        const int ntiles = cpad / 8;
+        for (int kt = warp; kt < nk16; kt += kWarps) {
+          const int k0 = kt * 16 + 2 * tig;
+          const uint32_t ah0 = *reinterpret_cast<const uint32_t*>(s.sh + static_cast<size_t>(gid) * gp + k0);
+          const uint32_t ah2 = *reinterpret_cast<const uint32_t*>(s.sh + static_cast<size_t>(gid) * gp + k0 + 8);
+          const uint32_t al0 = *reinterpret_cast<const uint32_t*>(s.sl + static_cast<size_t>(gid) * gp + k0);
+          const uint32_t al2 = *reinterpret_cast<const uint32_t*>(s.sl + static_cast<size_t>(gid) * gp + k0 + 8);
+#pragma unroll
+          for (int nt = 0; nt < kMaxNTiles; ++nt) {
+            if (nt < ntiles) {
+              const uint16_t* wc = s.w + static_cast<size_t>(nt * 8 + gid) * gp + k0;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wc);
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wc + 8);
+              mma_bf16_16816(acc[nt], ah0, 0u, ah2, 0u, b0, b1);
+              mma_bf16_16816(acc[nt], al0, 0u, al2, 0u, b0, b1);
+            }
+          }
         }
 #pragma unroll
-        for (int j = 0; j < kPC; ++j) s.red[(warp * kPC + j) * cpad + c] = acc[j];
+        for (int nt = 0; nt < kMaxNTiles; ++nt) {
+          if (nt < ntiles) {
+            float* rw = s.red + (warp * kPC + gid) * cpad + nt * 8 + 2 * tig;
+            rw[0] = acc[nt][0];
+            rw[1] = acc[nt][1];
+          }
+        }
       }
       __syncthreads();
       for (int idx = tid; idx < pc * ncol; idx += kThreads) {
@@ -232,94 +416,125 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     const int nchild = Lp * K;
     for (int q = 0; q < p.n_req; ++q) {
       const size_t qrow = static_cast<size_t>(q) * p.D + (i - 1);
-      const float* h1 = p.h1 + qrow * r;
-      const int* ctok_g = p.cand_tok + qrow * M;
-      const float* cbase = p.cand_base + qrow * M;
-      const float rest = p.rest_lse[qrow];
-      __syncthreads();
+      if (q > 0) {
+        __syncthreads();
+        load_cand_tokens(p, s, qrow);
+        __syncthreads();
+        stage_row(p, s, qrow, j0, nj, !last);
+      }
       for (int b = tid; b < Lp; b += kThreads) {
         const int node = live_prev[static_cast<size_t>(q) * W + b];
         s.pnode[b] = node;
         s.pscore[b] = (node >= 0 && node < p.N1) ? p.node_score[static_cast<size_t>(q) * p.N1 + node] : 0.0f;
       }
+      cp_async_wait_all();
       __syncthreads();
+      const float rest = s.rest[0];
       float* zw = s.z + warp * r;
-      float* lw = s.lam + warp * M;
       for (int b = warp; b < Lp; b += kWarps) {
         const float* u = p.uW1 + static_cast<size_t>(q * W + b) * r;
         for (int k = lane; k < r; k += 32) {
-          const float x = h1[k] + u[k];
+          const float x = s.h1s[k] + u[k];
           zw[k] = x / (1.0f + expf(-x));
         }
         __syncwarp();
-        float lmax = rest;
-        for (int c = lane; c < M; c += 32) {
-          int tok = ctok_g[c];
-          if (tok < 0 || tok >= p.V) { dt_report(p.status, DT_DEV_BOUNDS); tok = 0; }
-          const uint4* wrow = reinterpret_cast<const uint4*>(p.w2 + static_cast<size_t>(tok) * r);
-          float dot = 0.0f;
+        float acc[MPL];
+#pragma unroll
+        for (int j = 0; j < MPL; ++j) acc[j] = 0.0f;
+        if (p.stage_w2) {
           for (int k8 = 0; k8 < r / 8; ++k8) {
-            const uint4 w8 = __ldg(wrow + k8);
-            const float* zz = zw + k8 * 8;
-            dot = fmaf(zz[0], __uint_as_float(w8.x << 16), dot);
-            dot = fmaf(zz[1], __uint_as_float(w8.x & 0xFFFF0000u), dot);
-            dot = fmaf(zz[2], __uint_as_float(w8.y << 16), dot);
-            dot = fmaf(zz[3], __uint_as_float(w8.y & 0xFFFF0000u), dot);
-            dot = fmaf(zz[4], __uint_as_float(w8.z << 16), dot);
-            dot = fmaf(zz[5], __uint_as_float(w8.z & 0xFFFF0000u), dot);
-            dot = fmaf(zz[6], __uint_as_float(w8.w << 16), dot);
-            dot = fmaf(zz[7], __uint_as_float(w8.w & 0xFFFF0000u), dot);
+            const float4 za = *reinterpret_cast<const float4*>(zw + k8 * 8);
+            const float4 zb = *reinterpret_cast<const float4*>(zw + k8 * 8 + 4);
+#pragma unroll
+            for (int j = 0; j < MPL; ++j) {
+              const int c = lane + 32 * j;
+              if (c < M) {
+                const uint4 w8 = *reinterpret_cast<const uint4*>(s.w2s + static_cast<size_t>(c) * (r + 8) + k8 * 8);
+                fma8(acc[j], za, zb, w8);
+              }
+            }
           }
-          const float lam = (cbase[c] + dot) / p.T;
-          lw[c] = lam;
-          lmax = fmaxf(lmax, lam);
+        } else {
+          for (int k8 = 0; k8 < r / 8; ++k8) {
+            const float4 za = *reinterpret_cast<const float4*>(zw + k8 * 8);
+            const float4 zb = *reinterpret_cast<const float4*>(zw + k8 * 8 + 4);
+#pragma unroll
+            for (int j = 0; j < MPL; ++j) {
+              const int c = lane + 32 * j;
+              if (c < M) {
+                const uint4 w8 =
+                    __ldg(reinterpret_cast<const uint4*>(p.w2 + static_cast<size_t>(s.ctk[c]) * r) + k8);
+                fma8(acc[j], za, zb, w8);
+              }
+            }
+          }
+        }
+        float lam[MPL];
+        float lmax = rest;
+#pragma unroll
+        for (int j = 0; j < MPL; ++j) {
+          const int c = lane + 32 * j;
+          lam[j] = c < M ? (s.cbs[c] + acc[j]) / p.T : -INFINITY;
+          lmax = fmaxf(lmax, lam[j]);
         }
         lmax = warp_max(lmax);
         float se = 0.0f;
-        for (int c = lane; c < M; c += 32) se += expf(lw[c] - lmax);
+#pragma unroll
+        for (int j = 0; j < MPL; ++j)
+          if (lane + 32 * j < M) se += expf(lam[j] - lmax);
         se = warp_sum(se);
-        if (lane == 0) se += expf(rest - lmax);
-        se = __shfl_sync(0xFFFFFFFFu, se, 0);
+        se += expf(rest - lmax);
         const float logZ = lmax + logf(se);
-        // top-K by (logp desc, token asc): K rounds of warp argmax
-        int my_tok = 0;
+        // top-K by (logp desc, token asc): K rounds of warp argmax over register keys
+        uint64_t key[MPL];
+        float lp[MPL];
+#pragma unroll
+        for (int j = 0; j < MPL; ++j) {
+          const int c = lane + 32 * j;
+          lp[j] = lam[j] - logZ;
+          key[j] = c < M ? rank_key(lp[j], static_cast<uint32_t>(s.ctk[c])) : 0ull;
+        }
+        int my_c = 0;
         float my_lp = 0.0f;
+        int my_tok = 0x7FFFFFFF;
         for (int kk = 0; kk < K; ++kk) {
           uint64_t best = 0;
-          for (int c = lane; c < M; c += 32) {
-            const float lam = lw[c];
-            if (lam == -INFINITY) continue;  // already taken
-            const uint64_t key = rank_key(lam - logZ, static_cast<uint32_t>(ctok_g[c]));
-            best = key > best ? key : best;
-          }
+#pragma unroll
+          for (int j = 0; j < MPL; ++j) best = key[j] > best ? key[j] : best;
           best = warp_max_u64(best);
-          const uint32_t wtok = rank_key_id(best);
-          // the lane holding the winner marks it taken and broadcasts logp
+          int wc = -1;
           float wlp = 0.0f;
-          int owner = -1;
-          for (int c = lane; c < M; c += 32)
-            if (static_cast<uint32_t>(ctok_g[c]) == wtok && lw[c] != -INFINITY) {
-              wlp = lw[c] - logZ;
-              lw[c] = -INFINITY;
-              owner = lane;
+#pragma unroll
+          for (int j = 0; j < MPL; ++j)
+            if (best != 0 && key[j] == best) {
+              wc = lane + 32 * j;
+              wlp = lp[j];
+              key[j] = 0;
             }
-          const unsigned om = __ballot_sync(0xFFFFFFFFu, owner >= 0);
-          const int src = om ? __ffs(om) - 1 : 0;
+          const unsigned own = __ballot_sync(0xFFFFFFFFu, wc >= 0);
+          const int src = own ? __ffs(own) - 1 : 0;
+          wc = __shfl_sync(0xFFFFFFFFu, wc, src);
           wlp = __shfl_sync(0xFFFFFFFFu, wlp, src);
           if (lane == kk) {
-            my_tok = static_cast<int>(wtok);
+            if (wc < 0 || wc >= M) {
+              dt_report(p.status, DT_DEV_BOUNDS);
+              wc = 0;
+            }
+            my_c = wc;
             my_lp = wlp;
+            my_tok = static_cast<int>(rank_key_id(best));
           }
         }
-        // children of branch b sorted by token id
+        // children of branch b, sorted by token id
         int rank = 0;
         for (int m = 0; m < K; ++m) {
           const int t = __shfl_sync(0xFFFFFFFFu, my_tok, m);
-          rank += (m < K && t < my_tok) ? 1 : 0;
+          rank += t < my_tok ? 1 : 0;
         }
         if (lane < K) {
           const int slot = b * K + rank;
           s.ctok[slot] = my_tok;
+          s.cslot[slot] = my_c;
           s.clogp[slot] = my_lp;
           s.cscore[slot] = s.pscore[b] + my_lp;
         }
@@ -336,45 +551,71 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           p.node_score[nb + e] = s.cscore[e];
         }
       }
-      if (i < p.D) {
-        // top-W of the depth: rank by (score desc, node index asc)
-        for (int e = tid; e < nchild; e += kThreads) {
-          const uint64_t ke = rank_key(s.cscore[e], static_cast<uint32_t>(e));
-          int rk = 0;
-          for (int f = 0; f < nchild; ++f) rk += rank_key(s.cscore[f], static_cast<uint32_t>(f)) > ke;
-          s.crank[e] = rk;
-        }
-        __syncthreads();
-        // survivors in ascending slot order
-        for (int e = tid; e < nchild; e += kThreads) {
-          if (s.crank[e] < Li) {
-            int pos = 0;
-            for (int f = 0; f < e; ++f) pos += s.crank[f] < Li;
-            s.surv[q * W + pos] = e;
-            if (blockIdx.x == 0) {
-              live_next[static_cast<size_t>(q) * W + pos] = row_off + e;
+      if (!last) {
+        // top-W of the depth by (score desc, node index asc); survivors ascending
+        if (nchild <= kRankMax) {
+          for (int e = tid; e < nchild; e += kThreads) {
+            const uint64_t ke = rank_key(s.cscore[e], static_cast<uint32_t>(e));
+            int rk = 0;
+            for (int f = 0; f < nchild; ++f) rk += rank_key(s.cscore[f], static_cast<uint32_t>(f)) > ke;
+            s.crank[e] = rk;
+          }
+          __syncthreads();
+          for (int e = tid; e < nchild; e += kThreads) {
+            if (s.crank[e] < Li) {
+              int pos = 0;
+              for (int f = 0; f < e; ++f) pos += s.crank[f] < Li;
+              s.surv[q * W + pos] = e;
             }
+          }
+        } else {
+          const int npad = pow2_at_least(nchild);
+          for (int e = tid; e < npad; e += kThreads)
+            s.wkey[e] = e < nchild ? rank_key(s.cscore[e], static_cast<uint32_t>(e)) : 0ull;
+          for (int k2 = 2; k2 <= npad; k2 <<= 1) {
+            for (int j = k2 >> 1; j > 0; j >>= 1) {
+              __syncthreads();
+              for (int x = tid; x < npad; x += kThreads) {
+                const int l = x ^ j;
+                if (l > x) {
+                  const uint64_t a = s.wkey[x], bb = s.wkey[l];
+                  const bool desc = (x & k2) == 0;
+                  if (desc ? (a < bb) : (a > bb)) {
+                    s.wkey[x] = bb;
+                    s.wkey[l] = a;
+                  }
+                }
+              }
+            }
+          }
+          __syncthreads();
+          // the first Li keys are the survivors; order them by slot
+          for (int a = tid; a < Li; a += kThreads) {
+            const int ea = static_cast<int>(rank_key_id(s.wkey[a]));
+            int pos = 0;
+            for (int b2 = 0; b2 < Li; ++b2) pos += static_cast<int>(rank_key_id(s.wkey[b2])) < ea;
+            s.surv[q * W + pos] = ea;
           }
         }
         __syncthreads();
-        if (blockIdx.x == 0 && p.live_out) {
-          for (int j = tid; j < W; j += kThreads)
-            p.live_out[static_cast<size_t>(q) * W + j] = j < Li ? row_off + s.surv[q * W + j] : -1;
+        if (blockIdx.x == 0) {
+          for (int j = tid; j < W; j += kThreads) {
+            const int node = j < Li ? row_off + s.surv[q * W + j] : -1;
+            if (j < Li) live_next[static_cast<size_t>(q) * W + j] = node;
+            if (p.live_out) p.live_out[static_cast<size_t>(q) * W + j] = node;
+          }
         }
         // ================= phase C (this request): GRU of the survivors ======
         for (int idx = tid; idx < Li * nj; idx += kThreads) {
           const int jv = idx / nj, jj = idx - jv * nj;
           const int e = s.surv[q * W + jv];
           const int b = e / K;
-          int tok = s.ctok[e];
-          if (tok < 0 || tok >= p.V) { dt_report(p.status, DT_DEV_BOUNDS); tok = 0; }
-          const float* x = p.xtab + static_cast<size_t>(tok) * 3 * g + j0 + jj;
+          const float* x = s.xs + static_cast<size_t>(s.cslot[e]) * 3 * p.jper;
           const float* uu = s.uu + static_cast<size_t>(q * Lp + b) * 3 * p.jper;
-          const float ur = uu[jj], uz = uu[nj + jj], un = uu[2 * nj + jj];
           const float h = Sprev[static_cast<size_t>(q * W + b) * g + j0 + jj];
-          const float rg = sigmoidf_(x[0] + ur);
-          const float zg = sigmoidf_(x[g] + uz);
-          const float ng = tanhf(x[2 * g] + rg * un);
+          const float rg = sigmoidf_(x[jj] + uu[jj]);
+          const float zg = sigmoidf_(x[nj + jj] + uu[nj + jj]);
+          const float ng = tanhf(x[2 * nj + jj] + rg * uu[2 * nj + jj]);
           Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = (1.0f - zg) * ng + zg * h;
         }
       } else if (blockIdx.x == 0 && p.live_out) {
@@ -387,45 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   }
 }
 
-}  // namespace
-
-int chain_grid(const ChainParams& p, int num_sms) {
-  // one CTA per 8 state columns, at most one per SM
-  int G = (p.g + 7) / 8;
-  if (G > num_sms) G = num_sms;
-  if (G < 1) G = 1;
-  return G;
-}
-
-size_t chain_smem_bytes(const ChainParams& p) {
-  auto al = [](size_t b) { return (b + 15) & ~static_cast<size_t>(15); };
-  size_t b = 0;
-  b += al(static_cast<size_t>(p.g) * p.cpad * 2);
-  b += al(static_cast<size_t>(p.g) * kPC * 4);
-  b += al(static_cast<size_t>(kWarps) * kPC * p.cpad * 4);
-  b += al(static_cast<size_t>(p.n_req) * p.W * 3 * p.jper * 4);
-  b += al(static_cast<size_t>(kWarps) * p.r * 4);
-  b += al(static_cast<size_t>(kWarps) * p.M * 4);
-  b += 4 * al(static_cast<size_t>(p.W) * p.K * 4);
-  b += al(static_cast<size_t>(p.n_req) * p.W * 4);
-  b += 2 * al(static_cast<size_t>(p.W) * 4);
-  return b;
-}
-
-void chain_plan(ChainParams& p, int grid) {
-  p.jper = (p.g + grid - 1) / grid;
-  p.rper = (p.r + grid - 1) / grid;
-  const int ncol = 3 * p.jper + p.rper;
-  p.cpad = (ncol + 31) / 32 * 32;
-}
-
-cudaError_t chain_prepare() {
-  return cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-}
-
-cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = chain_smem_bytes(p);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+template <int MPL>
+cudaError_t launch_mpl(const ChainParams& p, int grid, size_t smem, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -436,7 +640,46 @@ cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_chain, p);
+  return cudaLaunchKernelEx(&cfg, k_chain<MPL>, p);
+}
+
+}  // namespace
+
+int chain_grid(const ChainParams& p, int num_sms) {
+  // one CTA per 8 state columns, at most one per SM
+  int G = (p.g + 7) / 8;
+  if (G > num_sms) G = num_sms;
+  if (G < 1) G = 1;
+  return G;
+}
+
+size_t chain_smem_bytes(const ChainParams& p) { return smem_sizes(p).total; }
+
+void chain_plan(ChainParams& p, int grid) {
+  p.jper = (p.g + grid - 1) / grid;
+  p.rper = (p.r + grid - 1) / grid;
+  const int ncol = 3 * p.jper + p.rper;
+  p.cpad = (ncol + 31) / 32 * 32;
+  p.stage_w2 = 1;
+  if (smem_sizes(p).total > 200 * 1024) p.stage_w2 = 0;  // wide candidate sets read W2 from L2
+}
+
+cudaError_t chain_prepare() {
+  cudaError_t e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<2>));
+  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<4>));
+  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<8>));
+  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<16>));
+  return e;
+}
+
+cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = chain_smem_bytes(p);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  const int mpl = (p.M + 31) / 32;
+  if (mpl <= 2) return launch_mpl<2>(p, grid, smem, stream);
+  if (mpl <= 4) return launch_mpl<4>(p, grid, smem, stream);
+  if (mpl <= 8) return launch_mpl<8>(p, grid, smem, stream);
+  return launch_mpl<16>(p, grid, smem, stream);
 }
 
 }  // namespace dt

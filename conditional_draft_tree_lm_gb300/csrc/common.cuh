@@ -25,6 +25,19 @@ enum {
 #define DT_WAIT_LIMIT_NS 2000000000ull
 #endif
 
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in maximum
+// minus the kernel's own static shared memory.
+inline cudaError_t dt_allow_max_dynamic_smem(const void* func) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, func);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              optin - static_cast<int>(fa.sharedSizeBytes));
+}
+
 DT_DEVINL void dt_report(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

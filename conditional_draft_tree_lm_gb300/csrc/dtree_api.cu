@@ -60,7 +60,7 @@ dt_status check(const dt_config* c) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, cand_tok, cand_base, rest_lse, S,
+  size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, cand_tok, cand_base, rest_lse, row_done, S,
       uW1, live, node_tok, node_parent, node_logp, node_score, sel, bar, status, H_dev, root_dev,
       out_tok, out_parent, out_depth, out_logp, out_mask, total;
   size_t xtab;
@@ -85,6 +85,7 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   put(L.cand_tok, rows * c.M * 4);
   put(L.cand_base, rows * c.M * 4);
   put(L.rest_lse, rows * 4);
+  put(L.row_done, rows * 4);
   put(L.S, 2ull * c.n_req * c.W * c.g * 4);
   put(L.uW1, static_cast<size_t>(c.n_req) * c.W * c.r * 4);
   put(L.live, 2ull * c.n_req * c.W * 4);
@@ -146,8 +147,11 @@ struct dt_ctx {
 
 namespace {
 
-dt_status cuda_status(cudaError_t e) {
+thread_local char g_last_error[256] = "";
+
+dt_status cuda_status(cudaError_t e, const char* what = "") {
   if (e == cudaSuccess) return DT_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
   if (e == cudaErrorMemoryAllocation) return DT_ERR_OOM;
   return DT_ERR_CUDA;
 }
@@ -155,7 +159,7 @@ dt_status cuda_status(cudaError_t e) {
 #define DT_TRY(x)                                      \
   do {                                                 \
     cudaError_t _e = (x);                              \
-    if (_e != cudaSuccess) return cuda_status(_e);     \
+    if (_e != cudaSuccess) return cuda_status(_e, #x); \
   } while (0)
 
 dt_status enqueue_base_logits(dt_ctx* c, const void* H, float* logits, cudaStream_t st) {
@@ -313,6 +317,8 @@ size_t dt_workspace_bytes(const dt_config* cfg) {
   return L.total + L.xtab;
 }
 
+const char* dt_last_error(void) { return g_last_error; }
+
 const char* dt_status_string(dt_status s) {
   switch (s) {
     case DT_OK: return "ok";
@@ -350,7 +356,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   if (e == cudaSuccess) e = prune_prepare();
   if (e != cudaSuccess) {
     delete c;
-    return cuda_status(e);
+    return cuda_status(e, "dt_create: kernel attributes");
   }
   c->topm = TopmParams{};
   c->topm.V = cfg->V;
@@ -365,7 +371,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     dt_destroy(c);
-    return cuda_status(e);
+    return cuda_status(e, "dt_create: workspace allocation");
   }
   c->topm.part_id = c->at<int>(c->lay.part_id);
   c->topm.part_val = c->at<float>(c->lay.part_val);
@@ -375,6 +381,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->topm.cand_tok = c->at<int>(c->lay.cand_tok);
   c->topm.cand_base = c->at<float>(c->lay.cand_base);
   c->topm.rest_lse = c->at<float>(c->lay.rest_lse);
+  c->topm.row_done = c->at<unsigned>(c->lay.row_done);
   c->topm.status = c->at<int>(c->lay.status);
   c->logits_src = c->at<float>(c->lay.logits);
 
@@ -387,7 +394,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   probe.M = cfg->M;
   c->chain_grid = chain_grid(probe, c->num_sms);
   chain_plan(probe, c->chain_grid);
-  if (chain_smem_bytes(probe) > 227 * 1024) {
+  if (chain_smem_bytes(probe) > 227 * 1024 || probe.cpad > 64) {
     dt_destroy(c);
     return DT_ERR_SHAPE;
   }
@@ -422,7 +429,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   e = launch_gemm_tc(tm_emb, tm_emb, tm_wih, p, c->num_sms, st);
   if (e != cudaSuccess) {
     dt_destroy(c);
-    return cuda_status(e);
+    return cuda_status(e, "dt_create: GRU input table GEMM");
   }
   c->last_stream = st;
   *out = c;
@@ -605,7 +612,7 @@ dt_status dt_get_device_status(dt_ctx* c) {
 
 int dt_round_kernel_count(const dt_ctx* c) {
   (void)c;
-  return 6;  // LM head GEMM, Top-M partial + merge, depth chain, Top-B, tree/mask
+  return 5;  // LM head GEMM, Top-M, depth chain, Top-B, tree/mask
 }
 
 }  // extern "C"

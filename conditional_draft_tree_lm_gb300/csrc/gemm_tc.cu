@@ -245,7 +245,7 @@ size_t gemm_smem_bytes(const GemmParams& p) {
 }
 
 cudaError_t gemm_prepare() {
-  return cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  return dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_tc));
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_a2, const CUtensorMap& tm_b,

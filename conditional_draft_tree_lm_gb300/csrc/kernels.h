@@ -59,6 +59,7 @@ struct TopmParams {
   int* cand_tok;    // [rows, M]
   float* cand_base; // [rows, M]
   float* rest_lse;  // [rows]
+  unsigned* row_done;  // [rows] chunk arrival counters (zero between launches)
   int* status;
 };
 void topm_plan(TopmParams& p, int num_sms);
@@ -94,6 +95,7 @@ struct ChainParams {
   int depth_first, depth_last;
   int jper, rper;     // S / r columns owned per CTA
   int cpad;           // padded owned-column count (multiple of 32)
+  int stage_w2;       // 1: stage the candidates' W2 rows in shared memory
   int off[kMaxDepth + 1];  // first node index of depth i
   int nn[kMaxDepth + 1];   // nodes created at depth i
   int L[kMaxDepth + 1];    // branches that live after depth i (L[0] = 1)

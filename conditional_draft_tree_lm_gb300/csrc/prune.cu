@@ -32,7 +32,7 @@ DT_DEVINL int depth_of(const int* off, int D, int v) {
 
 __global__ void __launch_bounds__(kThreads) k_prune_topb(const PruneParams p) {
   extern __shared__ uint32_t keys[];  // [N1 - 1]
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[(kThreads / 32) * 256];  // one 256-bin histogram per warp
   __shared__ uint32_t state[4];
   __shared__ int scan_scratch[40];
   __shared__ int off[kMaxDepth + 2];
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kThreads) k_prune_topb(const PruneParams p) {
   __syncthreads();
   uint32_t t = 0;
   int need = n;
-  if (p.B < n) radix_select_kth_largest(keys, n, p.B, hist, state, t, need);
+  if (p.B < n) radix_select_kth_largest(keys, n, p.B, hist, static_cast<int>(sizeof(hist) / 4), state, t, need);
   const int seg = (n + blockDim.x - 1) / blockDim.x;
   const int s0 = min(n, static_cast<int>(threadIdx.x) * seg);
   const int s1 = min(n, s0 + seg);
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) k_tree_mask(const PruneParams p) {
 size_t prune_smem_bytes(const PruneParams& p) { return static_cast<size_t>(p.N1) * 4; }
 
 cudaError_t prune_prepare() {
-  return cudaFuncSetAttribute(k_prune_topb, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  return dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_prune_topb));
 }
 
 cudaError_t launch_prune(const PruneParams& p, cudaStream_t stream) {

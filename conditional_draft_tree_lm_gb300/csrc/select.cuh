@@ -39,31 +39,31 @@ DT_DEVINL int block_exclusive_scan(int v, int* scratch, int* total) {
 }
 
 // Radix select over keys[0, n) in shared memory: the k-th largest key
-// (1 <= k <= n).  On return every thread holds `t` (that key) and `need` (how
-// many keys equal to t belong to the top k: exactly k - #{key > t}).
-// `hist` holds 256 uint32, `state` holds 4 uint32 (shared memory).
-DT_DEVINL void radix_select_kth_largest(const uint32_t* keys, int n, int k, uint32_t* hist,
+// (1 <= k <= n), four passes of 8 bits.  `hist` holds `hist_words` uint32
+// (a multiple of 256): up to hist_words/256 warps count into histograms of
+// their own, further warps share them, so no access leaves the buffer.
+// On return every thread holds `t` (that key) and `need` (how many keys equal
+// to t belong to the top k: exactly k - #{key > t}).  `state` holds 4 uint32.
+DT_DEVINL void radix_select_kth_largest(const uint32_t* keys, int n, int k, uint32_t* hist, int hist_words,
                                         uint32_t* state, uint32_t& t, int& need) {
+  const int nh = max(1, hist_words / 256);
+  const int nwarps = min(static_cast<int>(blockDim.x >> 5), nh);
+  uint32_t* my = hist + ((threadIdx.x >> 5) % nwarps) * 256;
   uint32_t prefix = 0, pmask = 0;
   uint32_t kk = static_cast<uint32_t>(k);
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
+    for (int b = threadIdx.x; b < nwarps * 256; b += blockDim.x) hist[b] = 0;
     __syncthreads();
-    // warp-uniform trip count so every lane takes part in __match_any_sync
-    for (int base = 0; base < n; base += blockDim.x) {
-      const int e = base + threadIdx.x;
-      bool in = false;
-      uint32_t digit = 0;
-      if (e < n) {
-        const uint32_t key = keys[e];
-        in = (key & pmask) == prefix;
-        digit = (key >> shift) & 255u;
-      }
-      const unsigned grp = __match_any_sync(0xFFFFFFFFu, in ? digit : 0x100u + (threadIdx.x & 31));
-      if (in) {
-        const int leader = __ffs(grp) - 1;
-        if ((threadIdx.x & 31) == leader) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(grp)));
-      }
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const uint32_t key = keys[e];
+      if ((key & pmask) == prefix) atomicAdd(&my[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    // fold the per-warp histograms into warp 0's
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+      uint32_t s = 0;
+      for (int w = 0; w < nwarps; ++w) s += hist[w * 256 + b];
+      hist[b] = s;
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -90,7 +90,10 @@ DT_DEVINL void radix_select_kth_largest(const uint32_t* keys, int n, int k, uint
         int dsel = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (cum + c[j] >= kk) { dsel = 255 - 8 * lane - j; break; }
+          if (cum + c[j] >= kk) {
+            dsel = 255 - 8 * lane - j;
+            break;
+          }
           cum += c[j];
         }
         state[0] = static_cast<uint32_t>(dsel);

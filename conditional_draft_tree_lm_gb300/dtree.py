@@ -24,7 +24,10 @@ STATUS = {
 class DtreeError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)} ({status_string(status)})")
+        detail = ""
+        if status in (3, 4):
+            detail = " — " + load_library().dt_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status_string(status)}){detail}")
 
 
 class DtConfig(ctypes.Structure):
@@ -55,6 +58,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dt_node_count": (c_int64, [POINTER(DtConfig)]),
         "dt_workspace_bytes": (c_size_t, [POINTER(DtConfig)]),
         "dt_status_string": (c_char_p, [c_int]),
+        "dt_last_error": (c_char_p, []),
         "dt_create": (c_int, [POINTER(DtConfig), POINTER(DtWeights), vp, POINTER(c_void_p)]),
         "dt_destroy": (c_int, [vp]),
         "dt_base_logits": (c_int, [vp, vp, vp, vp]),

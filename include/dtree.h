@@ -111,6 +111,10 @@ size_t dt_workspace_bytes(const dt_config* cfg);
 /* Static description of a status code. */
 const char* dt_status_string(dt_status s);
 
+/* The CUDA call and error text behind the calling thread's last DT_ERR_CUDA /
+ * DT_ERR_OOM ("" if none).  Valid until the thread's next libdtree call. */
+const char* dt_last_error(void);
+
 /* --------------------------------------------------------------------------
  * Context.
  * ------------------------------------------------------------------------ */
