@@ -8,23 +8,28 @@
 // columns, and keeps in shared memory, for the whole launch, the bf16 weight
 // columns that produce them: the three GRU gate rows of W_hh for each j in J
 // and the S-half of W1 for each row in R.  Per depth:
-//   pre  the depth's Top-M candidate tokens are read, and their base logits, W2
-//        rows, GRU-input slices X[token][gates of J] and the H-half h1_i of the
-//        bottleneck are copied to shared memory with cp.async, overlapping A.
+//   pre  the depth's Top-M candidate tokens (read once per launch), and their
+//        base logits, W2 rows, GRU-input slices X[token][gates of J] and the
+//        H-half h1_i of the bottleneck are copied to shared memory with
+//        cp.async ahead of time, overlapping the barrier and phase A.
 //   A    u = S(p) [W_hh(J gates) | W1_S(R)]^T for every live branch p: mma.sync
 //        m16n8k16 on the resident K-major bf16 weight columns, with each fp32
 //        state split into bf16 high + low parts (two products, fp32
 //        accumulation); the W1_S part goes to global memory.
 //   --   grid barrier
-//   B    every CTA (identically): z = SiLU(h1_i + u_W1), lambda_c = (base_c +
-//        z . W2[c]) / T on the Top-M candidates, logp = lambda - logsumexp(rest,
-//        lambda), per-branch top-K (ties to the lower token id), children
-//        sorted by token id, top-W of the depth by cumulative score (ties to the
+//   B    every CTA (identically): z = SiLU(h1_i + u_W1); lambda_c = (base_c +
+//        z . W2[c]) / T on the Top-M candidates (one tensor-core product over
+//        all branches); logp = lambda - logsumexp(rest, lambda); per-branch
+//        top-K (ties to the lower token id) by rank counting; children sorted
+//        by token id; top-W of the depth by cumulative score (ties to the
 //        lower node index).  CTA 0 writes the node arrays and the live list.
 //   C    GRU update of the survivors' state columns J:
 //        r = sigmoid(x_r + u_r), z = sigmoid(x_z + u_z), n = tanh(x_n + r u_n),
 //        h' = (1 - z) n + z h, with x = X[token] = E[token] W_ih^T + b_ih.
 //   --   grid barrier
+// The kernel is instantiated twice over the same code: with every dimension
+// fixed at compile time for the Qwen3-4B shape (index arithmetic folds to
+// constants, loops unroll), and with dimensions read from the parameters.
 // Every wait is bounded; on a timeout the kernel records DT_DEV_TIMEOUT and
 // returns.
 #include "common.cuh"
@@ -37,8 +42,11 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPC = 8;           // state rows per projection chunk
-constexpr int kRankMax = 256;    // top-W by rank counting up to this many children
+constexpr int kRankMax = 256;    // top-W by rank counting up to this many children (= kThreads)
 constexpr int kMaxNTiles = 8;    // owned columns per CTA <= 64 (8-wide MMA tiles)
+constexpr int kSLoads = 9;       // float4 state loads per thread: kPC*(g+24)/4/kThreads for g <= 1024
+constexpr int kMaxR32 = 32;      // bottleneck values per lane: r <= 1024
+constexpr int kZLoads = 16;      // z values per thread on the tensor-core path: W*r <= 4096
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16
 // mantissa bits, so two bf16 MMAs reproduce an fp32 operand to ~2^-17.
@@ -75,14 +83,19 @@ DT_DEVINL void cp_async4(void* s, const void* g) {
 DT_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 DT_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Grid-wide barrier on a monotonically increasing counter.  Returns false on
+DT_DEVINL void red_release_add_u32(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier on a monotonically increasing counter: the CTA's writes are
+// ordered before thread 0's release-add by bar.sync, and every CTA's writes are
+// visible after the acquire-load that sees the full count.  Returns false on
 // timeout (the status word is set).
 DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_abort) {
   __syncthreads();
   ++epoch;
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(bar, 1u);
+    red_release_add_u32(bar, 1u);
     const unsigned target = epoch * gridDim.x;
     int abort = 0;
     if (ld_acquire_u32(bar) < target) {
@@ -96,7 +109,6 @@ DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_
         }
       }
     }
-    __threadfence();
     *s_abort = abort;
   }
   __syncthreads();
@@ -105,16 +117,41 @@ DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_
 
 DT_DEVINL float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// Dimensions a launch runs with (see chain_plan).
+struct Shape {
+  int g, r, M, K, W, n_req, D, jper, rper, cpad;
+  bool stage_w2, mma_b, prefetch;
+};
+
+// The candidate tokens of every depth of request 0 are read once, at launch.
+DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096; }
+
+DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
+  return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
+               prefetch_tokens(p.D, p.M)};
+}
+
+// Generic instantiation: every dimension from the launch parameters.
+struct DimsRuntime {
+  static DT_DEVINL Shape get(const ChainParams& p) { return runtime_shape(p); }
+};
+// The Qwen3-4B shape (g=1024, r=256, M=64, K=W=8, one request, depth 15, 128
+// CTAs): dimensions are literals, so the compiler folds the index arithmetic.
+struct DimsQ4B {
+  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true};
+  static DT_DEVINL Shape get(const ChainParams&) { return kShape; }
+};
+
 struct Smem {
   uint16_t* w;      // [cpad][gp] bf16 owned weight columns, K-major
   uint16_t* sh;     // [kPC][gp] bf16 high part of the state chunk
   uint16_t* sl;     // [kPC][gp] bf16 low part (S - high)
   float* red;       // [kWarps][kPC][cpad]
   float* uu;        // [n_req*W][3*jper] owned GRU hidden projections
-  float* z;         // [kWarps][r]
+  float* z;         // [kWarps][r] (SIMT phase B)
   uint16_t* w2s;    // [M][r+8] staged W2 rows of the current request's candidates
   float* xs;        // [M][3*jper] staged GRU-input slices of the candidates
-  int* ctk;         // [M] candidate tokens
+  int* ctk;         // [M] candidate tokens of the current row
   float* cbs;       // [M] candidate base logits
   float* h1s;       // [r]
   float* rest;      // [1]
@@ -122,15 +159,20 @@ struct Smem {
   int* cslot;       // [W*K] candidate index of each child
   float* clogp;     // [W*K]
   float* cscore;    // [W*K]
-  int* crank;       // [W*K]
-  uint64_t* wkey;   // [npad] top-W sort keys (wide trees)
+  int* crank;       // [W*K] top-K winners / ranks
+  uint64_t* wkey;   // [pow2 >= W*K] top-W keys
   int* surv;        // [n_req][W] survivor child slot
   float* pscore;    // [W] parent scores of the current request
   int* pnode;       // [W] parent node indices of the current request
+  int* tok_all;     // [D][M] candidate tokens of request 0 (when prefetched)
+  int* ctk_buf;     // the [M] scratch behind ctk when tokens are read per row
+  uint16_t* zh;     // [16*ceil(W/16)][r+8] bf16 high part of z (tensor-core phase B)
+  uint16_t* zl;     // same, low part
+  uint64_t* lamkey; // [W][M] (lambda, token) keys (tensor-core phase B)
 };
 
 struct SmemSizes {
-  size_t off[20];
+  size_t off[23];
   size_t total;
 };
 
@@ -147,34 +189,37 @@ DT_HOST_DEVICE_INLINE int pow2_at_least(int n) {
 // that consecutive rows start 4 banks apart (conflict-free fragment loads).
 DT_HOST_DEVICE_INLINE int kstride(int g) { return (g + 15) / 16 * 16 + 8; }
 
-DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const ChainParams& p) {
-  const size_t WK = static_cast<size_t>(p.W) * p.K;
-  const size_t gp = static_cast<size_t>(kstride(p.g));
-  const size_t sz[20] = {
-      gp * p.cpad * 2,
+DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
+  const size_t WK = static_cast<size_t>(sh.W) * sh.K;
+  const size_t gp = static_cast<size_t>(kstride(sh.g));
+  const size_t sz[23] = {
+      gp * sh.cpad * 2,
       gp * kPC * 2 * 2,
-      static_cast<size_t>(kWarps) * kPC * p.cpad * 4,
-      static_cast<size_t>(p.n_req) * p.W * 3 * p.jper * 4,
-      static_cast<size_t>(kWarps) * p.r * 4,
-      p.stage_w2 ? static_cast<size_t>(p.M) * (p.r + 8) * 2 : 0,
-      static_cast<size_t>(p.M) * 3 * p.jper * 4,
-      static_cast<size_t>(p.M) * 4,
-      static_cast<size_t>(p.M) * 4,
-      static_cast<size_t>(p.r) * 4,
+      static_cast<size_t>(kWarps) * kPC * sh.cpad * 4,
+      static_cast<size_t>(sh.n_req) * sh.W * 3 * sh.jper * 4,
+      sh.mma_b ? 0 : static_cast<size_t>(kWarps) * sh.r * 4,
+      sh.stage_w2 ? static_cast<size_t>(sh.M) * (sh.r + 8) * 2 : 0,
+      static_cast<size_t>(sh.M) * 3 * sh.jper * 4,
+      static_cast<size_t>(sh.M) * 4,
+      static_cast<size_t>(sh.M) * 4,
+      static_cast<size_t>(sh.r) * 4,
       16,
       WK * 4,
       WK * 4,
       WK * 4,
       WK * 4,
       WK * 4,
-      WK > static_cast<size_t>(kRankMax) ? static_cast<size_t>(pow2_at_least(static_cast<int>(WK))) * 8 : 0,
-      static_cast<size_t>(p.n_req) * p.W * 4,
-      static_cast<size_t>(p.W) * 4,
-      static_cast<size_t>(p.W) * 4,
+      static_cast<size_t>(pow2_at_least(static_cast<int>(WK))) * 8,
+      static_cast<size_t>(sh.n_req) * sh.W * 4,
+      static_cast<size_t>(sh.W) * 4,
+      static_cast<size_t>(sh.W) * 4,
+      sh.prefetch ? static_cast<size_t>(sh.D) * sh.M * 4 : 0,
+      sh.mma_b ? static_cast<size_t>(2 * 16 * ((sh.W + 15) / 16)) * (sh.r + 8) * 2 : 0,
+      sh.mma_b ? static_cast<size_t>(sh.W) * sh.M * 8 : 0,
   };
   SmemSizes s;
   size_t o = 0;
-  for (int i = 0; i < 20; ++i) {
+  for (int i = 0; i < 23; ++i) {
     s.off[i] = o;
     o += al16(sz[i]);
   }
@@ -183,9 +228,9 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const ChainParams& p) {
 }
 
 // Read the candidate tokens of one (request, depth) row into shared memory.
-DT_DEVINL void load_cand_tokens(const ChainParams& p, const Smem& s, size_t qrow) {
-  for (int c = threadIdx.x; c < p.M; c += kThreads) {
-    int t = p.cand_tok[qrow * p.M + c];
+DT_DEVINL void load_cand_tokens(const ChainParams& p, const Shape& sh, const Smem& s, size_t qrow) {
+  for (int c = threadIdx.x; c < sh.M; c += kThreads) {
+    int t = p.cand_tok[qrow * sh.M + c];
     if (t < 0 || t >= p.V) {
       dt_report(p.status, DT_DEV_BOUNDS);
       t = 0;
@@ -194,10 +239,23 @@ DT_DEVINL void load_cand_tokens(const ChainParams& p, const Smem& s, size_t qrow
   }
 }
 
+// Point s.ctk at the candidate tokens of (request q, depth i): the launch-time
+// prefetch for request 0, else read into the scratch row.  Whole CTA; the
+// caller synchronises before the tokens are used.
+DT_DEVINL void select_row_tokens(const ChainParams& p, const Shape& sh, Smem& s, int q, int i) {
+  if (q == 0 && sh.prefetch) {
+    s.ctk = s.tok_all + static_cast<size_t>(i - 1) * sh.M;
+  } else {
+    s.ctk = s.ctk_buf;
+    load_cand_tokens(p, sh, s, static_cast<size_t>(q) * sh.D + (i - 1));
+  }
+}
+
 // Asynchronous copies of everything phase B/C read for one (request, depth) row.
-DT_DEVINL void stage_row(const ChainParams& p, const Smem& s, size_t qrow, int j0, int nj, bool want_x) {
-  const int r = p.r, M = p.M, g = p.g;
-  if (p.stage_w2) {
+DT_DEVINL void stage_row(const ChainParams& p, const Shape& sh, const Smem& s, size_t qrow, int j0, int nj,
+                         bool want_x) {
+  const int r = sh.r, M = sh.M, g = sh.g;
+  if (sh.stage_w2) {
     const int c8 = r / 8;
     for (int idx = threadIdx.x; idx < M * c8; idx += kThreads) {
       const int c = idx / c8, k = idx - c * c8;
@@ -210,7 +268,7 @@ DT_DEVINL void stage_row(const ChainParams& p, const Smem& s, size_t qrow, int j
     for (int idx = threadIdx.x; idx < M * per; idx += kThreads) {
       const int c = idx / per, rem = idx - c * per;
       const int gate = rem / nj, jj = rem - gate * nj;
-      cp_async4(s.xs + static_cast<size_t>(c) * 3 * p.jper + gate * nj + jj,
+      cp_async4(s.xs + static_cast<size_t>(c) * 3 * sh.jper + gate * nj + jj,
                 p.xtab + static_cast<size_t>(s.ctk[c]) * 3 * g + gate * g + j0 + jj);
     }
   }
@@ -231,23 +289,25 @@ DT_DEVINL void fma8(float& acc, const float4& za, const float4& zb, const uint4&
   acc = fmaf(zb.w, __uint_as_float(w8.w & 0xFFFF0000u), acc);
 }
 
-template <int MPL>
+template <int MPL, class Dm>
 __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int s_abort;
+  __shared__ int s_wcnt[kWarps];
 
-  const int g = p.g, r = p.r, M = p.M, K = p.K, W = p.W;
+  const Shape sh = Dm::get(p);
+  const int g = sh.g, r = sh.r, M = sh.M, K = sh.K, W = sh.W, n_req = sh.n_req, D = sh.D;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int j0 = blockIdx.x * p.jper;
-  const int nj = max(0, min(g, j0 + p.jper) - j0);
-  const int r0 = blockIdx.x * p.rper;
-  const int nr = max(0, min(r, r0 + p.rper) - r0);
+  const int j0 = blockIdx.x * sh.jper;
+  const int nj = max(0, min(g, j0 + sh.jper) - j0);
+  const int r0 = blockIdx.x * sh.rper;
+  const int nr = max(0, min(r, r0 + sh.rper) - r0);
   const int ncol = 3 * nj + nr;
-  const int cpad = p.cpad;
+  const int cpad = sh.cpad;
 
   Smem s;
   {
-    const SmemSizes L = smem_sizes(p);
+    const SmemSizes L = smem_sizes(sh);
     s.w = reinterpret_cast<uint16_t*>(smem_raw + L.off[0]);
     s.sh = reinterpret_cast<uint16_t*>(smem_raw + L.off[1]);
     s.sl = s.sh + static_cast<size_t>(kPC) * kstride(g);
@@ -269,6 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     s.surv = reinterpret_cast<int*>(smem_raw + L.off[17]);
     s.pscore = reinterpret_cast<float*>(smem_raw + L.off[18]);
     s.pnode = reinterpret_cast<int*>(smem_raw + L.off[19]);
+    s.tok_all = reinterpret_cast<int*>(smem_raw + L.off[20]);
+    s.ctk_buf = s.ctk;
+    s.zh = reinterpret_cast<uint16_t*>(smem_raw + L.off[21]);
+    s.zl = s.zh + static_cast<size_t>(16 * ((W + 15) / 16)) * (r + 8);
+    s.lamkey = reinterpret_cast<uint64_t*>(smem_raw + L.off[22]);
   }
 
   // ---- the owned weight columns, K-major: s.w[c][k] (zero padded) ----
@@ -291,11 +356,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     }
   }
 
+  // ---- candidate tokens of every depth of request 0, read once ----
+  if (sh.prefetch) {
+    for (int idx = tid; idx < D * M; idx += kThreads) {
+      int t = p.cand_tok[idx];  // request 0 owns rows 0..D-1
+      if (t < 0 || t >= p.V) {
+        dt_report(p.status, DT_DEV_BOUNDS);
+        t = 0;
+      }
+      s.tok_all[idx] = t;
+    }
+  }
+  __syncthreads();
+  // stage the first depth's request 0 (overlaps the root step and phase A)
+  select_row_tokens(p, sh, s, 0, p.depth_first);
+  __syncthreads();
+  stage_row(p, sh, s, static_cast<size_t>(p.depth_first - 1), j0, nj, p.depth_first != D);
+
   unsigned epoch = 0;
 
   // ---- depth 0: root state and root node ----
   if (p.depth_first == 1) {
-    for (int idx = tid; idx < p.n_req * nj; idx += kThreads) {
+    for (int idx = tid; idx < n_req * nj; idx += kThreads) {
       const int q = idx / nj, jj = j0 + (idx - q * nj);
       int tok = p.root_tok[q];
       if (tok < 0 || tok >= p.V) {
@@ -308,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       p.S[static_cast<size_t>(q * W) * g + jj] = (1.0f - zg) * ng;
     }
     if (blockIdx.x == 0) {
-      for (int q = tid; q < p.n_req; q += kThreads) {
+      for (int q = tid; q < n_req; q += kThreads) {
         const size_t b = static_cast<size_t>(q) * p.N1;
         p.node_tok[b] = p.root_tok[q];
         p.node_parent[b] = -1;
@@ -323,38 +405,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   for (int i = p.depth_first; i <= p.depth_last; ++i) {
     const int Lp = p.L[i - 1];  // live branches entering this depth
     const int Li = p.L[i];      // branches that live on
-    const int P = p.n_req * Lp;
-    const bool last = i == p.D;
-    const float* Sprev = p.S + static_cast<size_t>((i - 1) & 1) * p.n_req * W * g;
-    float* Snext = p.S + static_cast<size_t>(i & 1) * p.n_req * W * g;
-    const int* live_prev = p.live + static_cast<size_t>((i - 1) & 1) * p.n_req * W;
-    int* live_next = p.live + static_cast<size_t>(i & 1) * p.n_req * W;
-
-    // ---- pre: stage request 0 of this depth (overlaps phase A) ----
-    __syncthreads();
-    load_cand_tokens(p, s, static_cast<size_t>(i - 1));
-    __syncthreads();
-    stage_row(p, s, static_cast<size_t>(i - 1), j0, nj, !last);
+    const int P = n_req * Lp;
+    const bool last = i == D;
+    const float* Sprev = p.S + static_cast<size_t>((i - 1) & 1) * n_req * W * g;
+    float* Snext = p.S + static_cast<size_t>(i & 1) * n_req * W * g;
+    const int* live_prev = p.live + static_cast<size_t>((i - 1) & 1) * n_req * W;
+    int* live_next = p.live + static_cast<size_t>(i & 1) * n_req * W;
 
     // ================= phase A: projections of the live states ==============
     for (int p0 = 0; p0 < P; p0 += kPC) {
       const int pc = min(kPC, P - p0);
       __syncthreads();
       // state rows -> bf16 high + low parts (S = hi + lo to ~16 mantissa bits)
+      // (every load of the thread is issued before the first use: one L2 round trip)
       const int gp4 = gp / 4;
-      for (int idx = tid; idx < kPC * gp4; idx += kThreads) {
+      float4 v[kSLoads];
+#pragma unroll
+      for (int j = 0; j < kSLoads; ++j) {
+        const int idx = tid + j * kThreads;
         const int pp = idx / gp4, k4 = idx - pp * gp4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (pp < pc && 4 * k4 < g) {
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < kPC * gp4 && pp < pc && 4 * k4 < g) {
           const int pr = p0 + pp;
           const int q = pr / Lp, b = pr - q * Lp;
-          v = *reinterpret_cast<const float4*>(Sprev + static_cast<size_t>(q * W + b) * g + 4 * k4);
+          v[j] = *reinterpret_cast<const float4*>(Sprev + static_cast<size_t>(q * W + b) * g + 4 * k4);
         }
-        uint2 hi, lo;
-        hi.x = split_hi_lo(v.x, v.y, lo.x);
-        hi.y = split_hi_lo(v.z, v.w, lo.y);
-        *reinterpret_cast<uint2*>(s.sh + static_cast<size_t>(pp) * gp + 4 * k4) = hi;
-        *reinterpret_cast<uint2*>(s.sl + static_cast<size_t>(pp) * gp + 4 * k4) = lo;
+      }
+#pragma unroll
+      for (int j = 0; j < kSLoads; ++j) {
+        const int idx = tid + j * kThreads;
+        if (idx < kPC * gp4) {
+          const int pp = idx / gp4, k4 = idx - pp * gp4;
+          uint2 hi, lo;
+          hi.x = split_hi_lo(v[j].x, v[j].y, lo.x);
+          hi.y = split_hi_lo(v[j].z, v[j].w, lo.y);
+          *reinterpret_cast<uint2*>(s.sh + static_cast<size_t>(pp) * gp + 4 * k4) = hi;
+          *reinterpret_cast<uint2*>(s.sl + static_cast<size_t>(pp) * gp + 4 * k4) = lo;
+        }
       }
       __syncthreads();
       // u[pp][c] = sum_k S[pp][k] W[c][k]: mma.sync m16n8k16 (rows 8..15 zero),
@@ -402,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         for (int w8 = 0; w8 < kWarps; ++w8) sum += s.red[(w8 * kPC + pp) * cpad + c];
         const int pr = p0 + pp;
         if (c < 3 * nj) {
-          s.uu[static_cast<size_t>(pr) * 3 * p.jper + c] = sum;
+          s.uu[static_cast<size_t>(pr) * 3 * sh.jper + c] = sum;
         } else {
           const int q = pr / Lp, b = pr - q * Lp;
           p.uW1[static_cast<size_t>(q * W + b) * r + r0 + (c - 3 * nj)] = sum;
@@ -414,13 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     // ================= phase B: corrected log-probs and selections ==========
     const int row_off = p.off[i];
     const int nchild = Lp * K;
-    for (int q = 0; q < p.n_req; ++q) {
-      const size_t qrow = static_cast<size_t>(q) * p.D + (i - 1);
+    for (int q = 0; q < n_req; ++q) {
+      const size_t qrow = static_cast<size_t>(q) * D + (i - 1);
       if (q > 0) {
         __syncthreads();
-        load_cand_tokens(p, s, qrow);
+        select_row_tokens(p, sh, s, q, i);
         __syncthreads();
-        stage_row(p, s, qrow, j0, nj, !last);
+        stage_row(p, sh, s, qrow, j0, nj, !last);
       }
       for (int b = tid; b < Lp; b += kThreads) {
         const int node = live_prev[static_cast<size_t>(q) * W + b];
@@ -430,31 +517,131 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       cp_async_wait_all();
       __syncthreads();
       const float rest = s.rest[0];
-      float* zw = s.z + warp * r;
-      for (int b = warp; b < Lp; b += kWarps) {
-        const float* u = p.uW1 + static_cast<size_t>(q * W + b) * r;
-        for (int k = lane; k < r; k += 32) {
-          const float x = s.h1s[k] + u[k];
-          zw[k] = x / (1.0f + expf(-x));
+      if (sh.mma_b) {
+        // ---- z = SiLU(h1 + u) of every live branch -> bf16 high/low rows ----
+        const int zs = r + 8;
+        {
+          const float* ub = p.uW1 + static_cast<size_t>(q * W) * r;  // rows q*W .. q*W+Lp-1
+          const int nz = Lp * r;
+          float uv[kZLoads];
+#pragma unroll
+          for (int j = 0; j < kZLoads; ++j) {
+            const int idx = tid + j * kThreads;
+            uv[j] = idx < nz ? ub[idx] : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < kZLoads; ++j) {
+            const int idx = tid + j * kThreads;
+            if (idx < nz) {
+              const int b = idx / r, k = idx - b * r;
+              const float x = s.h1s[k] + uv[j];
+              const float zv = x / (1.0f + expf(-x));
+              const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
+              const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
+              s.zh[static_cast<size_t>(b) * zs + k] = __bfloat16_as_ushort(hi);
+              s.zl[static_cast<size_t>(b) * zs + k] = __bfloat16_as_ushort(lo);
+            }
+          }
         }
-        __syncwarp();
-        float acc[MPL];
+        __syncthreads();
+        // ---- lambda[b][c] = (base_c + z_b . W2[c]) / T: mma.sync over (branch, candidate) tiles ----
+        {
+          const int gid = lane >> 2, tig = lane & 3;
+          const int mtiles = (Lp + 15) / 16, ntiles = M / 8;
+          for (int t = warp; t < mtiles * ntiles; t += kWarps) {
+            const int mt = t / ntiles, nt = t - mt * ntiles;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint16_t* h0 = s.zh + static_cast<size_t>(mt * 16 + gid) * zs;
+            const uint16_t* l0 = s.zl + static_cast<size_t>(mt * 16 + gid) * zs;
+            const uint16_t* wr = s.w2s + static_cast<size_t>(nt * 8 + gid) * zs;
+#pragma unroll 4
+            for (int kt = 0; kt < r / 16; ++kt) {
+              const int k0 = kt * 16 + 2 * tig;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wr + k0);
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wr + k0 + 8);
+              mma_bf16_16816(acc, *reinterpret_cast<const uint32_t*>(h0 + k0),
+                             *reinterpret_cast<const uint32_t*>(h0 + 8 * zs + k0),
+                             *reinterpret_cast<const uint32_t*>(h0 + k0 + 8),
+                             *reinterpret_cast<const uint32_t*>(h0 + 8 * zs + k0 + 8), b0, b1);
+              mma_bf16_16816(acc, *reinterpret_cast<const uint32_t*>(l0 + k0),
+                             *reinterpret_cast<const uint32_t*>(l0 + 8 * zs + k0),
+                             *reinterpret_cast<const uint32_t*>(l0 + k0 + 8),
+                             *reinterpret_cast<const uint32_t*>(l0 + 8 * zs + k0 + 8), b0, b1);
+            }
 #pragma unroll
-        for (int j = 0; j < MPL; ++j) acc[j] = 0.0f;
-        if (p.stage_w2) {
-          for (int k8 = 0; k8 < r / 8; ++k8) {
-            const float4 za = *reinterpret_cast<const float4*>(zw + k8 * 8);
-            const float4 zb = *reinterpret_cast<const float4*>(zw + k8 * 8 + 4);
-#pragma unroll
-            for (int j = 0; j < MPL; ++j) {
-              const int c = lane + 32 * j;
-              if (c < M) {
-                const uint4 w8 = *reinterpret_cast<const uint4*>(s.w2s + static_cast<size_t>(c) * (r + 8) + k8 * 8);
-                fma8(acc[j], za, zb, w8);
+            for (int e = 0; e < 4; ++e) {
+              const int b = mt * 16 + gid + (e >= 2 ? 8 : 0);
+              const int c = nt * 8 + 2 * tig + (e & 1);
+              if (b < Lp) {
+                const float lam = (s.cbs[c] + acc[e]) / p.T;
+                s.lamkey[static_cast<size_t>(b) * M + c] = rank_key(lam, static_cast<uint32_t>(s.ctk[c]));
               }
             }
           }
-        } else {
+        }
+        __syncthreads();
+        // ---- per branch: log-partition, top-K by rank counting, children by token ----
+        for (int b = warp; b < Lp; b += kWarps) {
+          const uint64_t* kb = s.lamkey + static_cast<size_t>(b) * M;
+          float lmax = rest;
+          for (int c = lane; c < M; c += 32) lmax = fmaxf(lmax, key_f32(static_cast<uint32_t>(kb[c] >> 32)));
+          lmax = warp_max(lmax);
+          float se = 0.0f;
+          for (int c = lane; c < M; c += 32) se += expf(key_f32(static_cast<uint32_t>(kb[c] >> 32)) - lmax);
+          se = warp_sum(se) + expf(rest - lmax);
+          const float logZ = lmax + logf(se);
+          int* win = s.crank + b * K;
+          for (int c = lane; c < M; c += 32) {
+            const uint64_t kc = kb[c];
+            int rk = 0;
+#pragma unroll 8
+            for (int c2 = 0; c2 < M; ++c2) rk += kb[c2] > kc ? 1 : 0;
+            if (rk < K) win[rk] = c;
+          }
+          __syncwarp();
+          if (lane < K) {
+            int c = win[lane];
+            if (c < 0 || c >= M) {
+              dt_report(p.status, DT_DEV_BOUNDS);
+              c = 0;
+            }
+            const int tok = s.ctk[c];
+            int trank = 0;
+            for (int m = 0; m < K; ++m) trank += s.ctk[min(max(win[m], 0), M - 1)] < tok ? 1 : 0;
+            const float lp = key_f32(static_cast<uint32_t>(kb[c] >> 32)) - logZ;
+            const int slot = b * K + trank;
+            s.ctok[slot] = tok;
+            s.cslot[slot] = c;
+            s.clogp[slot] = lp;
+            s.cscore[slot] = s.pscore[b] + lp;
+          }
+          __syncwarp();
+        }
+      } else {
+        float* zw = s.z + warp * r;
+        for (int b = warp; b < Lp; b += kWarps) {
+          const float* u = p.uW1 + static_cast<size_t>(q * W + b) * r;
+          {
+            // all of the lane's loads first (one L2 round trip), then SiLU
+            float uv[kMaxR32];
+#pragma unroll
+            for (int j = 0; j < kMaxR32; ++j) {
+              const int k = lane + 32 * j;
+              uv[j] = k < r ? u[k] : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < kMaxR32; ++j) {
+              const int k = lane + 32 * j;
+              if (k < r) {
+                const float x = s.h1s[k] + uv[j];
+                zw[k] = x / (1.0f + expf(-x));
+              }
+            }
+          }
+          __syncwarp();
+          float acc[MPL];
+#pragma unroll
+          for (int j = 0; j < MPL; ++j) acc[j] = 0.0f;
           for (int k8 = 0; k8 < r / 8; ++k8) {
             const float4 za = *reinterpret_cast<const float4*>(zw + k8 * 8);
             const float4 zb = *reinterpret_cast<const float4*>(zw + k8 * 8 + 4);
@@ -463,82 +650,84 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               const int c = lane + 32 * j;
               if (c < M) {
                 const uint4 w8 =
-                    __ldg(reinterpret_cast<const uint4*>(p.w2 + static_cast<size_t>(s.ctk[c]) * r) + k8);
+                    sh.stage_w2
+                        ? *reinterpret_cast<const uint4*>(s.w2s + static_cast<size_t>(c) * (r + 8) + k8 * 8)
+                        : __ldg(reinterpret_cast<const uint4*>(p.w2 + static_cast<size_t>(s.ctk[c]) * r) + k8);
                 fma8(acc[j], za, zb, w8);
               }
             }
           }
-        }
-        float lam[MPL];
-        float lmax = rest;
+          float lam[MPL];
+          float lmax = rest;
 #pragma unroll
-        for (int j = 0; j < MPL; ++j) {
-          const int c = lane + 32 * j;
-          lam[j] = c < M ? (s.cbs[c] + acc[j]) / p.T : -INFINITY;
-          lmax = fmaxf(lmax, lam[j]);
-        }
-        lmax = warp_max(lmax);
-        float se = 0.0f;
-#pragma unroll
-        for (int j = 0; j < MPL; ++j)
-          if (lane + 32 * j < M) se += expf(lam[j] - lmax);
-        se = warp_sum(se);
-        se += expf(rest - lmax);
-        const float logZ = lmax + logf(se);
-        // top-K by (logp desc, token asc): K rounds of warp argmax over register keys
-        uint64_t key[MPL];
-        float lp[MPL];
-#pragma unroll
-        for (int j = 0; j < MPL; ++j) {
-          const int c = lane + 32 * j;
-          lp[j] = lam[j] - logZ;
-          key[j] = c < M ? rank_key(lp[j], static_cast<uint32_t>(s.ctk[c])) : 0ull;
-        }
-        int my_c = 0;
-        float my_lp = 0.0f;
-        int my_tok = 0x7FFFFFFF;
-        for (int kk = 0; kk < K; ++kk) {
-          uint64_t best = 0;
-#pragma unroll
-          for (int j = 0; j < MPL; ++j) best = key[j] > best ? key[j] : best;
-          best = warp_max_u64(best);
-          int wc = -1;
-          float wlp = 0.0f;
+          for (int j = 0; j < MPL; ++j) {
+            const int c = lane + 32 * j;
+            lam[j] = c < M ? (s.cbs[c] + acc[j]) / p.T : -INFINITY;
+            lmax = fmaxf(lmax, lam[j]);
+          }
+          lmax = warp_max(lmax);
+          float se = 0.0f;
 #pragma unroll
           for (int j = 0; j < MPL; ++j)
-            if (best != 0 && key[j] == best) {
-              wc = lane + 32 * j;
-              wlp = lp[j];
-              key[j] = 0;
-            }
-          const unsigned own = __ballot_sync(0xFFFFFFFFu, wc >= 0);
-          const int src = own ? __ffs(own) - 1 : 0;
-          wc = __shfl_sync(0xFFFFFFFFu, wc, src);
-          wlp = __shfl_sync(0xFFFFFFFFu, wlp, src);
-          if (lane == kk) {
-            if (wc < 0 || wc >= M) {
-              dt_report(p.status, DT_DEV_BOUNDS);
-              wc = 0;
-            }
-            my_c = wc;
-            my_lp = wlp;
-            my_tok = static_cast<int>(rank_key_id(best));
+            if (lane + 32 * j < M) se += expf(lam[j] - lmax);
+          se = warp_sum(se);
+          se += expf(rest - lmax);
+          const float logZ = lmax + logf(se);
+          // top-K by (logp desc, token asc): K rounds of warp argmax over register keys
+          uint64_t key[MPL];
+          float lp[MPL];
+#pragma unroll
+          for (int j = 0; j < MPL; ++j) {
+            const int c = lane + 32 * j;
+            lp[j] = lam[j] - logZ;
+            key[j] = c < M ? rank_key(lp[j], static_cast<uint32_t>(s.ctk[c])) : 0ull;
           }
+          int my_c = 0;
+          float my_lp = 0.0f;
+          int my_tok = 0x7FFFFFFF;
+          for (int kk = 0; kk < K; ++kk) {
+            uint64_t best = 0;
+#pragma unroll
+            for (int j = 0; j < MPL; ++j) best = key[j] > best ? key[j] : best;
+            best = warp_max_u64(best);
+            int wc = -1;
+            float wlp = 0.0f;
+#pragma unroll
+            for (int j = 0; j < MPL; ++j)
+              if (best != 0 && key[j] == best) {
+                wc = lane + 32 * j;
+                wlp = lp[j];
+                key[j] = 0;
+              }
+            const unsigned own = __ballot_sync(0xFFFFFFFFu, wc >= 0);
+            const int src = own ? __ffs(own) - 1 : 0;
+            wc = __shfl_sync(0xFFFFFFFFu, wc, src);
+            wlp = __shfl_sync(0xFFFFFFFFu, wlp, src);
+            if (lane == kk) {
+              if (wc < 0 || wc >= M) {
+                dt_report(p.status, DT_DEV_BOUNDS);
+                wc = 0;
+              }
+              my_c = wc;
+              my_lp = wlp;
+              my_tok = static_cast<int>(rank_key_id(best));
+            }
+          }
+          // children of branch b, sorted by token id
+          int rank = 0;
+          for (int m = 0; m < K; ++m) {
+            const int t = __shfl_sync(0xFFFFFFFFu, my_tok, m);
+            rank += t < my_tok ? 1 : 0;
+          }
+          if (lane < K) {
+            const int slot = b * K + rank;
+            s.ctok[slot] = my_tok;
+            s.cslot[slot] = my_c;
+            s.clogp[slot] = my_lp;
+            s.cscore[slot] = s.pscore[b] + my_lp;
+          }
+          __syncwarp();
         }
-        // children of branch b, sorted by token id
-        int rank = 0;
-        for (int m = 0; m < K; ++m) {
-          const int t = __shfl_sync(0xFFFFFFFFu, my_tok, m);
-          rank += t < my_tok ? 1 : 0;
-        }
-        if (lane < K) {
-          const int slot = b * K + rank;
-          s.ctok[slot] = my_tok;
-          s.cslot[slot] = my_c;
-          s.clogp[slot] = my_lp;
-          s.cscore[slot] = s.pscore[b] + my_lp;
-        }
-        __syncwarp();
       }
       __syncthreads();
       // node arrays of this depth (CTA 0)
@@ -554,19 +743,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       if (!last) {
         // top-W of the depth by (score desc, node index asc); survivors ascending
         if (nchild <= kRankMax) {
-          for (int e = tid; e < nchild; e += kThreads) {
-            const uint64_t ke = rank_key(s.cscore[e], static_cast<uint32_t>(e));
-            int rk = 0;
-            for (int f = 0; f < nchild; ++f) rk += rank_key(s.cscore[f], static_cast<uint32_t>(f)) > ke;
-            s.crank[e] = rk;
-          }
+          // one child per thread: rank over precomputed keys, survivors (rank <
+          // Li) placed in slot order with per-warp ballots
+          for (int e = tid; e < nchild; e += kThreads) s.wkey[e] = rank_key(s.cscore[e], static_cast<uint32_t>(e));
           __syncthreads();
-          for (int e = tid; e < nchild; e += kThreads) {
-            if (s.crank[e] < Li) {
-              int pos = 0;
-              for (int f = 0; f < e; ++f) pos += s.crank[f] < Li;
-              s.surv[q * W + pos] = e;
-            }
+          bool alive = false;
+          if (tid < nchild) {
+            const uint64_t ke = s.wkey[tid];
+            int rk = 0;
+#pragma unroll 8
+            for (int f = 0; f < nchild; ++f) rk += s.wkey[f] > ke ? 1 : 0;
+            alive = rk < Li;
+          }
+          const unsigned bal = __ballot_sync(0xFFFFFFFFu, alive);
+          if (lane == 0) s_wcnt[warp] = __popc(bal);
+          __syncthreads();
+          if (alive) {
+            int pos = __popc(bal & ((1u << lane) - 1u));
+            for (int w2 = 0; w2 < warp; ++w2) pos += s_wcnt[w2];
+            s.surv[q * W + pos] = tid;
           }
         } else {
           const int npad = pow2_at_least(nchild);
@@ -610,8 +805,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           const int jv = idx / nj, jj = idx - jv * nj;
           const int e = s.surv[q * W + jv];
           const int b = e / K;
-          const float* x = s.xs + static_cast<size_t>(s.cslot[e]) * 3 * p.jper;
-          const float* uu = s.uu + static_cast<size_t>(q * Lp + b) * 3 * p.jper;
+          const float* x = s.xs + static_cast<size_t>(s.cslot[e]) * 3 * sh.jper;
+          const float* uu = s.uu + static_cast<size_t>(q * Lp + b) * 3 * sh.jper;
           const float h = Sprev[static_cast<size_t>(q * W + b) * g + j0 + jj];
           const float rg = sigmoidf_(x[jj] + uu[jj]);
           const float zg = sigmoidf_(x[nj + jj] + uu[nj + jj]);
@@ -623,13 +818,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       }
     }
     if (i < p.depth_last) {
+      // stage the next depth's request 0 now: the copies overlap the barrier
+      __syncthreads();
+      select_row_tokens(p, sh, s, 0, i + 1);
+      __syncthreads();
+      stage_row(p, sh, s, static_cast<size_t>(i), j0, nj, i + 1 != D);
       if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) return;
     }
   }
 }
 
-template <int MPL>
-cudaError_t launch_mpl(const ChainParams& p, int grid, size_t smem, cudaStream_t stream) {
+template <int MPL, class Dm>
+cudaError_t launch_one(const ChainParams& p, int grid, size_t smem, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -640,7 +840,15 @@ cudaError_t launch_mpl(const ChainParams& p, int grid, size_t smem, cudaStream_t
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_chain<MPL>, p);
+  return cudaLaunchKernelEx(&cfg, k_chain<MPL, Dm>, p);
+}
+
+bool is_q4b(const ChainParams& p, int grid) {
+  const Shape a = runtime_shape(p);
+  const Shape b = DimsQ4B::kShape;
+  return grid == 128 && a.g == b.g && a.r == b.r && a.M == b.M && a.K == b.K && a.W == b.W &&
+         a.n_req == b.n_req && a.D == b.D && a.jper == b.jper && a.rper == b.rper && a.cpad == b.cpad &&
+         a.stage_w2 == b.stage_w2 && a.mma_b == b.mma_b && a.prefetch == b.prefetch;
 }
 
 }  // namespace
@@ -653,33 +861,43 @@ int chain_grid(const ChainParams& p, int num_sms) {
   return G;
 }
 
-size_t chain_smem_bytes(const ChainParams& p) { return smem_sizes(p).total; }
+size_t chain_smem_bytes(const ChainParams& p) { return smem_sizes(runtime_shape(p)).total; }
 
 void chain_plan(ChainParams& p, int grid) {
   p.jper = (p.g + grid - 1) / grid;
   p.rper = (p.r + grid - 1) / grid;
   const int ncol = 3 * p.jper + p.rper;
   p.cpad = (ncol + 31) / 32 * 32;
+  constexpr size_t kBudget = 224 * 1024;  // dynamic shared memory per CTA
+  // tensor-core phase B: staged W2 rows, whole k16 steps, n8 candidate tiles,
+  // z of all branches within one pass of kZLoads values per thread
   p.stage_w2 = 1;
-  if (smem_sizes(p).total > 200 * 1024) p.stage_w2 = 0;  // wide candidate sets read W2 from L2
+  p.mma_b = (p.r % 16 == 0 && p.M % 8 == 0 && p.W * p.r <= kZLoads * kThreads && p.W * p.M <= 4096) ? 1 : 0;
+  if (p.mma_b && chain_smem_bytes(p) > kBudget) p.mma_b = 0;
+  if (!p.mma_b && chain_smem_bytes(p) > kBudget) p.stage_w2 = 0;  // wide candidate sets read W2 from L2
 }
 
 cudaError_t chain_prepare() {
-  cudaError_t e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<2>));
-  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<4>));
-  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<8>));
-  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_chain<16>));
-  return e;
+  const void* fns[] = {
+      reinterpret_cast<const void*>(k_chain<2, DimsQ4B>),     reinterpret_cast<const void*>(k_chain<2, DimsRuntime>),
+      reinterpret_cast<const void*>(k_chain<4, DimsRuntime>), reinterpret_cast<const void*>(k_chain<8, DimsRuntime>),
+      reinterpret_cast<const void*>(k_chain<16, DimsRuntime>)};
+  for (const void* f : fns) {
+    cudaError_t e = dt_allow_max_dynamic_smem(f);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream) {
   const size_t smem = chain_smem_bytes(p);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   const int mpl = (p.M + 31) / 32;
-  if (mpl <= 2) return launch_mpl<2>(p, grid, smem, stream);
-  if (mpl <= 4) return launch_mpl<4>(p, grid, smem, stream);
-  if (mpl <= 8) return launch_mpl<8>(p, grid, smem, stream);
-  return launch_mpl<16>(p, grid, smem, stream);
+  if (is_q4b(p, grid)) return launch_one<2, DimsQ4B>(p, grid, smem, stream);
+  if (mpl <= 2) return launch_one<2, DimsRuntime>(p, grid, smem, stream);
+  if (mpl <= 4) return launch_one<4, DimsRuntime>(p, grid, smem, stream);
+  if (mpl <= 8) return launch_one<8, DimsRuntime>(p, grid, smem, stream);
+  return launch_one<16, DimsRuntime>(p, grid, smem, stream);
 }
 
 }  // namespace dt

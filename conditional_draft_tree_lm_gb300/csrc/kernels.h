@@ -96,6 +96,7 @@ struct ChainParams {
   int jper, rper;     // S / r columns owned per CTA
   int cpad;           // padded owned-column count (multiple of 32)
   int stage_w2;       // 1: stage the candidates' W2 rows in shared memory
+  int mma_b;          // 1: corrected logits of all branches as one tensor-core product
   int off[kMaxDepth + 1];  // first node index of depth i
   int nn[kMaxDepth + 1];   // nodes created at depth i
   int L[kMaxDepth + 1];    // branches that live after depth i (L[0] = 1)
