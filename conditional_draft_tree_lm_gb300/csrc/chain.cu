@@ -34,6 +34,7 @@
 // returns.
 #include "common.cuh"
 #include "kernels.h"
+#include "prune.cuh"
 
 namespace dt {
 
@@ -294,6 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ int s_wcnt[kWarps];
+  __shared__ uint32_t s_state[4];
+  __shared__ int s_scan[40];
 
   const Shape sh = Dm::get(p);
   const int g = sh.g, r = sh.r, M = sh.M, K = sh.K, W = sh.W, n_req = sh.n_req, D = sh.D;
@@ -826,6 +829,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) return;
     }
   }
+
+  // ---- tail: global Top-B and tree/mask of the single request (CTA 0) ----
+  if (p.fuse_tree && blockIdx.x == 0) {
+    __syncthreads();
+    // shared memory of the finished depth loop is reused: node keys in the
+    // weight area, radix histograms in the reduction area, small arrays in
+    // the state area (sizes checked by chain_can_fuse_tree)
+    int* offs = reinterpret_cast<int*>(s.sh);
+    int* nodes = offs + (kMaxDepth + 2);
+    int* par = nodes + (p.B + 1);
+    int* dep = par + (p.B + 1);
+    for (int k = tid; k <= D + 1; k += kThreads) offs[k] = p.off[k];
+    __syncthreads();
+    topb_select(p.node_score, p.N1, p.B, p.beta, D, offs, reinterpret_cast<uint32_t*>(s.w),
+                reinterpret_cast<uint32_t*>(s.red), kWarps * 256, s_state, s_scan, p.sel);
+    tree_and_mask(p.sel, p.N1, p.B, D, offs, p.node_tok, p.node_parent, p.node_score, nodes, par, dep, p.tok,
+                  p.parent, p.depth, p.logp_cum, p.mask, p.status);
+  }
 }
 
 template <int MPL, class Dm>
@@ -875,6 +896,16 @@ void chain_plan(ChainParams& p, int grid) {
   p.mma_b = (p.r % 16 == 0 && p.M % 8 == 0 && p.W * p.r <= kZLoads * kThreads && p.W * p.M <= 4096) ? 1 : 0;
   if (p.mma_b && chain_smem_bytes(p) > kBudget) p.mma_b = 0;
   if (!p.mma_b && chain_smem_bytes(p) > kBudget) p.stage_w2 = 0;  // wide candidate sets read W2 from L2
+}
+
+bool chain_can_fuse_tree(const ChainParams& p) {
+  if (p.n_req != 1) return false;
+  const size_t gp = static_cast<size_t>(kstride(p.g));
+  const size_t weight_bytes = gp * p.cpad * 2;                          // holds the Top-B keys
+  const size_t red_words = static_cast<size_t>(kWarps) * kPC * p.cpad;  // holds the histograms
+  const size_t state_bytes = gp * kPC * 2 * 2;                          // holds offsets + tree slots
+  return static_cast<size_t>(p.N1 - 1) * 4 <= weight_bytes && red_words >= static_cast<size_t>(kWarps) * 256 &&
+         static_cast<size_t>(kMaxDepth + 2 + 3 * (p.B + 1)) * 4 <= state_bytes;
 }
 
 cudaError_t chain_prepare() {

@@ -44,7 +44,7 @@ dt_status check(const dt_config* c) {
     return DT_ERR_INVALID_ARG;
   if (!(c->T > 0.0f) || !(c->beta <= 0.0f)) return DT_ERR_INVALID_ARG;
   if (c->K > c->M || c->M > c->V) return DT_ERR_INVALID_ARG;
-  if (c->block > kMaxDepth + 1) return DT_ERR_SHAPE;
+  if (c->block > kMaxDepth) return DT_ERR_SHAPE;  // depths 1..63: off[D+1] stays inside the tables
   if (c->M > 512 || c->K > 32 || c->W > 64) return DT_ERR_SHAPE;
   if (c->d % 8 != 0 || c->g % 8 != 0 || c->r % 8 != 0) return DT_ERR_SHAPE;
   if (c->r > 1024 || c->g > 1024) return DT_ERR_SHAPE;
@@ -60,7 +60,8 @@ dt_status check(const dt_config* c) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, cand_tok, cand_base, rest_lse, row_done, S,
+  size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, part_kth, cand_tok, cand_base, rest_lse,
+      row_done, S,
       uW1, live, node_tok, node_parent, node_logp, node_score, sel, bar, status, H_dev, root_dev,
       out_tok, out_parent, out_depth, out_logp, out_mask, total;
   size_t xtab;
@@ -82,6 +83,7 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   put(L.part_max, rows * tp.S * 4);
   put(L.part_sum, rows * tp.S * 4);
   put(L.part_cnt, rows * tp.S * 4);
+  put(L.part_kth, rows * tp.S * 4);
   put(L.cand_tok, rows * c.M * 4);
   put(L.cand_base, rows * c.M * 4);
   put(L.rest_lse, rows * 4);
@@ -274,9 +276,22 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
   ChainParams cp = chain_params(c, root, ntok, npar, nlogp, nscore, nullptr);
   cp.depth_first = 1;
   cp.depth_last = c->t.D;
+  int32_t* sel = c->at<int32_t>(c->lay.sel);
+  if (chain_can_fuse_tree(cp)) {
+    // single request: the chain kernel's CTA 0 also prunes and emits the tree
+    cp.fuse_tree = 1;
+    cp.B = c->cfg.B;
+    cp.beta = c->cfg.beta;
+    cp.sel = sel;
+    cp.tok = tok;
+    cp.parent = parent;
+    cp.depth = depth;
+    cp.logp_cum = logp_cum;
+    cp.mask = mask;
+    return enqueue_chain(c, cp, st);
+  }
   s = enqueue_chain(c, cp, st);
   if (s != DT_OK) return s;
-  int32_t* sel = c->at<int32_t>(c->lay.sel);
   PruneParams pp = prune_params(c, nscore, sel);
   DT_TRY(launch_prune(pp, st));
   pp.node_tok = ntok;
@@ -378,6 +393,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->topm.part_max = c->at<float>(c->lay.part_max);
   c->topm.part_sum = c->at<float>(c->lay.part_sum);
   c->topm.part_cnt = c->at<int>(c->lay.part_cnt);
+  c->topm.part_kth = c->at<float>(c->lay.part_kth);
   c->topm.cand_tok = c->at<int>(c->lay.cand_tok);
   c->topm.cand_base = c->at<float>(c->lay.cand_base);
   c->topm.rest_lse = c->at<float>(c->lay.rest_lse);
@@ -611,8 +627,10 @@ dt_status dt_get_device_status(dt_ctx* c) {
 }
 
 int dt_round_kernel_count(const dt_ctx* c) {
-  (void)c;
-  return 5;  // LM head GEMM, Top-M, depth chain, Top-B, tree/mask
+  if (!c) return -1;
+  // LM head GEMM, Top-M, depth chain (+ Top-B, tree/mask unless the chain's tail does them)
+  ChainParams cp = chain_params(const_cast<dt_ctx*>(c), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  return chain_can_fuse_tree(cp) ? 3 : 5;
 }
 
 }  // extern "C"

@@ -56,6 +56,7 @@ struct TopmParams {
   float* part_max;  // [rows, S]   max of logit/T over the chunk
   float* part_sum;  // [rows, S]   sum over the chunk's non-candidates of exp(logit/T - max)
   int* part_cnt;    // [rows, S]
+  float* part_kth;  // [rows, S]   the chunk's M-th largest logit (-inf if it has <= M)
   int* cand_tok;    // [rows, M]
   float* cand_base; // [rows, M]
   float* rest_lse;  // [rows]
@@ -97,6 +98,17 @@ struct ChainParams {
   int cpad;           // padded owned-column count (multiple of 32)
   int stage_w2;       // 1: stage the candidates' W2 rows in shared memory
   int mma_b;          // 1: corrected logits of all branches as one tensor-core product
+  // tail of a whole-round launch of one request: CTA 0 (which wrote every node
+  // array itself) runs the global Top-B and the tree/mask, no extra launch
+  int fuse_tree;
+  int B;
+  float beta;
+  int* sel;           // [B]
+  int* tok;           // [B+1]
+  int* parent;
+  int* depth;
+  float* logp_cum;
+  uint8_t* mask;      // [(B+1)^2]
   int off[kMaxDepth + 1];  // first node index of depth i
   int nn[kMaxDepth + 1];   // nodes created at depth i
   int L[kMaxDepth + 1];    // branches that live after depth i (L[0] = 1)
@@ -104,6 +116,7 @@ struct ChainParams {
 int chain_grid(const ChainParams& p, int num_sms);
 size_t chain_smem_bytes(const ChainParams& p);
 void chain_plan(ChainParams& p, int grid);
+bool chain_can_fuse_tree(const ChainParams& p);
 cudaError_t chain_prepare();
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream);
 
