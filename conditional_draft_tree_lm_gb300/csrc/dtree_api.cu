@@ -334,6 +334,14 @@ size_t dt_workspace_bytes(const dt_config* cfg) {
 
 const char* dt_last_error(void) { return g_last_error; }
 
+}  // extern "C"
+
+namespace dt {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg ? msg : ""); }
+}  // namespace dt
+
+extern "C" {
+
 const char* dt_status_string(dt_status s) {
   switch (s) {
     case DT_OK: return "ok";

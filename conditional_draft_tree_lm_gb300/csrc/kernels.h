@@ -69,6 +69,9 @@ size_t topm_merge_smem(const TopmParams& p);
 cudaError_t topm_prepare();
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream);
 
+// Text returned by dt_last_error() on the calling thread.
+void set_last_error(const char* msg);
+
 // ---------------------------------------------------------------- depth chain
 struct ChainParams {
   int n_req, D, g, r, M, K, W, V, ldw1, d;

@@ -70,6 +70,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dt_build_round_host": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_get_device_status": (c_int, [vp]),
         "dt_round_kernel_count": (c_int, [vp]),
+        "dt_topm_noalloc": (c_int, [vp, c_int, c_int, c_int, c_float, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -290,6 +291,24 @@ class DraftTreeBuilder:
 
     def round_kernel_count(self) -> int:
         return int(self.lib.dt_round_kernel_count(self.ctx))
+
+
+def topm_noalloc(logits, M, T, cand_tok, cand_base, rest_lse, stream=None):
+    """Top-M and rest log-partition of each row of ``logits`` ([rows, V] fp32)
+    without a context and without allocating device memory (dt_topm_noalloc):
+    for callers that must not allocate.  Outputs are caller tensors:
+    cand_tok [rows, M] int32, cand_base [rows, M] fp32, rest_lse [rows] fp32."""
+    import torch
+    if logits.dim() != 2:
+        raise ValueError("logits: expected [rows, V]")
+    rows, V = logits.shape
+    lib = load_library()
+    st = lib.dt_topm_noalloc(_ptr(logits, torch.float32, rows * V, "logits"), int(rows), int(V), int(M), float(T),
+                             _ptr(cand_tok, torch.int32, rows * M, "cand_tok"),
+                             _ptr(cand_base, torch.float32, rows * M, "cand_base"),
+                             _ptr(rest_lse, torch.float32, rows, "rest_lse"), _stream(stream))
+    if st != 0:
+        raise DtreeError(st, "dt_topm_noalloc: " + lib.dt_last_error().decode(errors="replace"))
 
 
 def bf16_tensor(bits, device="cuda"):

@@ -216,6 +216,35 @@ dt_status dt_build_round_host(dt_ctx* ctx, const void* H_host, const int32_t* ro
                               int32_t* tok_host, int32_t* parent_host, int32_t* depth_host,
                               float* logp_cum_host, uint8_t* mask_host, void* stream);
 
+/* --------------------------------------------------------------------------
+ * Step 2 without allocation.  The pages have no counterpart of this entry
+ * point: it exists for callers that must not allocate device memory — a
+ * serving process that fixes its GPU memory budget at start-up, code embedded
+ * in another framework whose allocator owns the device, or a loop that cannot
+ * afford the implicit synchronisation cudaMalloc/cudaFree bring.
+ *
+ * dt_topm_noalloc computes what dt_topm computes, with no context:
+ *   logits:    [rows, V] fp32 input.
+ *   cand_tok:  [rows, M] int32 out, logit descending, token id ascending.
+ *   cand_base: [rows, M] fp32 out, the base logits of those tokens.
+ *   rest_lse:  [rows] fp32 out, log sum over the non-candidates of exp(logit/T).
+ * It allocates nothing: its scratch is one fixed 4 MiB array of device memory
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits.  Sizes whose scratch would exceed it (roughly rows * chunks *
+ * (8 M + 16) bytes, chunks ~ 2 * SMs / rows, at least V / 16384) are rejected
+ * with DT_ERR_SHAPE and a message in dt_last_error(); M <= 512.
+ * The first call on each device does a one-time set-up (it looks up the
+ * array's device address and sets a kernel attribute), so make that first
+ * call before any stream capture.  All calls on a device share that device's
+ * array, which keeps the previous call's contents (the call clears what must
+ * start at zero): calls that overlap on the GPU, for example on two streams,
+ * race and must be ordered by the caller.  Asynchronous on `stream`.
+ * Device-side index checks are not reported (there is no status word).
+ * Errors: INVALID_ARG (null pointer, M > V, T <= 0), SHAPE, CUDA.
+ * ------------------------------------------------------------------------ */
+dt_status dt_topm_noalloc(const float* logits, int rows, int V, int M, float T, int32_t* cand_tok,
+                          float* cand_base, float* rest_lse, void* stream);
+
 /* Synchronise the context's last stream and read (and clear) its device status
  * word: DT_OK, DT_ERR_TIMEOUT or DT_ERR_DEVICE. */
 dt_status dt_get_device_status(dt_ctx* ctx);
