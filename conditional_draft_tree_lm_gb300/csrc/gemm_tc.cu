@@ -106,13 +106,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
           const uint32_t sb = sa + kABytes;
+          // straight-line issue (a run-time loop over N halves around each
+          // MMA slowed the whole stream by a quarter)
+          if (p.BN <= 256) {
+            const uint32_t idesc = idesc_bf16_f32(128, p.BN);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = sdesc_k_sw128(sa + k * 32);
-            for (int h = 0; h < p.BN; h += 256) {
-              const uint32_t n = min(256, p.BN - h);
-              const uint64_t bd = sdesc_k_sw128(sb + h * 128 + k * 32);
-              tc_mma_bf16(d_tmem + h, ad, bd, idesc_bf16_f32(128, n), (kb | k) != 0);
+            for (int k = 0; k < 4; ++k)
+              tc_mma_bf16(d_tmem, sdesc_k_sw128(sa + k * 32), sdesc_k_sw128(sb + k * 32), idesc, (kb | k) != 0);
+          } else {  // BN = 512: two N = 256 halves
+            const uint32_t idesc = idesc_bf16_f32(128, 256);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_k_sw128(sa + k * 32);
+              tc_mma_bf16(d_tmem, ad, sdesc_k_sw128(sb + k * 32), idesc, (kb | k) != 0);
+              tc_mma_bf16(d_tmem + 256, ad, sdesc_k_sw128(sb + 256 * 128 + k * 32), idesc, (kb | k) != 0);
             }
           }
           tc_commit(&empty[stage]);
@@ -143,12 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c0 = 0; c0 < p.BN; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tbase + c0, v);
+          // fully unrolled with predicated stores: v stays in registers
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int n = c0 + j;
-            if (n >= p.n_valid) break;
             const int q = n / p.block, i = n - q * p.block;
-            if (i > 0 && valid)
+            if (n < p.n_valid && i > 0 && valid)
               dst[static_cast<size_t>(q * p.D + i - 1) * nrows + row] = __uint_as_float(v[j]);
           }
         }
@@ -172,8 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<float4*>(o + j) = f;
               }
             } else {
-              for (int j = 0; j < 16 && col0 + j < p.n_valid; ++j)
-                o[j] = __uint_as_float(v[j]) + bf16_to_f32(p.bias[col0 + j]);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (col0 + j < p.n_valid) o[j] = __uint_as_float(v[j]) + bf16_to_f32(p.bias[col0 + j]);
             }
           }
         }
