@@ -83,6 +83,7 @@ DT_DEVINL void cp_async4(void* s, const void* g) {
 }
 DT_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 DT_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+DT_DEVINL void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 DT_DEVINL void red_release_add_u32(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -116,12 +117,70 @@ DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_
   return *s_abort == 0;
 }
 
-DT_DEVINL float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Activations on the fast exponential and division intrinsics (absolute
+// error ~1e-7; a large |x| saturates to the right limit: __fdividef returns 0
+// for a denominator beyond 2^126).
+DT_DEVINL float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+DT_DEVINL float tanhf_(float x) { return __fdividef(2.0f, 1.0f + __expf(-2.0f * x)) - 1.0f; }
+DT_DEVINL float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+
+// Bitonic sort of 64 (key, payload) pairs held by one warp, elements 2*lane
+// (ka, pa) and 2*lane + 1 (kb, pb), into descending key order: afterwards the
+// element of rank e sits in lane e/2, in ka when e is even and kb when odd.
+DT_DEVINL void warp_sort64_desc(uint64_t& ka, uint64_t& kb, int& pa, int& pb) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1) {
+    const bool desc = ((2 * lane) & k) == 0;
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == 1) {
+        if (desc ? (ka < kb) : (ka > kb)) {
+          const uint64_t t = ka;
+          ka = kb;
+          kb = t;
+          const int u = pa;
+          pa = pb;
+          pb = u;
+        }
+      } else {
+        const int lj = j >> 1;  // partner element e ^ j lives in lane ^ (j / 2)
+        const uint64_t oa = __shfl_xor_sync(0xFFFFFFFFu, ka, lj);
+        const uint64_t ob = __shfl_xor_sync(0xFFFFFFFFu, kb, lj);
+        const int qa = __shfl_xor_sync(0xFFFFFFFFu, pa, lj);
+        const int qb = __shfl_xor_sync(0xFFFFFFFFu, pb, lj);
+        const bool keep_max = ((lane & lj) == 0) == desc;  // the lower element of a descending pair keeps the max
+        if (keep_max ? (oa > ka) : (oa < ka)) {
+          ka = oa;
+          pa = qa;
+        }
+        if (keep_max ? (ob > kb) : (ob < kb)) {
+          kb = ob;
+          pb = qb;
+        }
+      }
+    }
+  }
+}
+
+// Element of rank w (0..63) of a warp_sort64_desc result, delivered to the
+// calling lane (every lane must call).
+DT_DEVINL void warp_sorted_at(uint64_t ka, uint64_t kb, int pa, int pb, int w, uint64_t& key, int& pay) {
+  const int src = (w >> 1) & 31;
+  const uint64_t xa = __shfl_sync(0xFFFFFFFFu, ka, src), xb = __shfl_sync(0xFFFFFFFFu, kb, src);
+  const int ya = __shfl_sync(0xFFFFFFFFu, pa, src), yb = __shfl_sync(0xFFFFFFFFu, pb, src);
+  key = (w & 1) ? xb : xa;
+  pay = (w & 1) ? yb : ya;
+}
 
 // Dimensions a launch runs with (see chain_plan).
 struct Shape {
   int g, r, M, K, W, n_req, D, jper, rper, cpad;
   bool stage_w2, mma_b, prefetch;
+  // one request with prefetched tokens: depth i+1's candidate data is staged
+  // at the start of depth i into a second buffer
+  bool dbuf;
 };
 
 // The candidate tokens of every depth of request 0 are read once, at launch.
@@ -129,7 +188,7 @@ DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096;
 
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
-               prefetch_tokens(p.D, p.M)};
+               prefetch_tokens(p.D, p.M), p.n_req == 1 && prefetch_tokens(p.D, p.M)};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -139,8 +198,17 @@ struct DimsRuntime {
 // The Qwen3-4B shape (g=1024, r=256, M=64, K=W=8, one request, depth 15, 128
 // CTAs): dimensions are literals, so the compiler folds the index arithmetic.
 struct DimsQ4B {
-  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true};
+  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true};
   static DT_DEVINL Shape get(const ChainParams&) { return kShape; }
+};
+
+// Candidate data of one (request, depth) row staged in shared memory.
+struct Stage {
+  uint16_t* w2s;  // [M][r+8] W2 rows of the candidates
+  float* xs;      // [M][3*jper] GRU-input slices of the candidates
+  float* cbs;     // [M] candidate base logits
+  float* h1s;     // [r]
+  float* rest;    // [1]
 };
 
 struct Smem {
@@ -170,14 +238,15 @@ struct Smem {
   uint16_t* zh;     // [16*ceil(W/16)][r+8] bf16 high part of z (tensor-core phase B)
   uint16_t* zl;     // same, low part
   uint64_t* lamkey; // [W][M] (lambda, token) keys (tensor-core phase B)
+  Stage st0, st1;   // stage buffers of even and odd depths (the same buffer without dbuf)
 };
+
+DT_HOST_DEVICE_INLINE size_t al16(size_t b) { return (b + 15) & ~static_cast<size_t>(15); }
 
 struct SmemSizes {
   size_t off[23];
   size_t total;
 };
-
-DT_HOST_DEVICE_INLINE size_t al16(size_t b) { return (b + 15) & ~static_cast<size_t>(15); }
 
 DT_HOST_DEVICE_INLINE int pow2_at_least(int n) {
   int v = 1;
@@ -190,6 +259,21 @@ DT_HOST_DEVICE_INLINE int pow2_at_least(int n) {
 // that consecutive rows start 4 banks apart (conflict-free fragment loads).
 DT_HOST_DEVICE_INLINE int kstride(int g) { return (g + 15) / 16 * 16 + 8; }
 
+// One stage buffer's bytes of each staged array (0 w2s, 1 xs, 2 cbs, 3 h1s,
+// 4 rest), and the region that holds both buffers when double-buffered.
+DT_HOST_DEVICE_INLINE size_t stage_one(const Shape& sh, int which) {
+  switch (which) {
+    case 0: return sh.stage_w2 ? static_cast<size_t>(sh.M) * (sh.r + 8) * 2 : 0;
+    case 1: return static_cast<size_t>(sh.M) * 3 * sh.jper * 4;
+    case 2: return static_cast<size_t>(sh.M) * 4;
+    case 3: return static_cast<size_t>(sh.r) * 4;
+    default: return 16;
+  }
+}
+DT_HOST_DEVICE_INLINE size_t stage_bytes(const Shape& sh, int which) {
+  return sh.dbuf ? 2 * al16(stage_one(sh, which)) : stage_one(sh, which);
+}
+
 DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
   const size_t WK = static_cast<size_t>(sh.W) * sh.K;
   const size_t gp = static_cast<size_t>(kstride(sh.g));
@@ -199,12 +283,12 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
       static_cast<size_t>(kWarps) * kPC * sh.cpad * 4,
       static_cast<size_t>(sh.n_req) * sh.W * 3 * sh.jper * 4,
       sh.mma_b ? 0 : static_cast<size_t>(kWarps) * sh.r * 4,
-      sh.stage_w2 ? static_cast<size_t>(sh.M) * (sh.r + 8) * 2 : 0,
-      static_cast<size_t>(sh.M) * 3 * sh.jper * 4,
+      stage_bytes(sh, 0),
+      stage_bytes(sh, 1),
       static_cast<size_t>(sh.M) * 4,
-      static_cast<size_t>(sh.M) * 4,
-      static_cast<size_t>(sh.r) * 4,
-      16,
+      stage_bytes(sh, 2),
+      stage_bytes(sh, 3),
+      stage_bytes(sh, 4),
       WK * 4,
       WK * 4,
       WK * 4,
@@ -252,30 +336,47 @@ DT_DEVINL void select_row_tokens(const ChainParams& p, const Shape& sh, Smem& s,
   }
 }
 
-// Asynchronous copies of everything phase B/C read for one (request, depth) row.
-DT_DEVINL void stage_row(const ChainParams& p, const Shape& sh, const Smem& s, size_t qrow, int j0, int nj,
-                         bool want_x) {
+// Asynchronous copies (one cp.async group) of everything phase B/C read for
+// one (request, depth) row into buffer b; tok holds the row's M candidate
+// tokens.  Whole CTA.
+DT_DEVINL void stage_row(const ChainParams& p, const Shape& sh, const Stage& b, const int* tok, size_t qrow, int j0,
+                         int nj, bool want_x) {
   const int r = sh.r, M = sh.M, g = sh.g;
   if (sh.stage_w2) {
     const int c8 = r / 8;
     for (int idx = threadIdx.x; idx < M * c8; idx += kThreads) {
       const int c = idx / c8, k = idx - c * c8;
-      cp_async16(s.w2s + static_cast<size_t>(c) * (r + 8) + k * 8,
-                 p.w2 + static_cast<size_t>(s.ctk[c]) * r + k * 8);
+      cp_async16(b.w2s + static_cast<size_t>(c) * (r + 8) + k * 8, p.w2 + static_cast<size_t>(tok[c]) * r + k * 8);
     }
   }
   if (want_x && nj > 0) {
-    const int per = 3 * nj;
-    for (int idx = threadIdx.x; idx < M * per; idx += kThreads) {
-      const int c = idx / per, rem = idx - c * per;
-      const int gate = rem / nj, jj = rem - gate * nj;
-      cp_async4(s.xs + static_cast<size_t>(c) * 3 * sh.jper + gate * nj + jj,
-                p.xtab + static_cast<size_t>(s.ctk[c]) * 3 * g + gate * g + j0 + jj);
+    if (nj == sh.jper && nj % 4 == 0 && g % 4 == 0) {
+      // 16-byte pieces: each gate's owned columns are contiguous in X and in xs
+      const int q4 = nj / 4, per = 3 * q4;
+      for (int idx = threadIdx.x; idx < M * per; idx += kThreads) {
+        const int c = idx / per, rem = idx - c * per;
+        const int gate = rem / q4, jj = (rem - gate * q4) * 4;
+        cp_async16(b.xs + static_cast<size_t>(c) * 3 * sh.jper + gate * nj + jj,
+                   p.xtab + static_cast<size_t>(tok[c]) * 3 * g + gate * g + j0 + jj);
+      }
+    } else {
+      const int per = 3 * nj;
+      for (int idx = threadIdx.x; idx < M * per; idx += kThreads) {
+        const int c = idx / per, rem = idx - c * per;
+        const int gate = rem / nj, jj = rem - gate * nj;
+        cp_async4(b.xs + static_cast<size_t>(c) * 3 * sh.jper + gate * nj + jj,
+                  p.xtab + static_cast<size_t>(tok[c]) * 3 * g + gate * g + j0 + jj);
+      }
     }
   }
-  for (int c = threadIdx.x; c < M; c += kThreads) cp_async4(s.cbs + c, p.cand_base + qrow * M + c);
-  for (int k = threadIdx.x; k < r; k += kThreads) cp_async4(s.h1s + k, p.h1 + qrow * r + k);
-  if (threadIdx.x == 0) cp_async4(s.rest, p.rest_lse + qrow);
+  if (M % 4 == 0 && r % 4 == 0) {
+    for (int c = threadIdx.x; c < M / 4; c += kThreads) cp_async16(b.cbs + 4 * c, p.cand_base + qrow * M + 4 * c);
+    for (int k = threadIdx.x; k < r / 4; k += kThreads) cp_async16(b.h1s + 4 * k, p.h1 + qrow * r + 4 * k);
+  } else {
+    for (int c = threadIdx.x; c < M; c += kThreads) cp_async4(b.cbs + c, p.cand_base + qrow * M + c);
+    for (int k = threadIdx.x; k < r; k += kThreads) cp_async4(b.h1s + k, p.h1 + qrow * r + k);
+  }
+  if (threadIdx.x == 0) cp_async4(b.rest, p.rest_lse + qrow);
   cp_async_commit();
 }
 
@@ -317,12 +418,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     s.red = reinterpret_cast<float*>(smem_raw + L.off[2]);
     s.uu = reinterpret_cast<float*>(smem_raw + L.off[3]);
     s.z = reinterpret_cast<float*>(smem_raw + L.off[4]);
-    s.w2s = reinterpret_cast<uint16_t*>(smem_raw + L.off[5]);
-    s.xs = reinterpret_cast<float*>(smem_raw + L.off[6]);
+    const int u = sh.dbuf ? 1 : 0;  // the odd buffer follows the even one
+    s.st0.w2s = reinterpret_cast<uint16_t*>(smem_raw + L.off[5]);
+    s.st0.xs = reinterpret_cast<float*>(smem_raw + L.off[6]);
+    s.st0.cbs = reinterpret_cast<float*>(smem_raw + L.off[8]);
+    s.st0.h1s = reinterpret_cast<float*>(smem_raw + L.off[9]);
+    s.st0.rest = reinterpret_cast<float*>(smem_raw + L.off[10]);
+    s.st1.w2s = reinterpret_cast<uint16_t*>(smem_raw + L.off[5] + u * al16(stage_one(sh, 0)));
+    s.st1.xs = reinterpret_cast<float*>(smem_raw + L.off[6] + u * al16(stage_one(sh, 1)));
+    s.st1.cbs = reinterpret_cast<float*>(smem_raw + L.off[8] + u * al16(stage_one(sh, 2)));
+    s.st1.h1s = reinterpret_cast<float*>(smem_raw + L.off[9] + u * al16(stage_one(sh, 3)));
+    s.st1.rest = reinterpret_cast<float*>(smem_raw + L.off[10] + u * al16(stage_one(sh, 4)));
+    s.w2s = s.st0.w2s;
+    s.xs = s.st0.xs;
     s.ctk = reinterpret_cast<int*>(smem_raw + L.off[7]);
-    s.cbs = reinterpret_cast<float*>(smem_raw + L.off[8]);
-    s.h1s = reinterpret_cast<float*>(smem_raw + L.off[9]);
-    s.rest = reinterpret_cast<float*>(smem_raw + L.off[10]);
+    s.cbs = s.st0.cbs;
+    s.h1s = s.st0.h1s;
+    s.rest = s.st0.rest;
     s.ctok = reinterpret_cast<int*>(smem_raw + L.off[11]);
     s.cslot = reinterpret_cast<int*>(smem_raw + L.off[12]);
     s.clogp = reinterpret_cast<float*>(smem_raw + L.off[13]);
@@ -374,7 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   // stage the first depth's request 0 (overlaps the root step and phase A)
   select_row_tokens(p, sh, s, 0, p.depth_first);
   __syncthreads();
-  stage_row(p, sh, s, static_cast<size_t>(p.depth_first - 1), j0, nj, p.depth_first != D);
+  auto buf = [&](int depth) -> Stage { return (depth & 1) ? s.st1 : s.st0; };
+  // on a barrier timeout: let the CTA's own copies land before it returns
+  auto drain = [&]() { cp_async_wait_all(); };
+  stage_row(p, sh, buf(p.depth_first), s.ctk, static_cast<size_t>(p.depth_first - 1), j0, nj,
+            p.depth_first != D);
 
   unsigned epoch = 0;
 
@@ -389,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       }
       const float* x = p.xtab + static_cast<size_t>(tok) * 3 * g;
       const float zg = sigmoidf_(x[g + jj]);
-      const float ng = tanhf(x[2 * g + jj]);
+      const float ng = tanhf_(x[2 * g + jj]);
       p.S[static_cast<size_t>(q * W) * g + jj] = (1.0f - zg) * ng;
     }
     if (blockIdx.x == 0) {
@@ -402,7 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         p.live[static_cast<size_t>(q) * W] = 0;
       }
     }
-    if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) return;
+    if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
+      drain();
+      return;
+    }
   }
 
   for (int i = p.depth_first; i <= p.depth_last; ++i) {
@@ -414,6 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     float* Snext = p.S + static_cast<size_t>(i & 1) * n_req * W * g;
     const int* live_prev = p.live + static_cast<size_t>((i - 1) & 1) * n_req * W;
     int* live_next = p.live + static_cast<size_t>(i & 1) * n_req * W;
+    // one request: the next depth's candidate data is staged now, into the
+    // other buffer (its last reader, depth i-1, finished before the barrier);
+    // it lands during this depth
+    if (sh.dbuf) s.ctk = s.tok_all + static_cast<size_t>(i - 1) * M;  // this depth's candidate tokens
 
     // ================= phase A: projections of the live states ==============
     for (int p0 = 0; p0 < P; p0 += kPC) {
@@ -434,6 +557,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           v[j] = *reinterpret_cast<const float4*>(Sprev + static_cast<size_t>(q * W + b) * g + 4 * k4);
         }
       }
+      // one request: the next depth's candidate data is staged now, into the
+      // other buffer (its last reader, depth i-1, finished before the
+      // barrier), while the state loads above are in flight; it lands during
+      // this depth
+      if (sh.dbuf && p0 == 0 && i < p.depth_last)
+        stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
+                  i + 1 != D);
 #pragma unroll
       for (int j = 0; j < kSLoads; ++j) {
         const int idx = tid + j * kThreads;
@@ -452,11 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       {
         const int gid = lane >> 2, tig = lane & 3;
         const int nk16 = (g + 15) / 16;
-        float acc[kMaxNTiles][4];
+        // high and low parts accumulate in separate chains
+        float acc[kMaxNTiles][4], acl[kMaxNTiles][4];
 #pragma unroll
         for (int nt = 0; nt < kMaxNTiles; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+          for (int e = 0; e < 4; ++e) {
+            acc[nt][e] = 0.0f;
+            acl[nt][e] = 0.0f;
+          }
         const int ntiles = cpad / 8;
         for (int kt = warp; kt < nk16; kt += kWarps) {
           const int k0 = kt * 16 + 2 * tig;
@@ -471,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wc);
               const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wc + 8);
               mma_bf16_16816(acc[nt], ah0, 0u, ah2, 0u, b0, b1);
-              mma_bf16_16816(acc[nt], al0, 0u, al2, 0u, b0, b1);
+              mma_bf16_16816(acl[nt], al0, 0u, al2, 0u, b0, b1);
             }
           }
         }
@@ -479,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         for (int nt = 0; nt < kMaxNTiles; ++nt) {
           if (nt < ntiles) {
             float* rw = s.red + (warp * kPC + gid) * cpad + nt * 8 + 2 * tig;
-            rw[0] = acc[nt][0];
-            rw[1] = acc[nt][1];
+            rw[0] = acc[nt][0] + acl[nt][0];
+            rw[1] = acc[nt][1] + acl[nt][1];
           }
         }
       }
@@ -499,7 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
     }
-    if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) return;
+    if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
+      drain();
+      return;
+    }
 
     // ================= phase B: corrected log-probs and selections ==========
     const int row_off = p.off[i];
@@ -510,35 +647,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         __syncthreads();
         select_row_tokens(p, sh, s, q, i);
         __syncthreads();
-        stage_row(p, sh, s, qrow, j0, nj, !last);
+        stage_row(p, sh, buf(i), s.ctk, qrow, j0, nj, !last);
+      }
+      {
+        const Stage cur = buf(i);
+        s.w2s = cur.w2s;
+        s.xs = cur.xs;
+        s.cbs = cur.cbs;
+        s.h1s = cur.h1s;
+        s.rest = cur.rest;
+      }
+      // the branches' u_W1 rows (tensor-core path) are loaded first, so that
+      // their latency overlaps the parent reads and the staging wait
+      float uv[kZLoads];
+      if (sh.mma_b) {
+        const float* ub = p.uW1 + static_cast<size_t>(q * W) * r;  // rows q*W .. q*W+Lp-1
+        const int nz = Lp * r;
+#pragma unroll
+        for (int j = 0; j < kZLoads; ++j) {
+          const int idx = tid + j * kThreads;
+          uv[j] = idx < nz ? ub[idx] : 0.0f;
+        }
       }
       for (int b = tid; b < Lp; b += kThreads) {
         const int node = live_prev[static_cast<size_t>(q) * W + b];
         s.pnode[b] = node;
         s.pscore[b] = (node >= 0 && node < p.N1) ? p.node_score[static_cast<size_t>(q) * p.N1 + node] : 0.0f;
       }
-      cp_async_wait_all();
+      if (sh.dbuf && i < p.depth_last)
+        cp_async_wait_group1();  // this depth's group; the next depth's may still fly
+      else
+        cp_async_wait_all();
       __syncthreads();
       const float rest = s.rest[0];
       if (sh.mma_b) {
         // ---- z = SiLU(h1 + u) of every live branch -> bf16 high/low rows ----
         const int zs = r + 8;
         {
-          const float* ub = p.uW1 + static_cast<size_t>(q * W) * r;  // rows q*W .. q*W+Lp-1
           const int nz = Lp * r;
-          float uv[kZLoads];
-#pragma unroll
-          for (int j = 0; j < kZLoads; ++j) {
-            const int idx = tid + j * kThreads;
-            uv[j] = idx < nz ? ub[idx] : 0.0f;
-          }
 #pragma unroll
           for (int j = 0; j < kZLoads; ++j) {
             const int idx = tid + j * kThreads;
             if (idx < nz) {
               const int b = idx / r, k = idx - b * r;
               const float x = s.h1s[k] + uv[j];
-              const float zv = x / (1.0f + expf(-x));
+              const float zv = siluf_(x);
               const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
               const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
               s.zh[static_cast<size_t>(b) * zs + k] = __bfloat16_as_ushort(hi);
@@ -553,24 +706,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           const int mtiles = (Lp + 15) / 16, ntiles = M / 8;
           for (int t = warp; t < mtiles * ntiles; t += kWarps) {
             const int mt = t / ntiles, nt = t - mt * ntiles;
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // four independent accumulation chains (high/low parts x even/odd
+            // k16 steps) keep the dependent-MMA latency short
+            float a0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float a2[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a3[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             const uint16_t* h0 = s.zh + static_cast<size_t>(mt * 16 + gid) * zs;
             const uint16_t* l0 = s.zl + static_cast<size_t>(mt * 16 + gid) * zs;
             const uint16_t* wr = s.w2s + static_cast<size_t>(nt * 8 + gid) * zs;
-#pragma unroll 4
-            for (int kt = 0; kt < r / 16; ++kt) {
+            // rows 8..15 of the tile hold branches only when Lp > mt*16 + 8;
+            // otherwise their fragments are zero and not read
+            const bool upper = mt * 16 + 8 < Lp;
+            auto kstep = [&](float (&dh)[4], float (&dl)[4], int kt) {
               const int k0 = kt * 16 + 2 * tig;
               const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wr + k0);
               const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wr + k0 + 8);
-              mma_bf16_16816(acc, *reinterpret_cast<const uint32_t*>(h0 + k0),
-                             *reinterpret_cast<const uint32_t*>(h0 + 8 * zs + k0),
+              mma_bf16_16816(dh, *reinterpret_cast<const uint32_t*>(h0 + k0),
+                             upper ? *reinterpret_cast<const uint32_t*>(h0 + 8 * zs + k0) : 0u,
                              *reinterpret_cast<const uint32_t*>(h0 + k0 + 8),
-                             *reinterpret_cast<const uint32_t*>(h0 + 8 * zs + k0 + 8), b0, b1);
-              mma_bf16_16816(acc, *reinterpret_cast<const uint32_t*>(l0 + k0),
-                             *reinterpret_cast<const uint32_t*>(l0 + 8 * zs + k0),
+                             upper ? *reinterpret_cast<const uint32_t*>(h0 + 8 * zs + k0 + 8) : 0u, b0, b1);
+              mma_bf16_16816(dl, *reinterpret_cast<const uint32_t*>(l0 + k0),
+                             upper ? *reinterpret_cast<const uint32_t*>(l0 + 8 * zs + k0) : 0u,
                              *reinterpret_cast<const uint32_t*>(l0 + k0 + 8),
-                             *reinterpret_cast<const uint32_t*>(l0 + 8 * zs + k0 + 8), b0, b1);
+                             upper ? *reinterpret_cast<const uint32_t*>(l0 + 8 * zs + k0 + 8) : 0u, b0, b1);
+            };
+            const int nk = r / 16;
+#pragma unroll 2
+            for (int kt = 0; kt < nk; kt += 2) {
+              kstep(a0, a1, kt);
+              if (kt + 1 < nk) kstep(a2, a3, kt + 1);
             }
+            float acc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = (a0[e] + a2[e]) + (a1[e] + a3[e]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int b = mt * 16 + gid + (e >= 2 ? 8 : 0);
@@ -583,7 +750,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           }
         }
         __syncthreads();
-        // ---- per branch: log-partition, top-K by rank counting, children by token ----
+        // ---- per branch: log-partition, top-K, children by token ----
+        if (M == 64 && K <= 32) {
+          // the branch's 64 keys sorted in registers (one warp per branch)
+          for (int b = warp; b < Lp; b += kWarps) {
+            const uint64_t* kr = s.lamkey + static_cast<size_t>(b) * 64;
+            uint64_t ka = kr[2 * lane], kb2 = kr[2 * lane + 1];
+            int pa = 2 * lane, pb = 2 * lane + 1;
+            const float la = key_f32(static_cast<uint32_t>(ka >> 32)), lb = key_f32(static_cast<uint32_t>(kb2 >> 32));
+            const float lmax = warp_max(fmaxf(rest, fmaxf(la, lb)));
+            const float se = warp_sum(expf(la - lmax) + expf(lb - lmax)) + expf(rest - lmax);
+            const float logZ = lmax + logf(se);
+            warp_sort64_desc(ka, kb2, pa, pb);
+            uint64_t wk;
+            int wc;
+            warp_sorted_at(ka, kb2, pa, pb, lane, wk, wc);  // lane w < K holds the w-th best
+            const int tok = static_cast<int>(rank_key_id(wk));
+            int trank = 0;
+            for (int m = 0; m < K; ++m) trank += __shfl_sync(0xFFFFFFFFu, tok, m) < tok ? 1 : 0;
+            if (lane < K) {
+              const float lp = key_f32(static_cast<uint32_t>(wk >> 32)) - logZ;
+              const int slot = b * K + trank;
+              s.ctok[slot] = tok;
+              s.cslot[slot] = wc;
+              s.clogp[slot] = lp;
+              s.cscore[slot] = s.pscore[b] + lp;
+            }
+          }
+        } else
         for (int b = warp; b < Lp; b += kWarps) {
           const uint64_t* kb = s.lamkey + static_cast<size_t>(b) * M;
           float lmax = rest;
@@ -637,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               const int k = lane + 32 * j;
               if (k < r) {
                 const float x = s.h1s[k] + uv[j];
-                zw[k] = x / (1.0f + expf(-x));
+                zw[k] = siluf_(x);
               }
             }
           }
@@ -813,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           const float h = Sprev[static_cast<size_t>(q * W + b) * g + j0 + jj];
           const float rg = sigmoidf_(x[jj] + uu[jj]);
           const float zg = sigmoidf_(x[nj + jj] + uu[nj + jj]);
-          const float ng = tanhf(x[2 * nj + jj] + rg * uu[2 * nj + jj]);
+          const float ng = tanhf_(x[2 * nj + jj] + rg * uu[2 * nj + jj]);
           Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = (1.0f - zg) * ng + zg * h;
         }
       } else if (blockIdx.x == 0 && p.live_out) {
@@ -821,12 +1015,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       }
     }
     if (i < p.depth_last) {
-      // stage the next depth's request 0 now: the copies overlap the barrier
-      __syncthreads();
-      select_row_tokens(p, sh, s, 0, i + 1);
-      __syncthreads();
-      stage_row(p, sh, s, static_cast<size_t>(i), j0, nj, i + 1 != D);
-      if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) return;
+      if (!sh.dbuf) {
+        // stage the next depth's request 0 now: the copies overlap the barrier
+        __syncthreads();
+        select_row_tokens(p, sh, s, 0, i + 1);
+        if (!sh.prefetch) __syncthreads();
+        stage_row(p, sh, buf(i + 1), s.ctk, static_cast<size_t>(i), j0, nj, i + 1 != D);
+      }
+      if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
+        drain();
+        return;
+      }
     }
   }
 
@@ -869,7 +1068,7 @@ bool is_q4b(const ChainParams& p, int grid) {
   const Shape b = DimsQ4B::kShape;
   return grid == 128 && a.g == b.g && a.r == b.r && a.M == b.M && a.K == b.K && a.W == b.W &&
          a.n_req == b.n_req && a.D == b.D && a.jper == b.jper && a.rper == b.rper && a.cpad == b.cpad &&
-         a.stage_w2 == b.stage_w2 && a.mma_b == b.mma_b && a.prefetch == b.prefetch;
+         a.stage_w2 == b.stage_w2 && a.mma_b == b.mma_b && a.prefetch == b.prefetch && a.dbuf == b.dbuf;
 }
 
 }  // namespace

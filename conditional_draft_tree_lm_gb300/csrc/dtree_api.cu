@@ -326,7 +326,7 @@ size_t dt_workspace_bytes(const dt_config* cfg) {
   tp.V = cfg->V;
   tp.rows = cfg->n_req * t.D;
   tp.M = cfg->M;
-  topm_plan(tp, 148);
+  topm_plan(tp, 1 << 20);  // the most chunks any SM count can plan: an upper bound
   Layout L;
   layout(*cfg, t, tp, L);
   return L.total + L.xtab;

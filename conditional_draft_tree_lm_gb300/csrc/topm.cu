@@ -2,24 +2,29 @@
 // row of base logits ("Resumen Técnico: DominoTree", Componentes Principales,
 // 2. Restricción de Candidatos (Top-M)).
 //
-// One kernel, grid (S chunks, rows).  Each CTA holds one chunk of one row
-// (<= 16384 logits, 32 per thread in registers) and finds the chunk's top-M:
-//   1. max, mean and standard deviation of the chunk;
-//   2. a histogram of the values within 4 sigma of the max in quarter-sigma
-//      buckets; the tightest bucket edge that keeps >= M values is chosen, so
-//      every one of the chunk's top-M lies above it;
-//   3. the values above that edge (typically M..2M of them) are collected with
-//      an exact count, and an exact radix select of the M largest runs on that
-//      small set, ties going to the lower token id.
-// When the collected count is outside [M, kCandCap] (flat or degenerate
-// chunks) the chunk is radix-selected in full.  The chunk also reports the max
-// of logit/T, the sum of exp(logit/T - max) over its non-selected tokens and
-// its M-th largest logit.  The last CTA of a row (a per-row arrival counter;
-// nothing waits) merges: the largest of the chunks' M-th values is a lower
-// bound on the row's M-th value, so only chunk candidates at or above it can
-// win; the exact top-M among those is sorted by (logit desc, id asc), and
-//   rest_lse = log( sum_chunks part_sum e^{part_max} + sum_{dropped} e^{logit/T} ),
-// so every non-candidate enters the log-partition exactly once.
+// One kernel, grid (S chunks, rows), 512 threads.  Each CTA holds one chunk of
+// one row (<= 16384 logits, 32 per thread in registers; padding is -inf) and
+// writes the chunk's top-M, sorted by (logit desc, token id asc):
+//   1. the chunk's max, and the mean and standard deviation of a sample (the
+//      first 4 values of every thread);
+//   2. from the sample, a threshold mx - c*sigma (c on a ladder 1 .. 4) that
+//      should keep about 2M values;
+//   3. the values at or above it are counted exactly (warp scans and one
+//      shared-memory atomic per warp) and collected; too few (< M) moves to
+//      the next rung and counts again, too many (> 512) or none left falls back
+//      to a radix select of the whole chunk;
+//   4. the candidates are ranked exactly by counting (a group of threads per
+//      candidate): a candidate's rank is its position in the sorted top-M.
+// The chunk also reports the max of logit/T and the sum of exp(logit/T - max)
+// over its non-selected tokens.
+//
+// The last CTA of a row (a per-row arrival counter; nothing waits) merges the
+// S sorted lists.  The M-th largest key among the first t entries of every
+// list is a lower bound on the row's M-th largest (a subset's M-th largest
+// never exceeds the whole set's), so only entries at or above it can win;
+// those few are ranked exactly and written in order, and
+//   rest_lse = log( sum_chunks part_sum e^{part_max} + sum_{losing entries} e^{logit/T} ),
+// so every non-candidate token enters the log-partition exactly once.
 #include "common.cuh"
 #include "kernels.h"
 #include "select.cuh"
@@ -30,24 +35,16 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kVPT = 32;            // values per thread: chunk <= kThreads * kVPT
+constexpr int kVPT = 32;              // values per thread: chunk <= kThreads * kVPT
 constexpr int kMaxChunk = kThreads * kVPT;
-constexpr int kMaxMerge = 8192;
-constexpr int kBuckets = 16;
-constexpr int kCandCap = 2048;      // candidates kept by the threshold filter
+constexpr int kMaxMerge = 8192;       // S * M entries merged per row
+constexpr int kSample = 4;            // values per thread in the sample
+constexpr int kRungs = 8;             // threshold ladder
+constexpr int kCandCap = kThreads;    // candidates ranked in the partial phase
+constexpr int kMergeCap = 2048;       // merge candidates ranked among themselves
 
-DT_DEVINL float block_max(float v, float* red) {
-  v = warp_max(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float m = threadIdx.x < kWarps ? red[threadIdx.x] : -INFINITY;
-    m = warp_max(m);
-    if (threadIdx.x == 0) red[kWarps] = m;
-  }
-  __syncthreads();
-  return red[kWarps];
+DT_DEVINL float rung_c(int k) {
+  return k < 5 ? 1.0f + 0.25f * static_cast<float>(k) : (k == 5 ? 2.5f : (k == 6 ? 3.0f : 4.0f));
 }
 
 DT_DEVINL float block_sum(float v, float* red) {
@@ -64,321 +61,359 @@ DT_DEVINL float block_sum(float v, float* red) {
   return red[kWarps];
 }
 
-// Index-ordered compaction of the keys >= the radix threshold (exactly `need`
-// of the keys equal to t, the earliest ones).  Calls emit(e, key, pos) for each
-// selected element in index order, and skip(e, key) for the others.
-template <class Emit, class Skip>
-DT_DEVINL void compact_topk(const uint32_t* keys, int n, uint32_t t, int need, int* scan, Emit emit, Skip skip) {
-  const int seg = (n + blockDim.x - 1) / blockDim.x;
-  const int s0 = min(n, static_cast<int>(threadIdx.x) * seg);
-  const int s1 = min(n, s0 + seg);
-  int ties = 0;
-  for (int e = s0; e < s1; ++e) ties += (keys[e] == t);
-  int tot;
-  const int tie_base = block_exclusive_scan(ties, scan, &tot);
-  int cnt = 0;
-  {
-    int tb = tie_base;
-    for (int e = s0; e < s1; ++e) {
-      const uint32_t k = keys[e];
-      if (k > t || (k == t && tb++ < need)) ++cnt;
-    }
+// Slot of this thread's first flagged value in a block-wide list: a warp scan
+// and one atomic per warp on *counter (slot order across warps is arbitrary).
+DT_DEVINL int claim_slots(int mine, int* counter) {
+  const int lane = threadIdx.x & 31;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
   }
-  const int out_base = block_exclusive_scan(cnt, scan, &tot);
-  int tb = tie_base, o = out_base;
-  for (int e = s0; e < s1; ++e) {
-    const uint32_t k = keys[e];
-    if (k > t || (k == t && tb++ < need)) {
-      emit(e, k, o);
-      ++o;
-    } else {
-      skip(e, k);
-    }
-  }
+  int base = 0;
+  if (lane == 31 && incl > 0) base = atomicAdd(counter, incl);
+  base = __shfl_sync(0xFFFFFFFFu, base, 31);
+  return base + incl - mine;
 }
 
-// Exact top-k among c candidates in shared memory (value keys ck, token ids
-// cid, any order, ids distinct): radix select on the value key; at the
-// threshold the lower ids win.  Sets sel[e] = 1 for the k winners.
-DT_DEVINL void small_topk(const uint32_t* ck, const uint32_t* cid, int c, int k, uint8_t* sel, uint32_t* hist,
-                          int hist_words, uint32_t* state) {
-  if (k >= c) {
-    for (int e = threadIdx.x; e < c; e += blockDim.x) sel[e] = 1;
-    __syncthreads();
-    return;
-  }
-  uint32_t t;
-  int need;
-  radix_select_kth_largest(ck, c, k, hist, hist_words, state, t, need);
-  for (int e = threadIdx.x; e < c; e += blockDim.x) {
-    const uint32_t ke = ck[e];
-    uint8_t s = ke > t ? 1 : 0;
-    if (ke == t) {
-      int rk = 0;
-      for (int f = 0; f < c; ++f) rk += (ck[f] == t && cid[f] < cid[e]) ? 1 : 0;
-      s = rk < need ? 1 : 0;
+// Exact ranks of keys[0, c) among themselves (the number of larger keys; keys
+// are distinct).  Each key is ranked by a group of g consecutive threads (g a
+// power of two <= 32, as many as the block allows), whose partial counts are
+// added with shuffles; fn(e, key, rank) then runs on the group's first thread.
+// Every thread of the block must call.
+template <class Fn>
+DT_DEVINL void rank_all(const uint64_t* keys, int c, Fn fn) {
+  int g = 1;
+  while (g < 32 && 2 * g * c <= kThreads) g <<= 1;
+  for (int base = 0; base < c * g; base += kThreads) {
+    const int idx = base + static_cast<int>(threadIdx.x);
+    const int e = idx / g, part = idx - e * g;
+    uint64_t ke = 0ull;
+    int rk = 0;
+    if (e < c) {
+      ke = keys[e];
+#pragma unroll 4
+      for (int f = part; f < c; f += g) rk += keys[f] > ke ? 1 : 0;
     }
-    sel[e] = s;
+    for (int o = 1; o < g; o <<= 1) rk += __shfl_xor_sync(0xFFFFFFFFu, rk, o);
+    if (e < c && part == 0) fn(e, ke, rk);
   }
-  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads) k_topm(const TopmParams p) {
-  extern __shared__ uint32_t dyn[];
+  extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ uint32_t hist[kWarps * 256];
   __shared__ uint32_t state[4];
   __shared__ int scan[40];
   __shared__ float red[kWarps + 1];
-  __shared__ float red3[3][kWarps + 1];
-  __shared__ unsigned cnt[kBuckets];
-  __shared__ int s_last, s_ncand;
+  __shared__ float red4[4][kWarps + 1];
+  __shared__ int rung_cnt[kWarps][kRungs];
+  __shared__ int s_rung, s_ncand, s_last;
+  __shared__ uint64_t s_lb;
+  // exp terms of losing candidates, stored at their rank and summed in rank
+  // order: the slot order of a candidate (claimed by atomics) never changes a
+  // result bit
+  __shared__ float s_term[kMergeCap];
+
+  // dynamic shared memory: a 64 KB area (chunk keys of the fallback, merge
+  // entries) followed by the candidate keys
+  uint64_t* big = reinterpret_cast<uint64_t*>(dyn);
+  uint64_t* cand = big + kMaxMerge;  // [kMergeCap]
 
   const int row = blockIdx.y, split = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int v0 = split * p.chunk;
   const int n = max(0, min(p.V, v0 + p.chunk) - v0);
   const float* x = p.logits + static_cast<size_t>(row) * p.V + v0;
   const float invT = 1.0f / p.T;
   const size_t q = static_cast<size_t>(row) * p.S + split;
   const int mloc = min(p.M, n);
-  // candidates (keys, ids, flags) live after the chunk-key area
-  uint32_t* ck = dyn + kMaxChunk;
-  uint32_t* cid = ck + kCandCap;
-  uint8_t* csel = reinterpret_cast<uint8_t*>(cid + kCandCap);
+  const int nv = n > tid ? min(kVPT, (n - tid + kThreads - 1) / kThreads) : 0;  // valid values of this thread
 
-  // ---------------- 1. the chunk in registers; max, mean, sigma ----------------
+  // ---------------- 1. the chunk in registers; max; sample statistics ----------------
   float vals[kVPT];
-  float mx = -INFINITY, sm = 0.0f, sq = 0.0f;
 #pragma unroll
-  for (int j = 0; j < kVPT; ++j) {
-    const int e = tid + j * kThreads;
-    vals[j] = e < n ? x[e] : -INFINITY;
-  }
+  for (int j = 0; j < kVPT; ++j) vals[j] = j < nv ? x[tid + j * kThreads] : -INFINITY;
+  float mx = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < kVPT; ++j) {
-    if (tid + j * kThreads < n) {
-      mx = fmaxf(mx, vals[j]);
+  for (int j = 0; j < kVPT; ++j) mx = fmaxf(mx, vals[j]);
+  float sm = 0.0f, sq = 0.0f, ns = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kSample; ++j)
+    if (j < nv) {
       sm += vals[j];
       sq += vals[j] * vals[j];
+      ns += 1.0f;
+    }
+  mx = warp_max(mx);
+  sm = warp_sum(sm);
+  sq = warp_sum(sq);
+  ns = warp_sum(ns);
+  if (lane == 0) {
+    red4[0][warp] = mx;
+    red4[1][warp] = sm;
+    red4[2][warp] = sq;
+    red4[3][warp] = ns;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    float a = tid < kWarps ? red4[0][tid] : -INFINITY;
+    float b = tid < kWarps ? red4[1][tid] : 0.0f;
+    float c = tid < kWarps ? red4[2][tid] : 0.0f;
+    float d = tid < kWarps ? red4[3][tid] : 0.0f;
+    a = warp_max(a);
+    b = warp_sum(b);
+    c = warp_sum(c);
+    d = warp_sum(d);
+    if (tid == 0) {
+      red4[0][kWarps] = a;
+      red4[1][kWarps] = b;
+      red4[2][kWarps] = c;
+      red4[3][kWarps] = d;
     }
   }
-  {
-    // max, sum and sum of squares in one block reduction
-    mx = warp_max(mx);
-    sm = warp_sum(sm);
-    sq = warp_sum(sq);
-    if (lane == 0) {
-      red3[0][tid >> 5] = mx;
-      red3[1][tid >> 5] = sm;
-      red3[2][tid >> 5] = sq;
-    }
-    __syncthreads();
-    if (tid < 32) {
-      float a = tid < kWarps ? red3[0][tid] : -INFINITY;
-      float b = tid < kWarps ? red3[1][tid] : 0.0f;
-      float c = tid < kWarps ? red3[2][tid] : 0.0f;
-      a = warp_max(a);
-      b = warp_sum(b);
-      c = warp_sum(c);
-      if (tid == 0) {
-        red3[0][kWarps] = a;
-        red3[1][kWarps] = b;
-        red3[2][kWarps] = c;
-      }
-    }
-    if (tid < kBuckets) cnt[tid] = 0u;
-    __syncthreads();
-    mx = red3[0][kWarps];
-    sm = red3[1][kWarps];
-    sq = red3[2][kWarps];
-  }
-  const float mean = n > 0 ? sm / n : 0.0f;
-  const float sigma = n > 0 ? sqrtf(fmaxf(sq / n - mean * mean, 0.0f)) : 0.0f;
+  __syncthreads();
+  mx = red4[0][kWarps];
+  const float nsamp = red4[3][kWarps];
+  const float mean = nsamp > 0.0f ? red4[1][kWarps] / nsamp : 0.0f;
+  const float sigma = nsamp > 0.0f ? sqrtf(fmaxf(red4[2][kWarps] / nsamp - mean * mean, 0.0f)) : 0.0f;
   const float mxT = mx * invT;
 
-  // ---------------- 2. histogram of the top 16 quarter-sigma buckets ----------------
-  const float step = 0.25f * sigma;
-  int chosen = -1;
-  const bool try_fast = mloc > 0 && mloc < n && step > 0.0f && step < INFINITY;
-  if (try_fast) {
-    const float inv_step = 1.0f / step;
+  // ---------------- 2. the first rung to try, from the sample ----------------
+  if (mloc < n && sigma > 0.0f) {
+    int cnt[kRungs];
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j) {
-      const float dd = (mx - vals[j]) * inv_step;  // padding (-inf) gives +inf: skipped
-      if (dd < static_cast<float>(kBuckets)) atomicAdd(&cnt[static_cast<int>(dd)], 1u);
+    for (int k = 0; k < kRungs; ++k) cnt[k] = 0;
+#pragma unroll
+    for (int j = 0; j < kSample; ++j)
+#pragma unroll
+      for (int k = 0; k < kRungs; ++k) cnt[k] += (j < nv && vals[j] >= mx - rung_c(k) * sigma) ? 1 : 0;
+#pragma unroll
+    for (int k = 0; k < kRungs; ++k) {
+      const int c = __reduce_add_sync(0xFFFFFFFFu, cnt[k]);
+      if (lane == 0) rung_cnt[warp][k] = c;
     }
     __syncthreads();
-    unsigned cum = 0;
-    for (int k = 0; k < kBuckets; ++k) {
-      cum += cnt[k];
-      if (cum >= static_cast<unsigned>(mloc)) {
-        if (cum <= static_cast<unsigned>(kCandCap)) chosen = k;
-        break;
-      }
+    if (warp == 0) {
+      // lane k totals rung k; the first rung expected to keep >= 2M values
+      int c = 0;
+      if (lane < kRungs)
+        for (int w = 0; w < kWarps; ++w) c += rung_cnt[w][lane];
+      const float est = static_cast<float>(c) * (static_cast<float>(n) / nsamp);
+      const unsigned ok = __ballot_sync(0xFFFFFFFFu, lane < kRungs && est >= 2.0f * mloc);
+      if (lane == 0) s_rung = ok ? __ffs(ok) - 1 : kRungs - 1;
     }
+  } else if (tid == 0) {
+    s_rung = mloc >= n ? kRungs : -1;  // all values are candidates / fall back
   }
+  __syncthreads();
 
+  // ---------------- 3. exact count and collection above the threshold ----------------
   float rest = 0.0f;
-  float kth = -INFINITY;  // the chunk's M-th largest logit (when n > M)
-  // ---------------- 3. collect above the edge (exact count) ----------------
-  int csize = 0;
-  float th = INFINITY;
-  int pos = 0;
-  if (chosen >= 0) {
-    th = mx - static_cast<float>(chosen + 1) * step;
-    int mine = 0;
+  int k = s_rung;
+  int c = 0;
+  uint32_t flags = 0u;
+  bool fast = k >= 0;
+  while (fast) {
+    const float th = k >= kRungs ? -INFINITY : mx - rung_c(k) * sigma;
+    flags = 0u;
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j) mine += (vals[j] >= th) ? 1 : 0;
-    pos = block_exclusive_scan(mine, scan, &csize);
-    // the buckets only steer the choice; the exact count decides
-    if (csize < mloc || csize > kCandCap) chosen = -1;
-  }
-  if (chosen >= 0) {
+    for (int j = 0; j < kVPT; ++j)
+      if (j < nv && vals[j] >= th) flags |= 1u << j;
+    if (tid == 0) s_ncand = 0;
+    __syncthreads();
+    const int mine = __popc(flags);
+    int pos = claim_slots(mine, &s_ncand);
+    if (pos + mine <= kCandCap) {
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j) {
-      const int e = tid + j * kThreads;
-      if (vals[j] >= th) {
-        ck[pos] = f32_key(vals[j]);
-        cid[pos] = static_cast<uint32_t>(v0 + e);
-        ++pos;
-      } else if (e < n) {
-        rest += expf(vals[j] * invT - mxT);
-      }
+      for (int j = 0; j < kVPT; ++j)
+        if ((flags >> j) & 1u) cand[pos++] = rank_key(vals[j], static_cast<uint32_t>(v0 + tid + j * kThreads));
     }
     __syncthreads();
-    small_topk(ck, cid, csize, mloc, csel, hist, 256, state);
-    int mine_sel = 0;
-    for (int e = tid; e < csize; e += kThreads) mine_sel += csel[e];
-    int wrote;
-    int o = block_exclusive_scan(mine_sel, scan, &wrote);
-    uint32_t kmin = 0xFFFFFFFFu;
-    for (int e = tid; e < csize; e += kThreads) {
-      if (csel[e]) {
-        p.part_id[q * p.M + o] = static_cast<int>(cid[e]);
-        p.part_val[q * p.M + o] = key_f32(ck[e]);
-        kmin = min(kmin, ck[e]);
-        ++o;
-      } else {
-        rest += expf(key_f32(ck[e]) * invT - mxT);
-      }
+    c = s_ncand;
+    __syncthreads();  // every thread has read the count before a retry resets it
+    if (c >= mloc && c <= kCandCap) break;      // the candidate set
+    if (c < mloc && k + 1 < kRungs) {          // too few: next rung
+      ++k;
+      continue;
     }
-    // the M-th largest = the smallest winner
-    kth = -block_max(-key_f32(kmin == 0xFFFFFFFFu ? f32_key(INFINITY) : kmin), red);
-  } else {
-    // ---------------- fallback: full radix select over the chunk ----------------
-    uint32_t* keys = dyn;
+    fast = false;                               // too many, or the ladder is exhausted
+  }
+  __syncthreads();
+
+  if (fast) {
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j) {
-      const int e = tid + j * kThreads;
-      if (e < n) keys[e] = f32_key(vals[j]);
-    }
+    for (int j = 0; j < kVPT; ++j)
+      if (!((flags >> j) & 1u)) rest += __expf(vals[j] * invT - mxT);  // padding gives 0
+    // ---------------- 4. exact ranks: the sorted partial list ----------------
+    rank_all(cand, c, [&](int, uint64_t ke, int rk) {
+      const float v = key_f32(static_cast<uint32_t>(ke >> 32));
+      if (rk < mloc) {
+        p.part_id[q * p.M + rk] = static_cast<int>(rank_key_id(ke));
+        p.part_val[q * p.M + rk] = v;
+        if (rk == mloc - 1) p.part_kth[q] = (mloc < n) ? v : -INFINITY;
+      } else {
+        s_term[rk] = expf(v * invT - mxT);
+      }
+    });
+    __syncthreads();
+    if (tid >= mloc && tid < c) rest += s_term[tid];  // c <= kCandCap = kThreads
+  } else {
+    // ---------------- fallback: radix select over the whole chunk ----------------
+    uint32_t* keys = reinterpret_cast<uint32_t*>(big);
+#pragma unroll
+    for (int j = 0; j < kVPT; ++j)
+      if (j < nv) keys[tid + j * kThreads] = f32_key(vals[j]);
     __syncthreads();
     uint32_t t = 0;
     int need = n;
-    if (mloc > 0 && mloc < n) {
-      radix_select_kth_largest(keys, n, mloc, hist, static_cast<int>(sizeof(hist) / 4), state, t, need);
-      kth = key_f32(t);
+    radix_select_kth_largest(keys, n, mloc, hist, kWarps * 256, state, t, need);
+    // keys above t win, plus the `need` lowest-indexed keys equal to t
+    uint32_t tie_mask = 0u;  // bit j: element tid + j*kThreads equals t
+#pragma unroll
+    for (int j = 0; j < kVPT; ++j)
+      if (j < nv && f32_key(vals[j]) == t) tie_mask |= 1u << j;
+    int tot;
+    (void)block_exclusive_scan(__popc(tie_mask), scan, &tot);
+    uint32_t tie_win = 0u;  // bit j: element tid + j*kThreads is a winning tie
+    if (tot <= need) {
+      tie_win = tie_mask;
+    } else {
+      // index order is j-major (e = tid + j * kThreads): one scan per slice
+      int before = 0;
+      for (int j = 0; j < kVPT; ++j) {
+        const int f = static_cast<int>((tie_mask >> j) & 1u);
+        int slice;
+        const int at = block_exclusive_scan(f, scan, &slice) + before;
+        if (f && at < need) tie_win |= 1u << j;
+        before += slice;
+      }
     }
-    compact_topk(
-        keys, n, t, need, scan,
-        [&](int e, uint32_t k, int o) {
-          p.part_id[q * p.M + o] = v0 + e;
-          p.part_val[q * p.M + o] = key_f32(k);
-        },
-        [&](int, uint32_t k) { rest += expf(key_f32(k) * invT - mxT); });
+    uint32_t win = tie_win;
+#pragma unroll
+    for (int j = 0; j < kVPT; ++j)
+      if (j < nv && f32_key(vals[j]) > t) win |= 1u << j;
+    int wrote;
+    int pos = block_exclusive_scan(__popc(win), scan, &wrote);
+#pragma unroll
+    for (int j = 0; j < kVPT; ++j) {
+      if ((win >> j) & 1u) {
+        cand[pos++] = rank_key(vals[j], static_cast<uint32_t>(v0 + tid + j * kThreads));
+      } else {
+        rest += __expf(vals[j] * invT - mxT);  // padding gives 0
+      }
+    }
+    __syncthreads();
+    rank_all(cand, mloc, [&](int, uint64_t ke, int rk) {
+      const float v = key_f32(static_cast<uint32_t>(ke >> 32));
+      p.part_id[q * p.M + rk] = static_cast<int>(rank_key_id(ke));
+      p.part_val[q * p.M + rk] = v;
+      if (rk == mloc - 1) p.part_kth[q] = (mloc < n) ? v : -INFINITY;
+    });
   }
   rest = block_sum(rest, red);
   if (tid == 0) {
     p.part_max[q] = mxT;
     p.part_sum[q] = rest;
     p.part_cnt[q] = mloc;
-    p.part_kth[q] = (mloc < n) ? kth : -INFINITY;
   }
 
   // ---------------- last CTA of the row merges ----------------
-  __threadfence();
+  // (the barrier orders the CTA's writes before thread 0's fence and arrival;
+  // the arriving-last CTA's fence orders its reads after every arrival)
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&p.row_done[row], 1u) == static_cast<unsigned>(p.S - 1);
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(&p.row_done[row], 1u) == static_cast<unsigned>(p.S - 1);
+    __threadfence();
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
   const size_t rb = static_cast<size_t>(row) * p.S;
-  float gmax = -INFINITY, lb = -INFINITY;
-  for (int s = tid; s < p.S; s += kThreads) {
-    gmax = fmaxf(gmax, p.part_max[rb + s]);
-    lb = fmaxf(lb, p.part_kth[rb + s]);
+  const int S = p.S, M = p.M;
+  const int total = S * M;
+  // every thread reads the S chunk maxima itself (no block reduction)
+  float gmax = -INFINITY;
+  for (int s2 = 0; s2 < S; ++s2) gmax = fmaxf(gmax, p.part_max[rb + s2]);
+  // entries e = s*M + j; value, id and list length are read together (one
+  // round trip); slots past a list's length hold stale data and get key 0
+  for (int e = tid; e < total; e += kThreads) {
+    const int s2 = e / M, j = e - s2 * M;
+    const float v = p.part_val[rb * M + e];
+    const int id = p.part_id[rb * M + e];
+    const int cnt = p.part_cnt[rb + s2];
+    big[e] = j < cnt ? rank_key(v, static_cast<uint32_t>(id)) : 0ull;
   }
-  gmax = block_max(gmax, red);
-  lb = block_max(lb, red);
-  // candidates at or above the lower bound (slot order, by a block scan); the
-  // others feed the log-partition
+  if (tid == 0) {
+    s_lb = 0ull;
+    s_ncand = 0;
+  }
+  __syncthreads();
+  // lower bound: the M-th largest key among the first t entries of every list
+  const int t = min(M, max(1, (2 * M + S - 1) / S));
+  const int nsub = S * t;  // <= 2M + S <= kMergeCap
+  if (nsub >= M) {
+    for (int u = tid; u < nsub; u += kThreads) {
+      const int s2 = u / t, j = u - s2 * t;
+      cand[u] = big[s2 * M + j];
+    }
+    __syncthreads();
+    rank_all(cand, nsub, [&](int, uint64_t ke, int rk) {
+      if (ke != 0ull && rk == M - 1) s_lb = ke;
+    });
+  }
+  __syncthreads();
+  const uint64_t lb = s_lb;
+  // candidates: entries at or above the bound; the others feed the log-partition
   float rest2 = 0.0f;
-  const int total = p.S * p.M;
-  const int per = (total + kThreads - 1) / kThreads;  // contiguous slots per thread
+  const int per = (total + kThreads - 1) / kThreads;
   const int e0 = min(total, tid * per), e1 = min(total, e0 + per);
   int mine_c = 0;
   for (int e = e0; e < e1; ++e) {
-    const int s = e / p.M, j = e - s * p.M;
-    if (j < p.part_cnt[rb + s] && p.part_val[(rb + s) * p.M + j] >= lb) ++mine_c;
+    const uint64_t k2 = big[e];
+    if (k2 == 0ull) continue;
+    if (k2 >= lb) ++mine_c;
+    else rest2 += expf(key_f32(static_cast<uint32_t>(k2 >> 32)) * invT - gmax);
   }
-  int ncand;
-  int at = block_exclusive_scan(mine_c, scan, &ncand);
+  int at = claim_slots(mine_c, &s_ncand);
   for (int e = e0; e < e1; ++e) {
-    const int s = e / p.M, j = e - s * p.M;
-    if (j < p.part_cnt[rb + s]) {
-      const float v = p.part_val[(rb + s) * p.M + j];
-      if (v >= lb) {
-        if (at < kCandCap) {
-          ck[at] = f32_key(v);
-          cid[at] = static_cast<uint32_t>(p.part_id[(rb + s) * p.M + j]);
-        }
-        ++at;
-      } else {
-        rest2 += expf(v * invT - gmax);
-      }
+    const uint64_t k2 = big[e];
+    if (k2 != 0ull && k2 >= lb) {
+      if (at < kMergeCap) cand[at] = k2;
+      ++at;
     }
   }
-  if (tid == 0) s_ncand = ncand;
   __syncthreads();
-  const int nc = min(s_ncand, kCandCap);
-  if (tid == 0 && s_ncand > kCandCap) dt_report(p.status, DT_DEV_BOUNDS);
-  small_topk(ck, cid, nc, p.M, csel, hist, 256, state);
-  // winners into hist (reused): ids then keys; the rest feeds the log-partition
-  uint32_t* win_id = hist;
-  uint32_t* win_key = hist + p.M;
-  int mine_sel = 0;
-  for (int e = tid; e < nc; e += kThreads) mine_sel += csel[e];
-  int wrote;
-  int o = block_exclusive_scan(mine_sel, scan, &wrote);
-  for (int e = tid; e < nc; e += kThreads) {
-    if (csel[e]) {
-      if (o < p.M) {
-        win_id[o] = cid[e];
-        win_key[o] = ck[e];
-      }
-      ++o;
+  const int nc = s_ncand;
+  // exact ranks of the candidates: among themselves, or (many candidates)
+  // against every entry, where entries below the bound never outrank one
+  const bool compact = nc <= kMergeCap;
+  const uint64_t* pool = compact ? cand : big;
+  const int npool = compact ? nc : total;
+  rank_all(pool, npool, [&](int, uint64_t ke, int rk) {
+    if (ke == 0ull || ke < lb) return;
+    if (rk < M) {
+      p.cand_tok[static_cast<size_t>(row) * M + rk] = static_cast<int>(rank_key_id(ke));
+      p.cand_base[static_cast<size_t>(row) * M + rk] = key_f32(static_cast<uint32_t>(ke >> 32));
     } else {
-      rest2 += expf(key_f32(ck[e]) * invT - gmax);
+      const float term = expf(key_f32(static_cast<uint32_t>(ke >> 32)) * invT - gmax);
+      if (compact) s_term[rk] = term;  // rk < nc <= kMergeCap
+      else rest2 += term;              // entry order: already deterministic
     }
+  });
+  if (compact) {
+    __syncthreads();
+    for (int i = M + tid; i < nc; i += kThreads) rest2 += s_term[i];
   }
-  for (int s = tid; s < p.S; s += kThreads) {
-    const float ps = p.part_sum[rb + s];
-    if (ps > 0.0f) rest2 += ps * expf(p.part_max[rb + s] - gmax);
+  for (int s2 = tid; s2 < S; s2 += kThreads) {
+    const float ps = p.part_sum[rb + s2];
+    if (ps > 0.0f) rest2 += ps * expf(p.part_max[rb + s2] - gmax);
   }
   rest2 = block_sum(rest2, red);
-  // order the winners by (logit desc, id asc)
-  const int nw = min(wrote, p.M);
-  for (int a = tid; a < nw; a += kThreads) {
-    const uint64_t ka = (static_cast<uint64_t>(win_key[a]) << 32) | (0xFFFFFFFFu - win_id[a]);
-    int pos2 = 0;
-    for (int b = 0; b < nw; ++b)
-      pos2 += ((static_cast<uint64_t>(win_key[b]) << 32) | (0xFFFFFFFFu - win_id[b])) > ka;
-    p.cand_tok[static_cast<size_t>(row) * p.M + pos2] = static_cast<int>(win_id[a]);
-    p.cand_base[static_cast<size_t>(row) * p.M + pos2] = key_f32(win_key[a]);
-  }
   if (tid == 0) {
-    if (nw != p.M) dt_report(p.status, DT_DEV_BOUNDS);
+    if (nc < M) dt_report(p.status, DT_DEV_BOUNDS);
     p.rest_lse[row] = rest2 > 0.0f ? gmax + logf(rest2) : -INFINITY;
     p.row_done[row] = 0u;  // ready for the next round
   }
@@ -387,20 +422,18 @@ __global__ void __launch_bounds__(kThreads) k_topm(const TopmParams p) {
 }  // namespace
 
 void topm_plan(TopmParams& p, int num_sms) {
-  int S = (p.V + kMaxChunk - 1) / kMaxChunk;
-  // 2 CTAs fit per SM (registers); rows * S <= 2 * SMs keeps the grid in one wave
-  const int want = max(1, (2 * num_sms) / p.rows);
-  const int cap_small = max(1, p.V / (2 * p.M));          // chunks of >= 2M logits
-  int S2 = min(want, cap_small);
-  if (S2 > S) S = S2;
-  const int cap_merge = max(1, kMaxMerge / p.M);
-  if (S > cap_merge) S = cap_merge;
+  // one CTA per SM over all rows (one wave), chunks of at most kMaxChunk
+  // logits and at least 2M, and at most kMaxMerge entries per row to merge
+  int S = max(1, num_sms / max(1, p.rows));
+  S = max(S, (p.V + kMaxChunk - 1) / kMaxChunk);
+  S = min(S, max(1, p.V / (2 * p.M)));
+  S = min(S, max(1, kMaxMerge / p.M));
   p.S = S;
   p.chunk = (p.V + S - 1) / S;
 }
 
 size_t topm_partial_smem(const TopmParams&) {
-  return static_cast<size_t>(kMaxChunk) * 4 + static_cast<size_t>(kCandCap) * 9 + 16;
+  return static_cast<size_t>(kMaxMerge) * 8 + static_cast<size_t>(kMergeCap) * 8;
 }
 
 size_t topm_merge_smem(const TopmParams& p) { return topm_partial_smem(p); }
@@ -408,7 +441,7 @@ size_t topm_merge_smem(const TopmParams& p) { return topm_partial_smem(p); }
 cudaError_t topm_prepare() { return dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm)); }
 
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {
-  if (p.chunk > kMaxChunk || p.S * p.M > kMaxMerge || 2 * p.M > kWarps * 256) return cudaErrorInvalidValue;
+  if (p.chunk > kMaxChunk || p.S * p.M > kMaxMerge || p.M > kCandCap) return cudaErrorInvalidValue;
   k_topm<<<dim3(p.S, p.rows), kThreads, topm_partial_smem(p), stream>>>(p);
   return cudaGetLastError();
 }

@@ -104,8 +104,10 @@ dt_status dt_check_config(const dt_config* cfg);
  * is NULL. */
 int64_t dt_node_count(const dt_config* cfg);
 
-/* Device bytes that dt_create allocates for this configuration (workspace,
- * GRU input table, captured-round buffers).  0 if the configuration is invalid. */
+/* Upper bound on the device bytes that dt_create allocates for this
+ * configuration (workspace, GRU input table, captured-round buffers); the
+ * Top-M scratch depends on the device's SM count, so the bound assumes the
+ * largest plan.  0 if the configuration is invalid. */
 size_t dt_workspace_bytes(const dt_config* cfg);
 
 /* Static description of a status code. */
