@@ -48,6 +48,7 @@ constexpr int kMaxNTiles = 8;    // owned columns per CTA <= 64 (8-wide MMA tile
 constexpr int kSLoads = 9;       // float4 state loads per thread: kPC*(g+24)/4/kThreads for g <= 1024
 constexpr int kMaxR32 = 32;      // bottleneck values per lane: r <= 1024
 constexpr int kZLoads = 16;      // z values per thread on the tensor-core path: W*r <= 4096
+constexpr int kFragMax = 8;      // fragment loads per lane in phase A: g <= 16 * kWarps * kFragMax
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16
 // mantissa bits, so two bf16 MMAs reproduce an fp32 operand to ~2^-17.
@@ -117,6 +118,20 @@ DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_
   return *s_abort == 0;
 }
 
+// Store state value v of (row, column j) into the fragment-ordered copy: its
+// bf16 high part and the bf16 of the remainder, at the places lane group
+// tig = (j mod 8) / 2 of a k16 step reads them as A-fragment registers
+// (a0/a2: columns 2tig, 2tig+1 and 2tig+8, 2tig+9 of the step).
+DT_DEVINL void store_frag(uint32_t* sf, int row, int j, int nk16, float v) {
+  const int kt = j >> 4, w = j & 15;
+  const int tig = (w & 7) >> 1, half = w & 1, pair = w >> 3;
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+  uint16_t* u = reinterpret_cast<uint16_t*>(sf + ((static_cast<size_t>(row) * nk16 + kt) * 4 + tig) * 4);
+  u[2 * pair + half] = __bfloat16_as_ushort(hi);
+  u[2 * (2 + pair) + half] = __bfloat16_as_ushort(lo);
+}
+
 // Activations on the fast exponential and division intrinsics (absolute
 // error ~1e-7; a large |x| saturates to the right limit: __fdividef returns 0
 // for a denominator beyond 2^126).
@@ -181,14 +196,21 @@ struct Shape {
   // one request with prefetched tokens: depth i+1's candidate data is staged
   // at the start of depth i into a second buffer
   bool dbuf;
+  // one request whose W state rows fit one A fragment: phase A reads the
+  // states as ready-made fragments from global memory (sfrag)
+  bool frag;
 };
+
+DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
+  return n_req == 1 && W <= kPC && g % (16 * kWarps) == 0 && g / (16 * kWarps) <= kFragMax;
+}
 
 // The candidate tokens of every depth of request 0 are read once, at launch.
 DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096; }
 
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
-               prefetch_tokens(p.D, p.M), p.n_req == 1 && prefetch_tokens(p.D, p.M)};
+               prefetch_tokens(p.D, p.M), p.n_req == 1 && prefetch_tokens(p.D, p.M), frag_ok(p.n_req, p.W, p.g)};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -198,7 +220,7 @@ struct DimsRuntime {
 // The Qwen3-4B shape (g=1024, r=256, M=64, K=W=8, one request, depth 15, 128
 // CTAs): dimensions are literals, so the compiler folds the index arithmetic.
 struct DimsQ4B {
-  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true};
+  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true};
   static DT_DEVINL Shape get(const ChainParams&) { return kShape; }
 };
 
@@ -506,7 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       const float* x = p.xtab + static_cast<size_t>(tok) * 3 * g;
       const float zg = sigmoidf_(x[g + jj]);
       const float ng = tanhf_(x[2 * g + jj]);
-      p.S[static_cast<size_t>(q * W) * g + jj] = (1.0f - zg) * ng;
+      const float s0 = (1.0f - zg) * ng;
+      p.S[static_cast<size_t>(q * W) * g + jj] = s0;
+      if (sh.frag) store_frag(p.sfrag, q * W, jj, g / 16, s0);  // parity 0 = depth 0
     }
     if (blockIdx.x == 0) {
       for (int q = tid; q < n_req; q += kThreads) {
@@ -539,7 +563,71 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     if (sh.dbuf) s.ctk = s.tok_all + static_cast<size_t>(i - 1) * M;  // this depth's candidate tokens
 
     // ================= phase A: projections of the live states ==============
-    for (int p0 = 0; p0 < P; p0 += kPC) {
+    if (sh.frag) {
+      // the live states (one request, P <= 8 rows) as ready-made A fragments:
+      // lane (gid, tig) of the warp owning k16 step kt reads one 16-byte word
+      // per step, straight into registers (high and low bf16 parts)
+      const int gid = lane >> 2, tig = lane & 3;
+      const int nk16 = g / 16;
+      const uint4* fr = reinterpret_cast<const uint4*>(p.sfrag + static_cast<size_t>((i - 1) & 1) * n_req * W * g);
+      uint4 f[kFragMax];
+#pragma unroll
+      for (int m = 0; m < kFragMax; ++m) {
+        const int kt = warp + kWarps * m;
+        f[m] = kt < nk16 ? __ldcg(fr + (static_cast<size_t>(gid) * nk16 + kt) * 4 + tig) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      // one request: the next depth's candidate data is staged now, into the
+      // other buffer (its last reader, depth i-1, finished before the
+      // barrier), while the state loads are in flight; it lands during this
+      // depth
+      if (sh.dbuf && i < p.depth_last)
+        stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
+                  i + 1 != D);
+      float acc[kMaxNTiles][4], acl[kMaxNTiles][4];
+#pragma unroll
+      for (int nt = 0; nt < kMaxNTiles; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[nt][e] = 0.0f;
+          acl[nt][e] = 0.0f;
+        }
+      const int ntiles = cpad / 8;
+#pragma unroll
+      for (int m = 0; m < kFragMax; ++m) {
+        const int kt = warp + kWarps * m;
+        if (kt < nk16) {
+          const int k0 = kt * 16 + 2 * tig;
+#pragma unroll
+          for (int nt = 0; nt < kMaxNTiles; ++nt) {
+            if (nt < ntiles) {
+              const uint16_t* wc = s.w + static_cast<size_t>(nt * 8 + gid) * gp + k0;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wc);
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wc + 8);
+              mma_bf16_16816(acc[nt], f[m].x, 0u, f[m].y, 0u, b0, b1);
+              mma_bf16_16816(acl[nt], f[m].z, 0u, f[m].w, 0u, b0, b1);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < kMaxNTiles; ++nt) {
+        if (nt < ntiles) {
+          float* rw = s.red + (warp * kPC + gid) * cpad + nt * 8 + 2 * tig;
+          rw[0] = acc[nt][0] + acl[nt][0];
+          rw[1] = acc[nt][1] + acl[nt][1];
+        }
+      }
+      __syncthreads();
+      for (int idx = tid; idx < P * ncol; idx += kThreads) {
+        const int pp = idx / ncol, c = idx - pp * ncol;
+        float sum = 0.0f;
+#pragma unroll
+        for (int w8 = 0; w8 < kWarps; ++w8) sum += s.red[(w8 * kPC + pp) * cpad + c];
+        if (c < 3 * nj) s.uu[static_cast<size_t>(pp) * 3 * sh.jper + c] = sum;
+        else p.uW1[static_cast<size_t>(pp) * r + r0 + (c - 3 * nj)] = sum;
+      }
+    }
+    for (int p0 = 0; p0 < (sh.frag ? 0 : P); p0 += kPC) {
       const int pc = min(kPC, P - p0);
       __syncthreads();
       // state rows -> bf16 high + low parts (S = hi + lo to ~16 mantissa bits)
@@ -1008,7 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           const float rg = sigmoidf_(x[jj] + uu[jj]);
           const float zg = sigmoidf_(x[nj + jj] + uu[nj + jj]);
           const float ng = tanhf_(x[2 * nj + jj] + rg * uu[2 * nj + jj]);
-          Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = (1.0f - zg) * ng + zg * h;
+          const float hn = (1.0f - zg) * ng + zg * h;
+          Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = hn;
+          if (sh.frag)
+            store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
         }
       } else if (blockIdx.x == 0 && p.live_out) {
         for (int j = tid; j < W; j += kThreads) p.live_out[static_cast<size_t>(q) * W + j] = -1;
@@ -1068,7 +1159,8 @@ bool is_q4b(const ChainParams& p, int grid) {
   const Shape b = DimsQ4B::kShape;
   return grid == 128 && a.g == b.g && a.r == b.r && a.M == b.M && a.K == b.K && a.W == b.W &&
          a.n_req == b.n_req && a.D == b.D && a.jper == b.jper && a.rper == b.rper && a.cpad == b.cpad &&
-         a.stage_w2 == b.stage_w2 && a.mma_b == b.mma_b && a.prefetch == b.prefetch && a.dbuf == b.dbuf;
+         a.stage_w2 == b.stage_w2 && a.mma_b == b.mma_b && a.prefetch == b.prefetch && a.dbuf == b.dbuf &&
+         a.frag == b.frag;
 }
 
 }  // namespace

@@ -87,6 +87,10 @@ struct ChainParams {
   const float* rest_lse;  // [n_req*D]
   const int* root_tok;    // [n_req]
   float* S;      // [2, n_req*W, g]
+  // the same states split into bf16 high + low parts, laid out as mma.sync
+  // A fragments: [2][n_req*W][g/16][4 lane groups][hi pair 0, hi pair 1,
+  // lo pair 0, lo pair 1] (used when one request's W rows fit one fragment)
+  uint32_t* sfrag;
   float* uW1;    // [n_req*W, r]
   int* live;     // [2, n_req, W]
   int* node_tok;
