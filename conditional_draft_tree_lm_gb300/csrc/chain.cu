@@ -49,6 +49,7 @@ constexpr int kSLoads = 9;       // float4 state loads per thread: kPC*(g+24)/4/
 constexpr int kMaxR32 = 32;      // bottleneck values per lane: r <= 1024
 constexpr int kZLoads = 16;      // z values per thread on the tensor-core path: W*r <= 4096
 constexpr int kFragMax = 8;      // fragment loads per lane in phase A: g <= 16 * kWarps * kFragMax
+constexpr int kZFragMax = 16;    // z fragment loads per lane in phase B: r <= 16 * kZFragMax
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16
 // mantissa bits, so two bf16 MMAs reproduce an fp32 operand to ~2^-17.
@@ -199,6 +200,9 @@ struct Shape {
   // one request whose W state rows fit one A fragment: phase A reads the
   // states as ready-made fragments from global memory (sfrag)
   bool frag;
+  // with frag and the tensor-core phase B: z is published as fragments by the
+  // bottleneck-row owners (zfrag) instead of u_W1
+  bool zf;
 };
 
 DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
@@ -210,7 +214,9 @@ DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096;
 
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
-               prefetch_tokens(p.D, p.M), p.n_req == 1 && prefetch_tokens(p.D, p.M), frag_ok(p.n_req, p.W, p.g)};
+               prefetch_tokens(p.D, p.M), p.n_req == 1 && prefetch_tokens(p.D, p.M), frag_ok(p.n_req, p.W, p.g),
+               frag_ok(p.n_req, p.W, p.g) && p.mma_b != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax &&
+                   p.n_req == 1 && prefetch_tokens(p.D, p.M)};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -220,7 +226,7 @@ struct DimsRuntime {
 // The Qwen3-4B shape (g=1024, r=256, M=64, K=W=8, one request, depth 15, 128
 // CTAs): dimensions are literals, so the compiler folds the index arithmetic.
 struct DimsQ4B {
-  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true};
+  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true, true};
   static DT_DEVINL Shape get(const ChainParams&) { return kShape; }
 };
 
@@ -583,14 +589,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       if (sh.dbuf && i < p.depth_last)
         stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
                   i + 1 != D);
-      float acc[kMaxNTiles][4], acl[kMaxNTiles][4];
+      // rows 0..7 of the tile carry the high parts and rows 8..15 the low
+      // parts of the same states: one MMA per k16 step gives both products
+      float acc[kMaxNTiles][4];
 #pragma unroll
       for (int nt = 0; nt < kMaxNTiles; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[nt][e] = 0.0f;
-          acl[nt][e] = 0.0f;
-        }
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
       const int ntiles = cpad / 8;
 #pragma unroll
       for (int m = 0; m < kFragMax; ++m) {
@@ -603,8 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               const uint16_t* wc = s.w + static_cast<size_t>(nt * 8 + gid) * gp + k0;
               const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wc);
               const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wc + 8);
-              mma_bf16_16816(acc[nt], f[m].x, 0u, f[m].y, 0u, b0, b1);
-              mma_bf16_16816(acl[nt], f[m].z, 0u, f[m].w, 0u, b0, b1);
+              mma_bf16_16816(acc[nt], f[m].x, f[m].z, f[m].y, f[m].w, b0, b1);
             }
           }
         }
@@ -613,18 +617,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       for (int nt = 0; nt < kMaxNTiles; ++nt) {
         if (nt < ntiles) {
           float* rw = s.red + (warp * kPC + gid) * cpad + nt * 8 + 2 * tig;
-          rw[0] = acc[nt][0] + acl[nt][0];
-          rw[1] = acc[nt][1] + acl[nt][1];
+          rw[0] = acc[nt][0] + acc[nt][2];
+          rw[1] = acc[nt][1] + acc[nt][3];
         }
       }
+      // this depth's staged h1_i (copied during the previous depth) is read
+      // below: the thread's own copies are complete, the barrier shares them
+      if (sh.zf) {
+        if (i < p.depth_last) cp_async_wait_group1();  // the next depth's group may still fly
+        else cp_async_wait_all();
+      }
       __syncthreads();
+      const float* h1i = buf(i).h1s;
       for (int idx = tid; idx < P * ncol; idx += kThreads) {
         const int pp = idx / ncol, c = idx - pp * ncol;
         float sum = 0.0f;
 #pragma unroll
         for (int w8 = 0; w8 < kWarps; ++w8) sum += s.red[(w8 * kPC + pp) * cpad + c];
-        if (c < 3 * nj) s.uu[static_cast<size_t>(pp) * 3 * sh.jper + c] = sum;
-        else p.uW1[static_cast<size_t>(pp) * r + r0 + (c - 3 * nj)] = sum;
+        if (c < 3 * nj) {
+          s.uu[static_cast<size_t>(pp) * 3 * sh.jper + c] = sum;
+        } else {
+          const int rho = r0 + (c - 3 * nj);
+          if (sh.zf) store_frag(p.zfrag, pp, rho, r / 16, siluf_(h1i[rho] + sum));
+          else p.uW1[static_cast<size_t>(pp) * r + rho] = sum;
+        }
       }
     }
     for (int p0 = 0; p0 < (sh.frag ? 0 : P); p0 += kPC) {
@@ -745,10 +761,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         s.h1s = cur.h1s;
         s.rest = cur.rest;
       }
-      // the branches' u_W1 rows (tensor-core path) are loaded first, so that
+      // the branches' z fragments (or u_W1 rows) are loaded first, so that
       // their latency overlaps the parent reads and the staging wait
+      // z fragments: the CTA reads the 8 x r/16 x 4 words once (two per
+      // thread) and keeps them in shared memory as [kt][gid][tig], where a
+      // warp's fragment loads of one k16 step are contiguous
+      constexpr int kZPer = (kPC * kZFragMax * 4 + kThreads - 1) / kThreads;
+      uint4 zq[kZPer];
+      if (sh.zf) {
+        const int nzw = kPC * (r / 16) * 4;
+        const uint4* zr = reinterpret_cast<const uint4*>(p.zfrag);
+#pragma unroll
+        for (int u = 0; u < kZPer; ++u) {
+          const int idx = tid + u * kThreads;
+          zq[u] = idx < nzw ? __ldcg(zr + idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
       float uv[kZLoads];
-      if (sh.mma_b) {
+      if (sh.mma_b && !sh.zf) {
         const float* ub = p.uW1 + static_cast<size_t>(q * W) * r;  // rows q*W .. q*W+Lp-1
         const int nz = Lp * r;
 #pragma unroll
@@ -762,6 +792,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         s.pnode[b] = node;
         s.pscore[b] = (node >= 0 && node < p.N1) ? p.node_score[static_cast<size_t>(q) * p.N1 + node] : 0.0f;
       }
+      if (sh.zf) {
+        // global order [gid][kt][tig] -> shared order [kt][gid][tig]
+        const int nk = r / 16, nzw = kPC * nk * 4;
+        uint4* zs4 = reinterpret_cast<uint4*>(s.zh);
+#pragma unroll
+        for (int u = 0; u < kZPer; ++u) {
+          const int idx = tid + u * kThreads;
+          if (idx < nzw) {
+            const int tg = idx & 3, rest4 = idx >> 2, gd = rest4 / nk, kt = rest4 - gd * nk;
+            zs4[(kt * kPC + gd) * 4 + tg] = zq[u];
+          }
+        }
+      }
       if (sh.dbuf && i < p.depth_last)
         cp_async_wait_group1();  // this depth's group; the next depth's may still fly
       else
@@ -771,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       if (sh.mma_b) {
         // ---- z = SiLU(h1 + u) of every live branch -> bf16 high/low rows ----
         const int zs = r + 8;
-        {
+        if (!sh.zf) {
           const int nz = Lp * r;
 #pragma unroll
           for (int j = 0; j < kZLoads; ++j) {
@@ -787,9 +830,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
             }
           }
         }
-        __syncthreads();
+        if (!sh.zf) __syncthreads();
         // ---- lambda[b][c] = (base_c + z_b . W2[c]) / T: mma.sync over (branch, candidate) tiles ----
-        {
+        if (sh.zf) {
+          // z fragments in registers: rows 0..7 high parts, rows 8..15 low
+          // parts of the (at most 8) branches; one MMA per k16 step
+          const int gid = lane >> 2, tig = lane & 3;
+          const int ntiles = M / 8, nk = r / 16;
+          const uint4* zs4 = reinterpret_cast<const uint4*>(s.zh);
+          for (int nt = warp; nt < ntiles; nt += kWarps) {
+            const uint16_t* wr = s.w2s + static_cast<size_t>(nt * 8 + gid) * zs;
+            float a0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int kt = 0; kt < kZFragMax; ++kt) {
+              if (kt < nk) {
+                const int k0 = kt * 16 + 2 * tig;
+                const uint4 zf = zs4[(kt * kPC + gid) * 4 + tig];
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wr + k0);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wr + k0 + 8);
+                mma_bf16_16816((kt & 1) ? a1 : a0, zf.x, zf.z, zf.y, zf.w, b0, b1);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = nt * 8 + 2 * tig + e;
+              if (gid < Lp) {
+                const float lam = (s.cbs[c] + ((a0[e] + a1[e]) + (a0[e + 2] + a1[e + 2]))) / p.T;
+                s.lamkey[static_cast<size_t>(gid) * M + c] = rank_key(lam, static_cast<uint32_t>(s.ctk[c]));
+              }
+            }
+          }
+        } else {
           const int gid = lane >> 2, tig = lane & 3;
           const int mtiles = (Lp + 15) / 16, ntiles = M / 8;
           for (int t = warp; t < mtiles * ntiles; t += kWarps) {
@@ -1160,7 +1231,7 @@ bool is_q4b(const ChainParams& p, int grid) {
   return grid == 128 && a.g == b.g && a.r == b.r && a.M == b.M && a.K == b.K && a.W == b.W &&
          a.n_req == b.n_req && a.D == b.D && a.jper == b.jper && a.rper == b.rper && a.cpad == b.cpad &&
          a.stage_w2 == b.stage_w2 && a.mma_b == b.mma_b && a.prefetch == b.prefetch && a.dbuf == b.dbuf &&
-         a.frag == b.frag;
+         a.frag == b.frag && a.zf == b.zf;
 }
 
 }  // namespace

@@ -61,7 +61,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
   size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, part_kth, cand_tok, cand_base, rest_lse,
-      row_done, S, sfrag,
+      row_done, S, sfrag, zfrag,
       uW1, live, node_tok, node_parent, node_logp, node_score, sel, bar, status, H_dev, root_dev,
       out_tok, out_parent, out_depth, out_logp, out_mask, total;
   size_t xtab;
@@ -90,6 +90,7 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   put(L.row_done, rows * 4);
   put(L.S, 2ull * c.n_req * c.W * c.g * 4);
   put(L.sfrag, 2ull * c.n_req * c.W * c.g * 4);
+  put(L.zfrag, static_cast<size_t>(c.n_req) * c.W * c.r * 4);
   put(L.uW1, static_cast<size_t>(c.n_req) * c.W * c.r * 4);
   put(L.live, 2ull * c.n_req * c.W * 4);
   put(L.node_tok, c.n_req * N1 * 4);
@@ -226,6 +227,7 @@ ChainParams chain_params(dt_ctx* c, const int32_t* root, int32_t* ntok, int32_t*
   p.root_tok = root;
   p.S = c->at<float>(c->lay.S);
   p.sfrag = c->at<uint32_t>(c->lay.sfrag);
+  p.zfrag = c->at<uint32_t>(c->lay.zfrag);
   p.uW1 = c->at<float>(c->lay.uW1);
   p.live = c->at<int>(c->lay.live);
   p.node_tok = ntok;

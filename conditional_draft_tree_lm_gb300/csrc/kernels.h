@@ -91,6 +91,9 @@ struct ChainParams {
   // A fragments: [2][n_req*W][g/16][4 lane groups][hi pair 0, hi pair 1,
   // lo pair 0, lo pair 1] (used when one request's W rows fit one fragment)
   uint32_t* sfrag;
+  // z = SiLU(h1_i + u_W1) of the live branches in the same fragment order
+  // ([n_req*W][r/16][4][4]), written by the CTAs that own bottleneck rows
+  uint32_t* zfrag;
   float* uW1;    // [n_req*W, r]
   int* live;     // [2, n_req, W]
   int* node_tok;
