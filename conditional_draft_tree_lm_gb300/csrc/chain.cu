@@ -214,9 +214,8 @@ DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096;
 
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
-               prefetch_tokens(p.D, p.M), p.n_req == 1 && prefetch_tokens(p.D, p.M), frag_ok(p.n_req, p.W, p.g),
-               frag_ok(p.n_req, p.W, p.g) && p.mma_b != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax &&
-                   p.n_req == 1 && prefetch_tokens(p.D, p.M)};
+               prefetch_tokens(p.D, p.M), p.dbuf != 0, frag_ok(p.n_req, p.W, p.g),
+               frag_ok(p.n_req, p.W, p.g) && p.mma_b != 0 && p.dbuf != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -1256,8 +1255,12 @@ void chain_plan(ChainParams& p, int grid) {
   // z of all branches within one pass of kZLoads values per thread
   p.stage_w2 = 1;
   p.mma_b = (p.r % 16 == 0 && p.M % 8 == 0 && p.W * p.r <= kZLoads * kThreads && p.W * p.M <= 4096) ? 1 : 0;
+  p.dbuf = (p.n_req == 1 && prefetch_tokens(p.D, p.M)) ? 1 : 0;
+  // over the budget: give up, in order, the second stage buffer, the
+  // tensor-core phase B and the W2 staging (wide candidate sets read W2 from L2)
+  if (p.dbuf && chain_smem_bytes(p) > kBudget) p.dbuf = 0;
   if (p.mma_b && chain_smem_bytes(p) > kBudget) p.mma_b = 0;
-  if (!p.mma_b && chain_smem_bytes(p) > kBudget) p.stage_w2 = 0;  // wide candidate sets read W2 from L2
+  if (!p.mma_b && chain_smem_bytes(p) > kBudget) p.stage_w2 = 0;
 }
 
 bool chain_can_fuse_tree(const ChainParams& p) {

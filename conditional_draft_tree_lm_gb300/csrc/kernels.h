@@ -107,6 +107,7 @@ struct ChainParams {
   int jper, rper;     // S / r columns owned per CTA
   int cpad;           // padded owned-column count (multiple of 32)
   int stage_w2;       // 1: stage the candidates' W2 rows in shared memory
+  int dbuf;           // 1: stage the next depth's candidate data a depth ahead (one request)
   int mma_b;          // 1: corrected logits of all branches as one tensor-core product
   // tail of a whole-round launch of one request: CTA 0 (which wrote every node
   // array itself) runs the global Top-B and the tree/mask, no extra launch
