@@ -40,11 +40,12 @@ def _peaks():
 
 
 def _config_dict(cfg, n_inputs):
+    lm_mb = cfg.V * cfg.d * 2 / 1e6
     return {
         "workload": f"{cfg.name}: d={cfg.d} V={cfg.V} block={cfg.block} g={cfg.g} r={cfg.r} "
                     f"M={cfg.M} K={cfg.K} W={cfg.W} B={cfg.B} beta={cfg.beta} T={cfg.T} n_req={cfg.n_req}",
         "n_req": cfg.n_req, "depth": cfg.block - 1, "B": cfg.B, "distinct_inputs": n_inputs,
-        "l2": "inputs larger than L2 (778 MB LM head streamed per round), no flush",
+        "l2": f"inputs larger than L2 ({lm_mb:.0f} MB LM head streamed per round), no flush",
     }
 
 
@@ -134,7 +135,7 @@ def cpu_cores():
 def bench_reference(args):
     """The fp64 oracle as it stands, on the host cores, same workload and metric."""
     from workloads import get_config, make_weights
-    cfg = get_config(WORKLOAD)
+    cfg = get_config(args.workload)
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -172,7 +173,7 @@ def bench_gpu(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     build_library()
-    cfg = get_config(WORKLOAD)
+    cfg = get_config(args.workload)
     w = make_weights(cfg)
     wd = {k: bf16_tensor(v) for k, v in w.items()}
     builder = DraftTreeBuilder(cfg, wd)
@@ -258,7 +259,7 @@ def bench_gpu(args):
     peak, peak_kind = _peaks()
     achieved = kbytes / (lm_ms / 1e3) / 1e9
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "lm_head_gemm_qwen3_4b_traffic.json")
+    prof = os.path.join(ROOT, "profiles", f"lm_head_gemm_{cfg.name}_traffic.json")
     if os.path.exists(prof):
         try:
             with open(prof) as f:
@@ -326,6 +327,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, help="a named workload of workloads/configs.py")
     ap.add_argument("--inputs", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
