@@ -141,10 +141,22 @@ DT_DEVINL float tanhf_(float x) { return __fdividef(2.0f, 1.0f + __expf(-2.0f * 
 DT_DEVINL float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 
-// Bitonic sort of 64 (key, payload) pairs held by one warp, elements 2*lane
-// (ka, pa) and 2*lane + 1 (kb, pb), into descending key order: afterwards the
-// element of rank e sits in lane e/2, in ka when e is even and kb when odd.
-DT_DEVINL void warp_sort64_desc(uint64_t& ka, uint64_t& kb, int& pa, int& pb) {
+// Keys that carry their candidate index: value key (high 32 bits), then the
+// token id inverted in 26 bits (ties go to the lower token), then the
+// candidate index in 6 bits.  Orders exactly like rank_key(value, token) for
+// distinct tokens < 2^26; valid for M <= 64.
+DT_DEVINL uint64_t cand_key(float v, int tok, int c) {
+  return (static_cast<uint64_t>(f32_key(v)) << 32) |
+         (static_cast<uint64_t>((0x3FFFFFFu - static_cast<uint32_t>(tok)) & 0x3FFFFFFu) << 6) |
+         static_cast<uint64_t>(c & 63);
+}
+DT_DEVINL int cand_key_tok(uint64_t k) { return static_cast<int>(0x3FFFFFFu - ((k >> 6) & 0x3FFFFFFu)); }
+DT_DEVINL int cand_key_c(uint64_t k) { return static_cast<int>(k & 63u); }
+
+// Bitonic sort of 64 distinct keys held by one warp (elements 2*lane in ka,
+// 2*lane + 1 in kb) into descending order, with branch-free min/max steps;
+// afterwards the key of rank e sits in lane e/2 (ka when e is even).
+DT_DEVINL void warp_sort64_keys_desc(uint64_t& ka, uint64_t& kb) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 2; k <= 64; k <<= 1) {
@@ -152,43 +164,21 @@ DT_DEVINL void warp_sort64_desc(uint64_t& ka, uint64_t& kb, int& pa, int& pb) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
       if (j == 1) {
-        if (desc ? (ka < kb) : (ka > kb)) {
-          const uint64_t t = ka;
-          ka = kb;
-          kb = t;
-          const int u = pa;
-          pa = pb;
-          pb = u;
-        }
+        const uint64_t hi = ka > kb ? ka : kb, lo = ka > kb ? kb : ka;
+        ka = desc ? hi : lo;
+        kb = desc ? lo : hi;
       } else {
-        const int lj = j >> 1;  // partner element e ^ j lives in lane ^ (j / 2)
+        const int lj = j >> 1;
         const uint64_t oa = __shfl_xor_sync(0xFFFFFFFFu, ka, lj);
         const uint64_t ob = __shfl_xor_sync(0xFFFFFFFFu, kb, lj);
-        const int qa = __shfl_xor_sync(0xFFFFFFFFu, pa, lj);
-        const int qb = __shfl_xor_sync(0xFFFFFFFFu, pb, lj);
-        const bool keep_max = ((lane & lj) == 0) == desc;  // the lower element of a descending pair keeps the max
-        if (keep_max ? (oa > ka) : (oa < ka)) {
-          ka = oa;
-          pa = qa;
-        }
-        if (keep_max ? (ob > kb) : (ob < kb)) {
-          kb = ob;
-          pb = qb;
-        }
+        const bool keep_max = ((lane & lj) == 0) == desc;
+        ka = keep_max ? (oa > ka ? oa : ka) : (oa < ka ? oa : ka);
+        kb = keep_max ? (ob > kb ? ob : kb) : (ob < kb ? ob : kb);
       }
     }
   }
 }
 
-// Element of rank w (0..63) of a warp_sort64_desc result, delivered to the
-// calling lane (every lane must call).
-DT_DEVINL void warp_sorted_at(uint64_t ka, uint64_t kb, int pa, int pb, int w, uint64_t& key, int& pay) {
-  const int src = (w >> 1) & 31;
-  const uint64_t xa = __shfl_sync(0xFFFFFFFFu, ka, src), xb = __shfl_sync(0xFFFFFFFFu, kb, src);
-  const int ya = __shfl_sync(0xFFFFFFFFu, pa, src), yb = __shfl_sync(0xFFFFFFFFu, pb, src);
-  key = (w & 1) ? xb : xa;
-  pay = (w & 1) ? yb : ya;
-}
 
 // Dimensions a launch runs with (see chain_plan).
 struct Shape {
@@ -256,7 +246,7 @@ struct Smem {
   float* clogp;     // [W*K]
   float* cscore;    // [W*K]
   int* crank;       // [W*K] top-K winners / ranks
-  uint64_t* wkey;   // [pow2 >= W*K] top-W keys
+  uint64_t* wkey;   // [max(64, pow2 >= W*K)] top-W keys
   int* surv;        // [n_req][W] survivor child slot
   float* pscore;    // [W] parent scores of the current request
   int* pnode;       // [W] parent node indices of the current request
@@ -321,7 +311,7 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
       WK * 4,
       WK * 4,
       WK * 4,
-      static_cast<size_t>(pow2_at_least(static_cast<int>(WK))) * 8,
+      static_cast<size_t>(max(64, pow2_at_least(static_cast<int>(WK)))) * 8,  // >= 64: one-warp top-W
       static_cast<size_t>(sh.n_req) * sh.W * 4,
       static_cast<size_t>(sh.W) * 4,
       static_cast<size_t>(sh.W) * 4,
@@ -424,9 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   __shared__ int s_abort;
   __shared__ int s_wcnt[kWarps];
   __shared__ uint32_t s_state[4];
-  __shared__ int s_scan[40];
+  __shared__ float s_tred[64];  // Top-B min/max partials of the tail
+  __shared__ int s_tscan[40];   // Top-B fallback scans
 
   const Shape sh = Dm::get(p);
+  // candidate keys carry their candidate index (M <= 64, token ids < 2^26)
+  const bool packed = sh.M <= 64 && p.V <= (1 << 26);
   const int g = sh.g, r = sh.r, M = sh.M, K = sh.K, W = sh.W, n_req = sh.n_req, D = sh.D;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j0 = blockIdx.x * sh.jper;
@@ -855,7 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               const int c = nt * 8 + 2 * tig + e;
               if (gid < Lp) {
                 const float lam = (s.cbs[c] + ((a0[e] + a1[e]) + (a0[e + 2] + a1[e + 2]))) / p.T;
-                s.lamkey[static_cast<size_t>(gid) * M + c] = rank_key(lam, static_cast<uint32_t>(s.ctk[c]));
+                s.lamkey[static_cast<size_t>(gid) * M + c] =
+                    packed ? cand_key(lam, s.ctk[c], c) : rank_key(lam, static_cast<uint32_t>(s.ctk[c]));
               }
             }
           }
@@ -902,28 +896,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               const int c = nt * 8 + 2 * tig + (e & 1);
               if (b < Lp) {
                 const float lam = (s.cbs[c] + acc[e]) / p.T;
-                s.lamkey[static_cast<size_t>(b) * M + c] = rank_key(lam, static_cast<uint32_t>(s.ctk[c]));
+                s.lamkey[static_cast<size_t>(b) * M + c] =
+                    packed ? cand_key(lam, s.ctk[c], c) : rank_key(lam, static_cast<uint32_t>(s.ctk[c]));
               }
             }
           }
         }
         __syncthreads();
         // ---- per branch: log-partition, top-K, children by token ----
-        if (M == 64 && K <= 32) {
-          // the branch's 64 keys sorted in registers (one warp per branch)
+        if (packed && M == 64 && K <= 32) {
+          // the branch's 64 keys (candidate index packed in) sorted in registers,
+          // one warp per branch
           for (int b = warp; b < Lp; b += kWarps) {
             const uint64_t* kr = s.lamkey + static_cast<size_t>(b) * 64;
             uint64_t ka = kr[2 * lane], kb2 = kr[2 * lane + 1];
-            int pa = 2 * lane, pb = 2 * lane + 1;
             const float la = key_f32(static_cast<uint32_t>(ka >> 32)), lb = key_f32(static_cast<uint32_t>(kb2 >> 32));
             const float lmax = warp_max(fmaxf(rest, fmaxf(la, lb)));
             const float se = warp_sum(expf(la - lmax) + expf(lb - lmax)) + expf(rest - lmax);
             const float logZ = lmax + logf(se);
-            warp_sort64_desc(ka, kb2, pa, pb);
-            uint64_t wk;
-            int wc;
-            warp_sorted_at(ka, kb2, pa, pb, lane, wk, wc);  // lane w < K holds the w-th best
-            const int tok = static_cast<int>(rank_key_id(wk));
+            warp_sort64_keys_desc(ka, kb2);
+            // lane w < K takes the w-th best (lane w/2, ka or kb)
+            const uint64_t xa = __shfl_sync(0xFFFFFFFFu, ka, (lane >> 1) & 31);
+            const uint64_t xb = __shfl_sync(0xFFFFFFFFu, kb2, (lane >> 1) & 31);
+            const uint64_t wk = (lane & 1) ? xb : xa;
+            const int tok = cand_key_tok(wk);
+            const int wc = cand_key_c(wk);
             int trank = 0;
             for (int m = 0; m < K; ++m) trank += __shfl_sync(0xFFFFFFFFu, tok, m) < tok ? 1 : 0;
             if (lane < K) {
@@ -1097,7 +1094,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       }
       if (!last) {
         // top-W of the depth by (score desc, node index asc); survivors ascending
-        if (nchild <= kRankMax) {
+        if (nchild <= 64) {
+          // one warp: two children per lane ranked by counting, survivors
+          // placed in slot order with two ballots (no CTA barrier)
+          if (warp == 0) {
+            for (int e = lane; e < 64; e += 32)
+              s.wkey[e] = e < nchild ? rank_key(s.cscore[e], static_cast<uint32_t>(e)) : 0ull;
+            __syncwarp();
+            const uint64_t k0 = s.wkey[lane], k1 = s.wkey[lane + 32];
+            int r0 = 0, r1 = 0;
+#pragma unroll 8
+            for (int f = 0; f < nchild; ++f) {
+              const uint64_t kf = s.wkey[f];
+              r0 += kf > k0 ? 1 : 0;
+              r1 += kf > k1 ? 1 : 0;
+            }
+            const bool a0 = lane < nchild && r0 < Li, a1 = lane + 32 < nchild && r1 < Li;
+            const unsigned b0 = __ballot_sync(0xFFFFFFFFu, a0), b1 = __ballot_sync(0xFFFFFFFFu, a1);
+            const unsigned lt = (1u << lane) - 1u;
+            if (a0) s.surv[q * W + __popc(b0 & lt)] = lane;
+            if (a1) s.surv[q * W + __popc(b0) + __popc(b1 & lt)] = lane + 32;
+          }
+        } else if (nchild <= kRankMax) {
           // one child per thread: rank over precomputed keys, survivors (rank <
           // Li) placed in slot order with per-warp ballots
           for (int e = tid; e < nchild; e += kThreads) s.wkey[e] = rank_key(s.cscore[e], static_cast<uint32_t>(e));
@@ -1200,12 +1218,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     int* nodes = offs + (kMaxDepth + 2);
     int* par = nodes + (p.B + 1);
     int* dep = par + (p.B + 1);
+    uint32_t* anc = reinterpret_cast<uint32_t*>(dep + (p.B + 1));
     for (int k = tid; k <= D + 1; k += kThreads) offs[k] = p.off[k];
     __syncthreads();
-    topb_select(p.node_score, p.N1, p.B, p.beta, D, offs, reinterpret_cast<uint32_t*>(s.w),
-                reinterpret_cast<uint32_t*>(s.red), kWarps * 256, s_state, s_scan, p.sel);
-    tree_and_mask(p.sel, p.N1, p.B, D, offs, p.node_tok, p.node_parent, p.node_score, nodes, par, dep, p.tok,
-                  p.parent, p.depth, p.logp_cum, p.mask, p.status);
+    // candidate keys first (8-byte aligned), then the float keys
+    uint64_t* tb_cands = reinterpret_cast<uint64_t*>(s.w);
+    uint32_t* tb_keys = reinterpret_cast<uint32_t*>(tb_cands + (p.N1 - 1));
+    topb_select(p.node_score, p.N1, p.B, p.beta, D, offs, tb_keys, tb_cands, p.N1 - 1,
+                reinterpret_cast<uint32_t*>(s.red), kWarps * 256, s_state, s_tred, s_tscan, p.sel);
+    tree_and_mask(p.sel, p.N1, p.B, D, offs, p.node_tok, p.node_parent, p.node_score, nodes, par, dep, anc,
+                  p.tok, p.parent, p.depth, p.logp_cum, p.mask, p.status);
   }
 }
 
@@ -1266,11 +1288,12 @@ void chain_plan(ChainParams& p, int grid) {
 bool chain_can_fuse_tree(const ChainParams& p) {
   if (p.n_req != 1) return false;
   const size_t gp = static_cast<size_t>(kstride(p.g));
-  const size_t weight_bytes = gp * p.cpad * 2;                          // holds the Top-B keys
+  const size_t weight_bytes = gp * p.cpad * 2;                          // holds the Top-B keys + candidates
   const size_t red_words = static_cast<size_t>(kWarps) * kPC * p.cpad;  // holds the histograms
-  const size_t state_bytes = gp * kPC * 2 * 2;                          // holds offsets + tree slots
-  return static_cast<size_t>(p.N1 - 1) * 4 <= weight_bytes && red_words >= static_cast<size_t>(kWarps) * 256 &&
-         static_cast<size_t>(kMaxDepth + 2 + 3 * (p.B + 1)) * 4 <= state_bytes;
+  const size_t state_bytes = gp * kPC * 2 * 2;                          // holds offsets, slots, ancestor rows
+  const size_t S = static_cast<size_t>(p.B) + 1;
+  return static_cast<size_t>(p.N1 - 1) * 12 <= weight_bytes && red_words >= static_cast<size_t>(kWarps) * 256 &&
+         (static_cast<size_t>(kMaxDepth + 2) + 3 * S + S * anc_words(static_cast<int>(S))) * 4 <= state_bytes;
 }
 
 cudaError_t chain_prepare() {

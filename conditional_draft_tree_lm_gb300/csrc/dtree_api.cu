@@ -52,7 +52,9 @@ dt_status check(const dt_config* c) {
   Tables t;
   if (!make_tables(*c, t)) return DT_ERR_SHAPE;
   if (c->B > t.N) return DT_ERR_INVALID_ARG;
-  if ((t.N + 1) * 4 > 227 * 1024) return DT_ERR_SHAPE;  // Top-B keys in shared memory
+  // Top-B in shared memory: N+1 float keys and up to 8192 candidate keys
+  if (static_cast<long long>(t.N + 1) * 4 + static_cast<long long>(t.N < 8192 ? t.N : 8192) * 8 > 190 * 1024)
+    return DT_ERR_SHAPE;
   if (c->n_req * c->W * 3 * 8 * 4 > 64 * 1024) return DT_ERR_SHAPE;  // chain state projections
   return DT_OK;
 }

@@ -110,4 +110,29 @@ DT_DEVINL void radix_select_kth_largest(const uint32_t* keys, int n, int k, uint
   need = static_cast<int>(kk);
 }
 
+// Exact ranks of keys[0, c) among themselves (the number of larger keys; keys
+// are distinct).  Each key is ranked by a group of g consecutive threads (g a
+// power of two <= 32, as many as the block allows), whose partial counts are
+// added with shuffles; fn(e, key, rank) then runs on the group's first thread.
+// Every thread of the block must call (blockDim.x a multiple of 32).
+template <class Fn>
+DT_DEVINL void block_rank_all(const uint64_t* keys, int c, Fn fn) {
+  const int nt = static_cast<int>(blockDim.x);
+  int g = 1;
+  while (g < 32 && 2 * g * c <= nt) g <<= 1;
+  for (int base = 0; base < c * g; base += nt) {
+    const int idx = base + static_cast<int>(threadIdx.x);
+    const int e = idx / g, part = idx - e * g;
+    uint64_t ke = 0ull;
+    int rk = 0;
+    if (e < c) {
+      ke = keys[e];
+#pragma unroll 4
+      for (int f = part; f < c; f += g) rk += keys[f] > ke ? 1 : 0;
+    }
+    for (int o = 1; o < g; o <<= 1) rk += __shfl_xor_sync(0xFFFFFFFFu, rk, o);
+    if (e < c && part == 0) fn(e, ke, rk);
+  }
+}
+
 }  // namespace dt
