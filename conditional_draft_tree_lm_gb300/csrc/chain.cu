@@ -491,6 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     }
   }
 
+  // the resident weights are loaded; everything below reads the previous
+  // kernels' results (and the barrier counter Top-M cleared)
+  dt_grid_wait();
+
   // ---- candidate tokens of every depth of request 0, read once ----
   if (sh.prefetch) {
     for (int idx = tid; idx < D * M; idx += kThreads) {
@@ -1238,11 +1242,13 @@ cudaError_t launch_one(const ChainParams& p, int grid, size_t smem, cudaStream_t
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_chain<MPL, Dm>, p);
 }
 

@@ -42,6 +42,14 @@ DT_DEVINL void dt_report(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before the previous kernel ends;
+// dt_grid_wait blocks until that kernel has completed and its writes are
+// visible (a no-op for an ordinary launch).  dt_grid_release lets the next
+// such kernel start launching.
+DT_DEVINL void dt_grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DT_DEVINL void dt_grid_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 DT_DEVINL uint64_t dt_globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

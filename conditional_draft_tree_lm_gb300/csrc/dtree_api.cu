@@ -195,9 +195,13 @@ dt_status enqueue_base_logits(dt_ctx* c, const void* H, float* logits, cudaStrea
   return DT_OK;
 }
 
-dt_status enqueue_topm(dt_ctx* c, const float* logits, cudaStream_t st) {
+// clear: a word Top-M sets to zero (the following chain's barrier counter),
+// or null; pdl: launch as a programmatic dependent of the LM-head GEMM.
+dt_status enqueue_topm(dt_ctx* c, const float* logits, cudaStream_t st, unsigned* clear = nullptr, int pdl = 0) {
   TopmParams p = c->topm;
   p.logits = logits;
+  p.clear_word = clear;
+  p.pdl = pdl;
   DT_TRY(launch_topm(p, st));
   return DT_OK;
 }
@@ -248,8 +252,10 @@ ChainParams chain_params(dt_ctx* c, const int32_t* root, int32_t* ntok, int32_t*
   return p;
 }
 
-dt_status enqueue_chain(dt_ctx* c, const ChainParams& p, cudaStream_t st) {
-  DT_TRY(cudaMemsetAsync(p.bar, 0, sizeof(unsigned), st));
+// counter_cleared: the preceding Top-M kernel already zeroed the barrier
+// counter (the whole-round path), so no memset is enqueued.
+dt_status enqueue_chain(dt_ctx* c, const ChainParams& p, cudaStream_t st, bool counter_cleared = false) {
+  if (!counter_cleared) DT_TRY(cudaMemsetAsync(p.bar, 0, sizeof(unsigned), st));
   DT_TRY(launch_chain(p, c->chain_grid, st));
   return DT_OK;
 }
@@ -273,7 +279,11 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
   float* logits = c->at<float>(c->lay.logits);
   dt_status s = enqueue_base_logits(c, H, logits, st);
   if (s != DT_OK) return s;
-  s = enqueue_topm(c, logits, st);
+  // Top-M and the chain launch as programmatic dependents (each waits for its
+  // predecessor's end before reading its results); Top-M also clears the
+  // chain's barrier counter, so the round needs no memset
+  unsigned* bar = c->at<unsigned>(c->lay.bar);
+  s = enqueue_topm(c, logits, st, bar, 1);
   if (s != DT_OK) return s;
   int32_t* ntok = c->at<int32_t>(c->lay.node_tok);
   int32_t* npar = c->at<int32_t>(c->lay.node_parent);
@@ -282,6 +292,7 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
   ChainParams cp = chain_params(c, root, ntok, npar, nlogp, nscore, nullptr);
   cp.depth_first = 1;
   cp.depth_last = c->t.D;
+  cp.pdl = 1;
   int32_t* sel = c->at<int32_t>(c->lay.sel);
   if (chain_can_fuse_tree(cp)) {
     // single request: the chain kernel's CTA 0 also prunes and emits the tree
@@ -294,9 +305,9 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
     cp.depth = depth;
     cp.logp_cum = logp_cum;
     cp.mask = mask;
-    return enqueue_chain(c, cp, st);
+    return enqueue_chain(c, cp, st, true);
   }
-  s = enqueue_chain(c, cp, st);
+  s = enqueue_chain(c, cp, st, true);
   if (s != DT_OK) return s;
   PruneParams pp = prune_params(c, nscore, sel);
   DT_TRY(launch_prune(pp, st));

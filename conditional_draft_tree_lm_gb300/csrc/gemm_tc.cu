@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = p.m_tiles_a + p.m_tiles_a2;
   const int num_tiles = m_tiles * p.n_tiles;
   const int num_kb = (p.K + 63) / 64;
+  dt_grid_release();  // the next kernel may launch; it waits for this one's end
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {

@@ -62,6 +62,8 @@ struct TopmParams {
   float* rest_lse;  // [rows]
   unsigned* row_done;  // [rows] chunk arrival counters (zero between launches)
   int* status;
+  unsigned* clear_word;  // or null: a word the kernel sets to zero (the next chain's barrier counter)
+  int pdl;               // 1: launched as a programmatic dependent of the previous kernel
 };
 void topm_plan(TopmParams& p, int num_sms);
 size_t topm_partial_smem(const TopmParams& p);
@@ -104,6 +106,7 @@ struct ChainParams {
   unsigned* bar;      // grid-barrier counter, zero at launch
   int* status;
   int depth_first, depth_last;
+  int pdl;            // 1: launched as a programmatic dependent of the previous kernel
   int jper, rper;     // S / r columns owned per CTA
   int cpad;           // padded owned-column count (multiple of 32)
   int stage_w2;       // 1: stage the candidates' W2 rows in shared memory

@@ -131,6 +131,11 @@ __global__ void __launch_bounds__(kThreads) k_topm(const TopmParams p) {
   const int mloc = min(p.M, n);
   const int nv = n > tid ? min(kVPT, (n - tid + kThreads - 1) / kThreads) : 0;  // valid values of this thread
 
+  // the logits come from the previous kernel; the next one may then launch
+  dt_grid_wait();
+  dt_grid_release();
+  if (p.clear_word && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *p.clear_word = 0u;
+
   // ---------------- 1. the chunk in registers; max; sample statistics ----------------
   float vals[kVPT];
 #pragma unroll
@@ -442,8 +447,17 @@ cudaError_t topm_prepare() { return dt_allow_max_dynamic_smem(reinterpret_cast<c
 
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {
   if (p.chunk > kMaxChunk || p.S * p.M > kMaxMerge || p.M > kCandCap) return cudaErrorInvalidValue;
-  k_topm<<<dim3(p.S, p.rows), kThreads, topm_partial_smem(p), stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.S, p.rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = topm_partial_smem(p);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_topm, p);
 }
 
 }  // namespace dt
