@@ -112,6 +112,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def replica_seeds(rank, n_inputs):
+    """Round seeds of one replica: every rank builds trees of its own inputs."""
+    return [rank * 100000 + s for s in range(n_inputs)]
+
+
+def job_throughput(dist, elapsed_s, e2e_s, steps, e2e_steps, world, device="cpu"):
+    """Whole-job rates of N independent replicas: the slowest rank's times
+    (max over ranks) divide the rounds of all ranks."""
+    import torch
+    if dist is not None:
+        t = torch.tensor([elapsed_s, e2e_s], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s, e2e_s = float(t[0]), float(t[1])
+    return steps * world / elapsed_s, e2e_steps * world / e2e_s, elapsed_s, e2e_s
+
+
 def run_oracle_rounds(cfg, w, seeds):
     from oracle.dartree import Oracle
     from workloads import make_round_inputs
@@ -178,7 +194,7 @@ def bench_gpu(args):
     wd = {k: bf16_tensor(v) for k, v in w.items()}
     builder = DraftTreeBuilder(cfg, wd)
     n_inputs = args.inputs
-    seeds = [rank * 100000 + s for s in range(n_inputs)]
+    seeds = replica_seeds(rank, n_inputs)
     Hs, roots = [], []
     for s in seeds:
         H, root = make_round_inputs(cfg, s)
@@ -248,13 +264,9 @@ def bench_gpu(args):
     d2h = sum(v.numel() * v.element_size() for v in out_h.values())
 
     status = builder.device_status()
-    elapsed = ms / 1e3
-    if dist:
-        t = torch.tensor([elapsed, e2e_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed, e2e_s = float(t[0]), float(t[1])
-    rounds = args.steps * world
-    value = rounds / elapsed
+    value, e2e_value, elapsed, e2e_s = job_throughput(dist, ms / 1e3, e2e_s, args.steps, n_e2e, world,
+                                                      device="cuda" if dist is not None and
+                                                      dist.get_backend() == "nccl" else "cpu")
     kbytes, rbytes = algorithmic_bytes(cfg)
     peak, peak_kind = _peaks()
     achieved = kbytes / (lm_ms / 1e3) / 1e9
@@ -282,7 +294,7 @@ def bench_gpu(args):
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
                      "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": lm_ms * 1e3},
-        "e2e": {"value": n_e2e * world / e2e_s, "unit": "builds/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_value, "unit": "builds/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": builder.round_kernel_count() * args.steps,
         "clocks": clk,
