@@ -28,6 +28,12 @@ What it computes, in the order the pages give it:
   children carry cumulative corrected log-probabilities, and the W best children
   of the depth live on with their GRU states.  All children are nodes of the
   fixed-width super-tree.
+* Marginal scoring (the conditional-versus-marginal ablation, "Resumen
+  Técnico: DominoTree", Contribuciones Clave, "Ablación de la
+  Condicionalidad"; the position-only scores of factorised tree drafters,
+  Planteamiento del Problema): with ``cfg.marginal`` the correction is left out,
+  Delta L = 0, over the same super-tree, so a node's log-probability depends
+  only on its depth and token.
 * Deferred pruning (same page, 2. "Poda Diferida de Mejor Primera Búsqueda"):
   one global Top-B over score + beta * depth (beta <= 0), then the compact tree
   with parent indices and the ancestor-only attention mask used for tree
@@ -281,10 +287,14 @@ class Oracle:
         state = {0: gru_step(a_root, np.zeros((1, cfg.g)), self.w_hh)[0]}
         live = [0]
         lives = [list(live)]
+        marginal = bool(getattr(cfg, "marginal", False))
         for i in range(1, D + 1):
-            S = np.stack([state[p] for p in live])
-            w2_rows = self.w["w2"][C[i - 1]]
-            dL = correction(Hf[i], S, self.w1, w2_rows)
+            if marginal:
+                dL = np.zeros((len(live), M))
+            else:
+                S = np.stack([state[p] for p in live])
+                w2_rows = self.w["w2"][C[i - 1]]
+                dL = correction(Hf[i], S, self.w1, w2_rows)
             lp = corrected_logprobs(base[i - 1], dL, rho[i - 1], T)
             first = len(tok)
             for bi, p in enumerate(live):
@@ -305,6 +315,8 @@ class Oracle:
                            swap=swaps.get(("W", i)))
             live = sorted(int(idx[j]) for j in kept)
             lives.append(list(live))
+            if marginal:
+                continue  # no correction, no GRU state
             a = gru_input([tok[q] for q in live], self.w["emb"], self.w_ih, self.b_ih)
             hp = np.stack([state[parent[q]] for q in live])
             hn = gru_step(a, hp, self.w_hh)

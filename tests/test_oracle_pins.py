@@ -429,6 +429,26 @@ def test_zero_correction_is_path_independent():
         assert sorted(top) == ref[0]
 
 
+@pytest.mark.parametrize("seed", [4, 9])
+def test_marginal_mode_equals_zeroed_correction(seed):
+    """Marginal scoring (Delta L = 0 by flag) builds exactly the tree of the
+    conditional build whose W2 is zero, which runs the whole correction and
+    GRU path; the two share nothing but the inputs."""
+    cfg = get_config("tiny")
+    w = make_weights(cfg)
+    H, root = make_round_inputs(cfg, seed)
+    tm = od.Oracle(w, cfg.with_(marginal=True)).build_request(H[0], int(root[0]))
+    w0 = dict(w)
+    w0["w2"] = np.zeros_like(w["w2"])
+    tz = od.Oracle(w0, cfg).build_request(H[0], int(root[0]))
+    for k in ("node_tok", "node_parent", "node_depth", "sel", "tok", "parent", "depth", "mask"):
+        assert np.array_equal(getattr(tm, k), getattr(tz, k)), k
+    np.testing.assert_allclose(tm.node_score, tz.node_score, rtol=0, atol=1e-12)
+    # and it differs from the conditional tree of the real W2 (the ablation is not vacuous)
+    tc = od.Oracle(w, cfg).build_request(H[0], int(root[0]))
+    assert not np.allclose(tm.node_score, tc.node_score)
+
+
 def test_single_branch_is_a_chain_of_corrected_argmax():
     cfg = get_config("tiny").with_(K=1, W=1, B=7)
     w = make_weights(cfg)

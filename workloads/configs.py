@@ -32,6 +32,7 @@ class WorkloadConfig:
     root: str = "uniform"   # "zero": root token id 0; "uniform": uniform over V
     h_scale: str = "unit"   # "unit": H ~ N(0,1); "heavy": per-position scale ~ U[0.5, 4]
     weight_dtype: str = "bf16"  # "bf16" (rounded, RNE) or "fp32"
+    marginal: bool = False      # marginal scoring: Delta L = 0 (path-independent children)
 
     @property
     def D(self) -> int:
@@ -65,6 +66,10 @@ CONFIGS = {
     "serving32": WorkloadConfig("serving32", d=2560, V=151936, block=16,
                                 g=1024, r=256, M=64, K=8, W=8, B=64, n_req=32,
                                 beta=0.0, T=1.0),
+    # The Qwen3-4B shape with marginal scoring (the correction left out): the
+    # conditional-versus-marginal ablation over the same super-tree.
+    "qwen3_4b_marginal": WorkloadConfig("qwen3_4b_marginal", d=2560, V=151936, block=16, g=1024,
+                                        r=256, M=64, K=8, W=8, B=64, beta=0.0, T=1.0, marginal=True),
     # Wide tree with heavy-tailed H (betas 0, -0.25, -1 are run).
     "wide": WorkloadConfig("wide", d=2560, V=151936, block=16, g=1024, r=256,
                            M=256, K=32, W=64, B=512, beta=0.0, T=1.0,
