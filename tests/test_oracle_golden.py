@@ -17,7 +17,11 @@ def test_oracle_reproduces_golden_trees():
     with open(GOLDEN) as f:
         gold = json.load(f)
     cfg = get_config("tiny")
-    assert gold["workload"] == cfg.as_dict()
+    # the fixture's workload fields match; fields added to the workload since
+    # the fixture was written keep their defaults (conditional scoring)
+    now = cfg.as_dict()
+    assert {k: now[k] for k in gold["workload"]} == gold["workload"]
+    assert now.get("marginal") is False
     orc = Oracle(make_weights(cfg), cfg)
     for rd in gold["rounds"]:
         H, root = make_round_inputs(cfg, rd["seed"])
