@@ -97,6 +97,7 @@ DT_DEVINL void red_release_add_u32(unsigned* p, unsigned v) {
 // timeout (the status word is set).
 DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_abort) {
   __syncthreads();
+  if (gridDim.x == 1) return true;  // one CTA: bar.sync orders its global writes
   ++epoch;
   if (threadIdx.x == 0) {
     red_release_add_u32(bar, 1u);
@@ -203,9 +204,10 @@ DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
 DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096; }
 
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
+  const bool fr = !p.marginal && frag_ok(p.n_req, p.W, p.g);
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
-               prefetch_tokens(p.D, p.M), p.dbuf != 0, frag_ok(p.n_req, p.W, p.g),
-               frag_ok(p.n_req, p.W, p.g) && p.mma_b != 0 && p.dbuf != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax};
+               prefetch_tokens(p.D, p.M), p.dbuf != 0, fr,
+               fr && p.mma_b != 0 && p.dbuf != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
 
   // ---- the owned weight columns, K-major: s.w[c][k] (zero padded) ----
   const int gp = kstride(g);
-  {
+  if (!p.marginal) {
     const int g8 = gp / 8;  // 16-byte chunks per padded row
     for (int idx = tid; idx < cpad * g8; idx += kThreads) {
       const int c = idx / g8, k8 = idx - c * g8;
@@ -565,7 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     if (sh.dbuf) s.ctk = s.tok_all + static_cast<size_t>(i - 1) * M;  // this depth's candidate tokens
 
     // ================= phase A: projections of the live states ==============
-    if (sh.frag) {
+    if (p.marginal) {
+      // marginal scoring: no states to project; only the staging of the next
+      // depth's candidate data
+      if (sh.dbuf && i < p.depth_last)
+        stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj, false);
+    } else if (sh.frag) {
       // the live states (one request, P <= 8 rows) as ready-made A fragments:
       // lane (gid, tig) of the warp owning k16 step kt reads one 16-byte word
       // per step, straight into registers (high and low bf16 parts)
@@ -639,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
     }
-    for (int p0 = 0; p0 < (sh.frag ? 0 : P); p0 += kPC) {
+    for (int p0 = 0; p0 < (sh.frag || p.marginal ? 0 : P); p0 += kPC) {
       const int pc = min(kPC, P - p0);
       __syncthreads();
       // state rows -> bf16 high + low parts (S = hi + lo to ~16 mantissa bits)
@@ -977,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         float* zw = s.z + warp * r;
         for (int b = warp; b < Lp; b += kWarps) {
           const float* u = p.uW1 + static_cast<size_t>(q * W + b) * r;
-          {
+          if (!p.marginal) {
             // all of the lane's loads first (one L2 round trip), then SiLU
             float uv[kMaxR32];
 #pragma unroll
@@ -998,7 +1005,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           float acc[MPL];
 #pragma unroll
           for (int j = 0; j < MPL; ++j) acc[j] = 0.0f;
-          for (int k8 = 0; k8 < r / 8; ++k8) {
+          // marginal scoring: no correction, lambda = base / T
+          for (int k8 = 0; k8 < (p.marginal ? 0 : r / 8); ++k8) {
             const float4 za = *reinterpret_cast<const float4*>(zw + k8 * 8);
             const float4 zb = *reinterpret_cast<const float4*>(zw + k8 * 8 + 4);
 #pragma unroll
@@ -1264,6 +1272,7 @@ bool is_q4b(const ChainParams& p, int grid) {
 }  // namespace
 
 int chain_grid(const ChainParams& p, int num_sms) {
+  if (p.marginal) return 1;  // no state: one CTA selects every depth
   // one CTA per 8 state columns, at most one per SM
   int G = (p.g + 7) / 8;
   if (G > num_sms) G = num_sms;
@@ -1274,6 +1283,17 @@ int chain_grid(const ChainParams& p, int num_sms) {
 size_t chain_smem_bytes(const ChainParams& p) { return smem_sizes(runtime_shape(p)).total; }
 
 void chain_plan(ChainParams& p, int grid) {
+  if (p.marginal) {
+    // no GRU columns or bottleneck rows; the weight area (cpad) stays for the
+    // Top-B keys of the fused tail
+    p.jper = 0;
+    p.rper = 0;
+    p.cpad = 32;
+    p.stage_w2 = 0;
+    p.mma_b = 0;
+    p.dbuf = (p.n_req == 1 && prefetch_tokens(p.D, p.M)) ? 1 : 0;
+    return;
+  }
   p.jper = (p.g + grid - 1) / grid;
   p.rper = (p.r + grid - 1) / grid;
   const int ncol = 3 * p.jper + p.rper;

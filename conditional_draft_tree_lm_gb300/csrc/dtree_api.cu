@@ -38,7 +38,7 @@ bool make_tables(const dt_config& c, Tables& t) {
 
 dt_status check(const dt_config* c) {
   if (!c) return DT_ERR_INVALID_ARG;
-  if (c->flags != 0) return DT_ERR_INVALID_ARG;
+  if ((c->flags & ~DT_FLAG_MARGINAL) != 0) return DT_ERR_INVALID_ARG;
   if (c->d <= 0 || c->V <= 0 || c->g <= 0 || c->r <= 0 || c->M <= 0 || c->K <= 0 || c->W <= 0 ||
       c->B <= 0 || c->n_req <= 0 || c->block < 2)
     return DT_ERR_INVALID_ARG;
@@ -222,6 +222,7 @@ ChainParams chain_params(dt_ctx* c, const int32_t* root, int32_t* ntok, int32_t*
   p.ldw1 = k.d + k.g;
   p.N1 = c->t.N + 1;
   p.T = k.T;
+  p.marginal = (k.flags & DT_FLAG_MARGINAL) ? 1 : 0;
   p.w_hh = static_cast<const uint16_t*>(c->w.w_hh);
   p.w1 = static_cast<const uint16_t*>(c->w.w1);
   p.w2 = static_cast<const uint16_t*>(c->w.w2);
@@ -433,6 +434,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   probe.W = cfg->W;
   probe.K = cfg->K;
   probe.M = cfg->M;
+  probe.marginal = (cfg->flags & DT_FLAG_MARGINAL) ? 1 : 0;
   c->chain_grid = chain_grid(probe, c->num_sms);
   chain_plan(probe, c->chain_grid);
   if (chain_smem_bytes(probe) > 227 * 1024 || probe.cpad > 64) {

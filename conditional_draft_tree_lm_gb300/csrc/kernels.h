@@ -107,6 +107,7 @@ struct ChainParams {
   int* status;
   int depth_first, depth_last;
   int pdl;            // 1: launched as a programmatic dependent of the previous kernel
+  int marginal;       // 1: marginal scoring (no correction, no GRU state; one CTA)
   int jper, rper;     // S / r columns owned per CTA
   int cpad;           // padded owned-column count (multiple of 32)
   int stage_w2;       // 1: stage the candidates' W2 rows in shared memory

@@ -71,8 +71,16 @@ typedef struct dt_config {
   int n_req;  /* independent requests per round; n_req * block <= 512 */
   float beta; /* depth bonus of the Top-B key (score + beta * depth); <= 0 */
   float T;    /* temperature dividing the corrected logits; > 0 */
-  unsigned flags; /* reserved, must be 0 */
+  unsigned flags; /* 0 or DT_FLAG_MARGINAL */
 } dt_config;
+
+/* Marginal scoring over the same super-tree: the correction Delta L is left
+ * out, so a node's log-probability depends only on its depth and token and
+ * every branch of a depth gets the same children (the conditional-versus-
+ * marginal ablation of the DominoTree summary, Contribuciones Clave,
+ * "Ablación de la Condicionalidad").  No GRU state is kept; the depth chain
+ * runs on one CTA. */
+#define DT_FLAG_MARGINAL 1u
 
 /* Frozen weights (device pointers, borrowed: they must outlive the context).
  * All bf16, row-major, torch.nn.Linear out-by-in layout.  GRU gate blocks are
@@ -96,7 +104,7 @@ typedef struct dt_ctx dt_ctx;
 /* Validate a configuration: K <= M <= V, M <= 512, 1 <= K <= 32,
  * 1 <= W <= 64, 2 <= block <= 64, d % 8 == 0, g % 8 == 0, r % 8 == 0,
  * r <= 1024, g <= 4096, n_req * block <= 512, 1 <= B <= N, T > 0, beta <= 0,
- * flags == 0.  Returns DT_OK, DT_ERR_INVALID_ARG or DT_ERR_SHAPE. */
+ * flags 0 or DT_FLAG_MARGINAL.  Returns DT_OK, DT_ERR_INVALID_ARG or DT_ERR_SHAPE. */
 dt_status dt_check_config(const dt_config* cfg);
 
 /* N: super-tree nodes of one request without the root (n_1 = K,
