@@ -11,6 +11,8 @@ from .generate import (
     make_weights,
     make_round_inputs,
     make_rounds,
+    make_target_logits,
+    make_tree,
     WEIGHT_NAMES,
 )
 
@@ -23,5 +25,7 @@ __all__ = [
     "make_weights",
     "make_round_inputs",
     "make_rounds",
+    "make_target_logits",
+    "make_tree",
     "WEIGHT_NAMES",
 ]

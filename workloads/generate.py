@@ -19,6 +19,9 @@ Recipe (the same for the oracle and the CUDA library):
   heavy-tailed workload) rounded to bfloat16 (kept float32 for the fp32
   workload), then one root token per request (id 0 for the tiny workload,
   uniform over the vocabulary otherwise).
+* Verification inputs (the acceptance walk): random trees from
+  ``default_rng([2, seed])`` and target logits from ``default_rng([3, seed])``
+  (``make_tree``, ``make_target_logits``).
 
 bfloat16 arrays are returned as their raw ``uint16`` bit patterns.
 """
@@ -133,3 +136,52 @@ def make_rounds(cfg: WorkloadConfig, seeds):
         Hs.append(H)
         roots.append(root)
     return np.stack(Hs), np.stack(roots)
+
+
+def make_tree(S: int, V: int, D: int, seed: int):
+    """A random tree of S slots in the emitted-tree layout, for verification
+    inputs: slot 0 is the root (parent -1, depth 0); slot c > 0 takes a parent
+    uniformly among the earlier slots of depth < D; sibling tokens are distinct
+    and uniform over the vocabulary.  Draws from ``default_rng([2, seed])``.
+    Returns (tok, parent, depth) int32 [S]."""
+    rng = np.random.default_rng([2, seed])
+    tok = np.zeros(S, dtype=np.int32)
+    parent = np.full(S, -1, dtype=np.int32)
+    depth = np.zeros(S, dtype=np.int32)
+    tok[0] = rng.integers(0, V)
+    used = [set() for _ in range(S)]
+    for c in range(1, S):
+        open_slots = np.flatnonzero(depth[:c] < D)
+        p = int(open_slots[rng.integers(0, open_slots.size)])
+        t = int(rng.integers(0, V))
+        while t in used[p]:
+            t = int(rng.integers(0, V))
+        used[p].add(t)
+        tok[c], parent[c], depth[c] = t, p, depth[p] + 1
+    return tok, parent, depth
+
+
+def make_target_logits(tok, parent, V: int, seed: int, follow: float = 0.7, tie: bool = False):
+    """Target-model logits [S, V] float32 for one tree, from
+    ``default_rng([3, seed])``: N(0, 1) everywhere; at each slot with children,
+    with probability ``follow`` the token of one child (uniform among them) is
+    raised to the row maximum plus U(0.25, 1), so that the target agrees with
+    the draft there.  With ``tie``, the raised value is also written at one
+    more token of the row (uniform over the vocabulary): an exact tie at the
+    maximum."""
+    rng = np.random.default_rng([3, seed])
+    tok = np.asarray(tok)
+    parent = np.asarray(parent)
+    S = tok.size
+    Z = rng.standard_normal(size=(S, V), dtype=np.float32)
+    kids = [[] for _ in range(S)]
+    for c in range(1, S):
+        kids[int(parent[c])].append(c)
+    for a in range(S):
+        if kids[a] and rng.random() < follow:
+            c = kids[a][int(rng.integers(0, len(kids[a])))]
+            v = np.float32(Z[a].max() + rng.uniform(0.25, 1.0))
+            Z[a, int(tok[c])] = v
+            if tie:
+                Z[a, int(rng.integers(0, V))] = v
+    return Z
