@@ -112,6 +112,68 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def walk_bytes(cfg):
+    """HBM bytes one acceptance walk must move: the target logits of every tree
+    slot once, the trees, the outputs."""
+    S, D = cfg.B + 1, cfg.block - 1
+    return cfg.n_req * (S * cfg.V * 4 + 2 * S * 4 + (D + 2) * 4)
+
+
+def time_accept_walk(builder, cfg, trees, stream, peak, n_launch=200):
+    """The acceptance walk (dt_accept_walk) over the round's own trees, timed
+    alone with CUDA events around graph replays on the current stream;
+    distinct target-logit buffers rotate so that their total exceeds L2."""
+    import numpy as np
+    import torch
+    from workloads import make_target_logits
+    per = cfg.n_req * (cfg.B + 1) * cfg.V * 4
+    n_in = int(min(8, max(2, -(-4 * 129e6 // per))))
+    Zs, TPs = [], []
+    for j in range(n_in):
+        t = trees[j % len(trees)]
+        tok, par = t["tok"].cpu().numpy(), t["parent"].cpu().numpy()
+        Z = np.stack([make_target_logits(tok[q], par[q], cfg.V, 7000 + 100 * j + q, follow=0.8)
+                      for q in range(cfg.n_req)])
+        Zs.append(torch.from_numpy(Z).cuda())
+        TPs.append((t["tok"], t["parent"]))
+    D = cfg.block - 1
+    acc = torch.empty(cfg.n_req, D, dtype=torch.int32, device="cuda")
+    alen = torch.empty(cfg.n_req, dtype=torch.int32, device="cuda")
+    bon = torch.empty(cfg.n_req, dtype=torch.int32, device="cuda")
+    lens = []
+    for j in range(n_in):
+        builder.accept_walk(Zs[j], *TPs[j], accepted=acc, accept_len=alen, bonus=bon)
+        lens += alen.cpu().tolist()
+    torch.cuda.synchronize()
+    # one CUDA graph of n_in launches (one per input), so that host-side call
+    # overhead does not starve a kernel of a few microseconds
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for j in range(n_in):
+                builder.accept_walk(Zs[j], *TPs[j], accepted=acc, accept_len=alen, bonus=bon, stream=side)
+    stream.wait_stream(side)
+    reps = max(1, n_launch // n_in)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n_in)
+    nb = walk_bytes(cfg)
+    del Zs
+    return {"kernel": "k_accept (row argmax + walk, one launch)", "us_per_launch": us,
+            "algorithmic_bytes_per_launch": nb, "achieved": nb / (us * 1e-6) / 1e9, "peak": peak,
+            "unit": "GB/s", "frac": nb / (us * 1e-6) / 1e9 / peak, "distinct_inputs": n_in,
+            "mean_accept_len": float(np.mean(lens)),
+            "inputs": "target logits N(0,1) per slot, the draft followed at 80 % of slots (synthetic)"}
+
+
 def replica_seeds(rank, n_inputs):
     """Round seeds of one replica: every rank builds trees of its own inputs."""
     return [rank * 100000 + s for s in range(n_inputs)]
@@ -246,6 +308,8 @@ def bench_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     lm_ms = e0.elapsed_time(e1) / nk
+    peak, peak_kind = _peaks()
+    walk = time_accept_walk(builder, cfg, outs, stream, peak) if not args.no_walk else None
     clk = clocks.stop()
     # end to end through the public API with host buffers (pinned)
     Hh = [torch.from_numpy(np.ascontiguousarray(make_round_inputs(cfg, s)[0]).view(np.int16))
@@ -268,7 +332,6 @@ def bench_gpu(args):
                                                       device="cuda" if dist is not None and
                                                       dist.get_backend() == "nccl" else "cpu")
     kbytes, rbytes = algorithmic_bytes(cfg)
-    peak, peak_kind = _peaks()
     achieved = kbytes / (lm_ms / 1e3) / 1e9
     traffic = None
     prof = os.path.join(ROOT, "profiles", f"lm_head_gemm_{cfg.name}_traffic.json")
@@ -297,6 +360,7 @@ def bench_gpu(args):
         "e2e": {"value": e2e_value, "unit": "builds/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": builder.round_kernel_count() * args.steps,
+        "accept_walk": walk,
         "clocks": clk,
         "device_status": status,
     }
@@ -343,6 +407,7 @@ def main():
     ap.add_argument("--inputs", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-walk", action="store_true", help="skip the acceptance-walk measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -65,7 +65,7 @@ struct Layout {
   size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, part_kth, cand_tok, cand_base, rest_lse,
       row_done, S, sfrag, zfrag,
       uW1, live, node_tok, node_parent, node_logp, node_score, sel, bar, status, H_dev, root_dev,
-      out_tok, out_parent, out_depth, out_logp, out_mask, total;
+      out_tok, out_parent, out_depth, out_logp, out_mask, acc_key, acc_done, total;
   size_t xtab;
 };
 
@@ -109,6 +109,8 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   put(L.out_depth, c.n_req * S1 * 4);
   put(L.out_logp, c.n_req * S1 * 4);
   put(L.out_mask, c.n_req * S1 * S1);
+  put(L.acc_key, c.n_req * S1 * 8);
+  put(L.acc_done, static_cast<size_t>(c.n_req) * 8);
   L.total = o;
   L.xtab = static_cast<size_t>(c.V) * 3 * c.g * 4;
 }
@@ -133,6 +135,7 @@ struct dt_ctx {
   float* xtab = nullptr;
   CUtensorMap tm_lm, tm_w1h;
   TopmParams topm;
+  AcceptParams acc;
   int chain_grid = 0;
   const float* logits_src = nullptr;
   int next_depth = 1;
@@ -405,6 +408,12 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->topm.M = cfg->M;
   c->topm.T = cfg->T;
   topm_plan(c->topm, c->num_sms);
+  c->acc = AcceptParams{};
+  c->acc.n_req = cfg->n_req;
+  c->acc.S = cfg->B + 1;
+  c->acc.V = cfg->V;
+  c->acc.D = c->t.D;
+  accept_plan(c->acc, c->num_sms);
   layout(*cfg, c->t, c->topm, c->lay);
   e = cudaMalloc(&c->ws, c->lay.total);
   if (e == cudaSuccess) e = cudaMalloc(&c->xtab, c->lay.xtab);
@@ -426,6 +435,9 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->topm.row_done = c->at<unsigned>(c->lay.row_done);
   c->topm.status = c->at<int>(c->lay.status);
   c->logits_src = c->at<float>(c->lay.logits);
+  c->acc.rowkey = c->at<uint64_t>(c->lay.acc_key);
+  c->acc.req_done = c->at<uint64_t>(c->lay.acc_done);
+  c->acc.status = c->at<int>(c->lay.status);
 
   ChainParams probe = {};
   probe.g = cfg->g;
@@ -563,6 +575,25 @@ dt_status dt_tree_mask(dt_ctx* c, const int32_t* sel, const int32_t* node_tok, c
   p.logp_cum = logp_cum;
   p.mask = mask;
   DT_TRY(launch_tree_mask(p, st));
+  c->last_stream = st;
+  return DT_OK;
+}
+
+dt_status dt_accept_walk(dt_ctx* c, const float* target_logits, const int32_t* tok, const int32_t* parent,
+                         int32_t* target_tok, int32_t* accepted, int32_t* accept_len, int32_t* bonus, void* stream) {
+  if (!c || !target_logits || !tok || !parent || !accepted || !accept_len || !bonus) return DT_ERR_INVALID_ARG;
+  if (c->acc.vec4 && (reinterpret_cast<uintptr_t>(target_logits) & 15u) != 0) return DT_ERR_INVALID_ARG;
+  if (c->acc.S > kAcceptMaxSlots) return DT_ERR_SHAPE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AcceptParams p = c->acc;
+  p.Z = target_logits;
+  p.tok = tok;
+  p.parent = parent;
+  p.target_tok = target_tok;
+  p.accepted = accepted;
+  p.accept_len = accept_len;
+  p.bonus = bonus;
+  DT_TRY(launch_accept(p, st));
   c->last_stream = st;
   return DT_OK;
 }

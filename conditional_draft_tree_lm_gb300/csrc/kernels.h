@@ -156,4 +156,27 @@ cudaError_t prune_prepare();
 cudaError_t launch_prune(const PruneParams& p, cudaStream_t stream);
 cudaError_t launch_tree_mask(const PruneParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- acceptance walk
+struct AcceptParams {
+  const float* Z;       // [n_req * S, V] target logits, row q*S + a = slot a of request q
+  const int* tok;       // [n_req, S]
+  const int* parent;    // [n_req, S]
+  int n_req, S, V, D;
+  long long piece;      // logits per CTA, a multiple of 4 (accept_plan)
+  int grid;             // CTAs
+  int vec4;             // 1: 16-byte loads (V a multiple of 4)
+  uint64_t* rowkey;     // [n_req * S] (value, token) key of each row (zero between launches)
+  uint64_t* req_done;   // [n_req] scanned-element counters (zero between launches)
+  int* target_tok;      // [n_req, S] or null
+  int* accepted;        // [n_req, D]
+  int* accept_len;      // [n_req]
+  int* bonus;           // [n_req]
+  int* status;
+};
+// Slots per tree the walk handles: its shared memory holds two ints per slot.
+constexpr int kAcceptMaxSlots = 3072;
+void accept_plan(AcceptParams& p, int num_sms);
+size_t accept_smem_bytes(const AcceptParams& p);
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
+
 }  // namespace dt

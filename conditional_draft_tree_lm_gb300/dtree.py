@@ -67,6 +67,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dt_expand_depth": (c_int, [vp, c_int, i32p, vp, vp, vp, vp, vp, vp]),
         "dt_prune_topB": (c_int, [vp, vp, vp, vp]),
         "dt_tree_mask": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "dt_accept_walk": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_build_round": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_build_round_host": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_get_device_status": (c_int, [vp]),
@@ -228,6 +229,31 @@ class DraftTreeBuilder:
                                      _ptr(logp_cum, torch.float32, cfg.n_req * s1, "logp_cum"),
                                      _ptr(mask, torch.uint8, cfg.n_req * s1 * s1, "mask"), _stream(stream)),
                "dt_tree_mask")
+
+    def accept_walk(self, target_logits, tok, parent, accepted=None, accept_len=None, bonus=None,
+                    target_tok=None, stream=None):
+        """Greedy verification of the emitted trees (``dt_accept_walk``).
+        target_logits [n_req, B+1, V] fp32; tok, parent [n_req, B+1] int32.
+        Returns dict(accepted [n_req, D], accept_len [n_req], bonus [n_req],
+        target_tok [n_req, B+1] or None)."""
+        import torch
+        cfg = self.cfg
+        s1 = cfg.B + 1
+        D = cfg.block - 1
+        dev = target_logits.device
+        accepted = accepted if accepted is not None else torch.empty(cfg.n_req, D, dtype=torch.int32, device=dev)
+        accept_len = accept_len if accept_len is not None else torch.empty(cfg.n_req, dtype=torch.int32, device=dev)
+        bonus = bonus if bonus is not None else torch.empty(cfg.n_req, dtype=torch.int32, device=dev)
+        _check(self.lib.dt_accept_walk(self.ctx, _ptr(target_logits, torch.float32, cfg.n_req * s1 * cfg.V,
+                                                      "target_logits"),
+                                       _ptr(tok, torch.int32, cfg.n_req * s1, "tok"),
+                                       _ptr(parent, torch.int32, cfg.n_req * s1, "parent"),
+                                       _ptr(target_tok, torch.int32, cfg.n_req * s1, "target_tok"),
+                                       _ptr(accepted, torch.int32, cfg.n_req * D, "accepted"),
+                                       _ptr(accept_len, torch.int32, cfg.n_req, "accept_len"),
+                                       _ptr(bonus, torch.int32, cfg.n_req, "bonus"), _stream(stream)),
+               "dt_accept_walk")
+        return {"accepted": accepted, "accept_len": accept_len, "bonus": bonus, "target_tok": target_tok}
 
     def new_tree(self, device="cuda"):
         """Output tensors of one round: tok, parent, depth [n_req, B+1], logp_cum, mask."""

@@ -206,6 +206,30 @@ dt_status dt_tree_mask(dt_ctx* ctx, const int32_t* sel, const int32_t* node_tok,
                        int32_t* parent, int32_t* depth, float* logp_cum, uint8_t* mask,
                        void* stream);
 
+/* Step 6 — greedy verification of the emitted trees: the acceptance walk
+ * (DominoTree page, Metodología, 5. Verificación; Resultados Experimentales,
+ * Ausencia de Pérdida).  The target model has scored every tree slot in one
+ * pass with the ancestor-only mask; its token after slot a is the argmax of its
+ * logits at a (equal maxima: the lower token id).  From the root, the walk
+ * moves into the child whose draft token equals the target's token at the
+ * current slot, while one exists; the target's token at the last slot reached
+ * is the bonus token, so accept_len + 1 tokens are committed.
+ *   target_logits: [n_req, B+1, V] fp32, finite, 16-byte aligned when V is a
+ *                  multiple of 4 (row q, a = the target's logits at slot a).
+ *   tok, parent:   [n_req, B+1] int32, a tree in dt_tree_mask's layout
+ *                  (parent[0] = -1, parent[c] < c, sibling tokens distinct).
+ *   target_tok:    [n_req, B+1] int32 out, or NULL: the target's token per slot.
+ *   accepted:      [n_req, D] int32 out: the accepted slots in path order,
+ *                  padded with -1.
+ *   accept_len:    [n_req] int32 out; bonus: [n_req] int32 out.
+ * All device pointers, caller-owned.  One launch; the logits are read once.
+ * A parent index outside [0, c) or two siblings carrying the accepted token
+ * are recorded in the device status word (DT_DEV_TREE); the lower slot is then
+ * taken.  B+1 > 3072 returns DT_ERR_SHAPE. */
+dt_status dt_accept_walk(dt_ctx* ctx, const float* target_logits, const int32_t* tok,
+                         const int32_t* parent, int32_t* target_tok, int32_t* accepted,
+                         int32_t* accept_len, int32_t* bonus, void* stream);
+
 /* --------------------------------------------------------------------------
  * Whole round.
  * ------------------------------------------------------------------------ */
