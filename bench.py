@@ -190,6 +190,14 @@ def job_throughput(dist, elapsed_s, e2e_s, steps, e2e_steps, world, device="cpu"
     return steps * world / elapsed_s, e2e_steps * world / e2e_s, elapsed_s, e2e_s
 
 
+def oracle_round(orc, cfg, H, root):
+    """One round of the oracle of the workload's builder."""
+    if getattr(cfg, "builder", "dartree") == "best_first":
+        from oracle.besttree import build_best_first
+        return [build_best_first(orc, H[q], int(root[q])) for q in range(H.shape[0])]
+    return orc.build_round(H, root)
+
+
 def run_oracle_rounds(cfg, w, seeds):
     from oracle.dartree import Oracle
     from workloads import make_round_inputs
@@ -198,7 +206,7 @@ def run_oracle_rounds(cfg, w, seeds):
     for s in seeds:
         H, root = make_round_inputs(cfg, s)
         t0 = time.perf_counter()
-        trees.append(orc.build_round(H, root))
+        trees.append(oracle_round(orc, cfg, H, root))
         times.append(time.perf_counter() - t0)
     return orc, trees, times
 
@@ -374,7 +382,7 @@ def bench_gpu(args):
         while time.perf_counter() - t_start < t_budget and k < 16:
             H, root = make_round_inputs(cfg, seeds[k % n_inputs])
             t0 = time.perf_counter()
-            orc.build_round(H, root)
+            oracle_round(orc, cfg, H, root)
             times.append(time.perf_counter() - t0)
             seeds_cpu.append(seeds[k % n_inputs])
             k += 1

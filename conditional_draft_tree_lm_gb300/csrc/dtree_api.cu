@@ -38,7 +38,8 @@ bool make_tables(const dt_config& c, Tables& t) {
 
 dt_status check(const dt_config* c) {
   if (!c) return DT_ERR_INVALID_ARG;
-  if ((c->flags & ~DT_FLAG_MARGINAL) != 0) return DT_ERR_INVALID_ARG;
+  if ((c->flags & ~(DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST)) != 0) return DT_ERR_INVALID_ARG;
+  if ((c->flags & DT_FLAG_BEST_FIRST) && c->n_req != 1) return DT_ERR_SHAPE;
   if (c->d <= 0 || c->V <= 0 || c->g <= 0 || c->r <= 0 || c->M <= 0 || c->K <= 0 || c->W <= 0 ||
       c->B <= 0 || c->n_req <= 0 || c->block < 2)
     return DT_ERR_INVALID_ARG;
@@ -136,6 +137,8 @@ struct dt_ctx {
   CUtensorMap tm_lm, tm_w1h;
   TopmParams topm;
   AcceptParams acc;
+  BestParams best;
+  int best_first = 0;
   int chain_grid = 0;
   const float* logits_src = nullptr;
   int next_depth = 1;
@@ -289,6 +292,33 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
   unsigned* bar = c->at<unsigned>(c->lay.bar);
   s = enqueue_topm(c, logits, st, bar, 1);
   if (s != DT_OK) return s;
+  int32_t* sel = c->at<int32_t>(c->lay.sel);
+  if (c->best_first) {
+    BestParams bp = c->best;
+    bp.w_hh = static_cast<const uint16_t*>(c->w.w_hh);
+    bp.w1 = static_cast<const uint16_t*>(c->w.w1);
+    bp.w2 = static_cast<const uint16_t*>(c->w.w2);
+    bp.xtab = c->xtab;
+    bp.h1 = c->at<float>(c->lay.h1);
+    bp.cand_tok = c->at<int>(c->lay.cand_tok);
+    bp.cand_base = c->at<float>(c->lay.cand_base);
+    bp.rest_lse = c->at<float>(c->lay.rest_lse);
+    bp.root_tok = root;
+    bp.srow = c->at<float>(c->lay.S);
+    bp.zrow = c->at<float>(c->lay.uW1);
+    bp.bar = bar;
+    bp.status = c->at<int>(c->lay.status);
+    bp.pdl = 1;
+    bp.sel = sel;
+    bp.pops = nullptr;
+    bp.tok = tok;
+    bp.parent = parent;
+    bp.depth = depth;
+    bp.logp_cum = logp_cum;
+    bp.mask = mask;
+    DT_TRY(launch_best(bp, c->chain_grid, st));
+    return DT_OK;
+  }
   int32_t* ntok = c->at<int32_t>(c->lay.node_tok);
   int32_t* npar = c->at<int32_t>(c->lay.node_parent);
   float* nlogp = c->at<float>(c->lay.node_logp);
@@ -297,7 +327,6 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
   cp.depth_first = 1;
   cp.depth_last = c->t.D;
   cp.pdl = 1;
-  int32_t* sel = c->at<int32_t>(c->lay.sel);
   if (chain_can_fuse_tree(cp)) {
     // single request: the chain kernel's CTA 0 also prunes and emits the tree
     cp.fuse_tree = 1;
@@ -398,6 +427,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   if (e == cudaSuccess) e = topm_prepare();
   if (e == cudaSuccess) e = chain_prepare();
   if (e == cudaSuccess) e = prune_prepare();
+  if (e == cudaSuccess) e = best_prepare();
   if (e != cudaSuccess) {
     delete c;
     return cuda_status(e, "dt_create: kernel attributes");
@@ -446,12 +476,35 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   probe.W = cfg->W;
   probe.K = cfg->K;
   probe.M = cfg->M;
-  probe.marginal = (cfg->flags & DT_FLAG_MARGINAL) ? 1 : 0;
+  // (the best-first builder always shards the state columns over the CTAs,
+  // also under marginal scoring)
+  probe.marginal = ((cfg->flags & DT_FLAG_MARGINAL) && !(cfg->flags & DT_FLAG_BEST_FIRST)) ? 1 : 0;
   c->chain_grid = chain_grid(probe, c->num_sms);
   chain_plan(probe, c->chain_grid);
   if (chain_smem_bytes(probe) > 227 * 1024 || probe.cpad > 64) {
     dt_destroy(c);
     return DT_ERR_SHAPE;
+  }
+  c->best_first = (cfg->flags & DT_FLAG_BEST_FIRST) ? 1 : 0;
+  if (c->best_first) {
+    BestParams& b = c->best;
+    b = BestParams{};
+    b.D = c->t.D;
+    b.g = cfg->g;
+    b.r = cfg->r;
+    b.M = cfg->M;
+    b.K = cfg->K;
+    b.V = cfg->V;
+    b.d = cfg->d;
+    b.ldw1 = cfg->d + cfg->g;
+    b.B = cfg->B;
+    b.T = cfg->T;
+    b.beta = cfg->beta;
+    b.marginal = (cfg->flags & DT_FLAG_MARGINAL) ? 1 : 0;
+    if (!best_plan(b, c->chain_grid)) {
+      dt_destroy(c);
+      return DT_ERR_SHAPE;
+    }
   }
 
   // tensor maps of the weights
@@ -536,6 +589,7 @@ dt_status dt_expand_depth(dt_ctx* c, int depth, const int32_t* root_tok, int32_t
                           int32_t* node_parent, float* node_logp, float* node_score, int32_t* live,
                           void* stream) {
   if (!c || !node_tok || !node_parent || !node_logp || !node_score) return DT_ERR_INVALID_ARG;
+  if (c->best_first) return DT_ERR_INVALID_ARG;  // not a depth-wise build
   if (depth < 1 || depth > c->t.D) return DT_ERR_INVALID_ARG;
   if (depth == 1 && !root_tok) return DT_ERR_INVALID_ARG;
   if (depth != 1 && depth != c->next_depth) return DT_ERR_INVALID_ARG;
@@ -686,6 +740,7 @@ dt_status dt_get_device_status(dt_ctx* c) {
 
 int dt_round_kernel_count(const dt_ctx* c) {
   if (!c) return -1;
+  if (c->best_first) return 3;  // LM head GEMM, Top-M, best-first builder (tree and mask in its tail)
   // LM head GEMM, Top-M, depth chain (+ Top-B, tree/mask unless the chain's tail does them)
   ChainParams cp = chain_params(const_cast<dt_ctx*>(c), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
   return chain_can_fuse_tree(cp) ? 3 : 5;

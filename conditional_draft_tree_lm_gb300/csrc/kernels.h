@@ -156,6 +156,41 @@ cudaError_t prune_prepare();
 cudaError_t launch_prune(const PruneParams& p, cudaStream_t stream);
 cudaError_t launch_tree_mask(const PruneParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- best-first builder
+struct BestParams {
+  int D, g, r, M, K, V, ldw1, d, B;
+  float T, beta;
+  int marginal;
+  const uint16_t* w_hh;    // [3g, g]
+  const uint16_t* w1;      // [r, d+g]
+  const uint16_t* w2;      // [V, r]
+  const float* xtab;       // [V, 3g]
+  const float* h1;         // [D, r] of the request
+  const int* cand_tok;     // [D, M]
+  const float* cand_base;  // [D, M]
+  const float* rest_lse;   // [D]
+  const int* root_tok;     // [1]
+  float* srow;             // [g] state of the node being expanded (exchanged between CTAs)
+  float* zrow;             // [r] its bottleneck z (exchanged)
+  unsigned* bar;           // grid-barrier counter, zero at launch
+  int* status;
+  int jper, rper, cpad;    // owned state columns / bottleneck rows per CTA, padded columns
+  int nmax;                // node capacity 1 + B*K
+  int xpre;                // 1: the children's GRU-input slices are prefetched into shared memory
+  int pdl;
+  int* sel;                // [B] popped nodes, ascending
+  int* pops;               // [B] popped nodes in pop order, or null
+  int* tok;                // [B+1]
+  int* parent;
+  int* depth;
+  float* logp_cum;
+  uint8_t* mask;           // [(B+1)^2]
+};
+bool best_plan(BestParams& p, int grid);
+size_t best_smem_bytes(const BestParams& p);
+cudaError_t best_prepare();
+cudaError_t launch_best(const BestParams& p, int grid, cudaStream_t stream);
+
 // ---------------------------------------------------------------- acceptance walk
 struct AcceptParams {
   const float* Z;       // [n_req * S, V] target logits, row q*S + a = slot a of request q

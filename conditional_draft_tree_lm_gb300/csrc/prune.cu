@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kThreads) k_tree_mask(const PruneParams p) {
   const size_t nb = static_cast<size_t>(q) * p.N1;
   const size_t ob = static_cast<size_t>(q) * S;
   tree_and_mask(p.sel + static_cast<size_t>(q) * p.B, p.N1, p.B, p.D, off, p.node_tok + nb, p.node_parent + nb,
-                p.node_score + nb, sm, sm + S, sm + 2 * S, reinterpret_cast<uint32_t*>(sm + 3 * S), p.tok + ob,
+                p.node_score + nb, nullptr, sm, sm + S, sm + 2 * S, reinterpret_cast<uint32_t*>(sm + 3 * S), p.tok + ob,
                 p.parent + ob, p.depth + ob, p.logp_cum + ob, p.mask + ob * S, p.status);
 }
 

@@ -182,10 +182,12 @@ DT_HOST_DEVICE_INLINE int anc_words(int S) { return (S + 31) / 32; }
 
 // sel: [B] ascending node indices.  nodes/par/dep: B+1 ints of shared memory
 // each; anc: (B+1) * anc_words(B+1) uint32 of shared memory.  node_*: [N1]
-// arrays of one request.  Outputs: tok/parent/depth/logp_cum [B+1], mask
-// [(B+1)^2].
+// arrays of one request; node_depth may be null, then a node's depth comes
+// from the depth offsets off (depth-major numbering).  Outputs:
+// tok/parent/depth/logp_cum [B+1], mask [(B+1)^2].
 DT_DEVINL void tree_and_mask(const int* sel, int N1, int B, int D, const int* off, const int* node_tok,
-                             const int* node_parent, const float* node_score, int* nodes, int* par, int* dep,
+                             const int* node_parent, const float* node_score, const int* node_depth, int* nodes,
+                             int* par, int* dep,
                              uint32_t* anc, int* tok, int* parent, int* depth, float* logp_cum, uint8_t* mask,
                              int* status) {
   const int S = B + 1;
@@ -205,7 +207,7 @@ DT_DEVINL void tree_and_mask(const int* sel, int N1, int B, int D, const int* of
     const int v = nodes[k];
     int ps = -1, d = 0;
     if (k > 0) {
-      d = depth_of(off, D, v);
+      d = node_depth ? node_depth[v] : depth_of(off, D, v);
       const int pv = node_parent[v];
       // binary search of pv among nodes[0..S) (ascending)
       int lo = 0, hi = S - 1;

@@ -38,6 +38,7 @@ class DtConfig(ctypes.Structure):
 
 WEIGHT_FIELDS = ("lm_head", "emb", "w_ih", "b_ih", "w_hh", "w1", "w2")
 FLAG_MARGINAL = 1  # DT_FLAG_MARGINAL: marginal scoring (no correction)
+FLAG_BEST_FIRST = 2  # DT_FLAG_BEST_FIRST: sequential conditional best-first builder
 
 
 class DtWeights(ctypes.Structure):
@@ -89,10 +90,12 @@ def status_string(s: int) -> str:
 
 def make_config(cfg) -> DtConfig:
     """DtConfig from any object with the workload fields (d, V, block, g, r, M, K, W, B, n_req, beta, T,
-    and optionally marginal)."""
+    and optionally marginal and builder)."""
+    flags = FLAG_MARGINAL if getattr(cfg, "marginal", False) else 0
+    if getattr(cfg, "builder", "dartree") == "best_first":
+        flags |= FLAG_BEST_FIRST
     return DtConfig(cfg.d, cfg.V, cfg.block, cfg.g, cfg.r, cfg.M, cfg.K, cfg.W, cfg.B,
-                    getattr(cfg, "n_req", 1), float(cfg.beta), float(cfg.T),
-                    FLAG_MARGINAL if getattr(cfg, "marginal", False) else 0)
+                    getattr(cfg, "n_req", 1), float(cfg.beta), float(cfg.T), flags)
 
 
 def check_config(cfg) -> int:

@@ -71,7 +71,7 @@ typedef struct dt_config {
   int n_req;  /* independent requests per round; n_req * block <= 512 */
   float beta; /* depth bonus of the Top-B key (score + beta * depth); <= 0 */
   float T;    /* temperature dividing the corrected logits; > 0 */
-  unsigned flags; /* 0 or DT_FLAG_MARGINAL */
+  unsigned flags; /* DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST, or 0 */
 } dt_config;
 
 /* Marginal scoring over the same super-tree: the correction Delta L is left
@@ -81,6 +81,21 @@ typedef struct dt_config {
  * "Ablación de la Condicionalidad").  No GRU state is kept; the depth chain
  * runs on one CTA. */
 #define DT_FLAG_MARGINAL 1u
+
+/* Sequential conditional best-first construction instead of depth batching:
+ * the node-by-node builder of the DominoTree summary (Metodología, 1. Montículo
+ * de Mejor Primera Búsqueda con Puntuación Condicional).  The root is
+ * expanded, then B pops of the frontier node with the largest score +
+ * beta * depth (equal keys: the lower node index; nodes are numbered in
+ * creation order, an expansion's K children in token order); each popped
+ * node below depth D, except the B-th, gets its GRU state and is expanded with
+ * the same correction and log-partition.  The tree is the root plus the popped
+ * nodes in ascending node index.  W is not used.  Only dt_build_round and
+ * dt_build_round_host build in this mode (dt_expand_depth returns
+ * DT_ERR_INVALID_ARG); n_req must be 1, M <= 64 with M % 8 == 0, and the
+ * frontier (1 + B*K nodes) must fit in shared memory, else dt_create returns
+ * DT_ERR_SHAPE.  Combines with DT_FLAG_MARGINAL. */
+#define DT_FLAG_BEST_FIRST 2u
 
 /* Frozen weights (device pointers, borrowed: they must outlive the context).
  * All bf16, row-major, torch.nn.Linear out-by-in layout.  GRU gate blocks are
@@ -104,7 +119,8 @@ typedef struct dt_ctx dt_ctx;
 /* Validate a configuration: K <= M <= V, M <= 512, 1 <= K <= 32,
  * 1 <= W <= 64, 2 <= block <= 64, d % 8 == 0, g % 8 == 0, r % 8 == 0,
  * r <= 1024, g <= 4096, n_req * block <= 512, 1 <= B <= N, T > 0, beta <= 0,
- * flags 0 or DT_FLAG_MARGINAL.  Returns DT_OK, DT_ERR_INVALID_ARG or DT_ERR_SHAPE. */
+ * flags within DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST.  Returns DT_OK,
+ * DT_ERR_INVALID_ARG or DT_ERR_SHAPE. */
 dt_status dt_check_config(const dt_config* cfg);
 
 /* N: super-tree nodes of one request without the root (n_1 = K,

@@ -61,6 +61,7 @@ def test_check_config_accepts_named_workloads(lib):
     (dict(n_req=100), 2),           # n_req * block > 512
     (dict(K=40, M=64), 2),          # K above 32
     (dict(block=1), 1),
+    (dict(builder="best_first", n_req=2), 2),   # the best-first builder takes one request
 ])
 def test_check_config_rejects(lib, bad, code):
     from conditional_draft_tree_lm_gb300 import check_config
@@ -83,3 +84,15 @@ def test_workspace_bytes(lib):
     logits = (cfg.block - 1) * cfg.V * 4
     assert xtab + logits < n < xtab + logits + 64 * 2 ** 20
     assert workspace_bytes(get_config("tiny_bf16", K=20, M=16)) == 0
+
+
+def test_check_config_flags(lib):
+    """Unknown flag bits are rejected; the two defined flags combine."""
+    import ctypes
+    from conditional_draft_tree_lm_gb300.dtree import load_library, make_config
+    cfg = make_config(get_config("tiny_bf16", builder="best_first", marginal=True))
+    assert cfg.flags == 3
+    L = load_library()
+    assert L.dt_check_config(ctypes.byref(cfg)) == 0
+    cfg.flags = 4
+    assert L.dt_check_config(ctypes.byref(cfg)) == 1

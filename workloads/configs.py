@@ -33,6 +33,7 @@ class WorkloadConfig:
     h_scale: str = "unit"   # "unit": H ~ N(0,1); "heavy": per-position scale ~ U[0.5, 4]
     weight_dtype: str = "bf16"  # "bf16" (rounded, RNE) or "fp32"
     marginal: bool = False      # marginal scoring: Delta L = 0 (path-independent children)
+    builder: str = "dartree"    # "dartree" (depth-batched) or "best_first" (sequential heap)
 
     @property
     def D(self) -> int:
@@ -71,6 +72,11 @@ CONFIGS = {
     "qwen3_4b_marginal": WorkloadConfig("qwen3_4b_marginal", d=2560, V=151936, block=16, g=1024,
                                         r=256, M=64, K=8, W=8, B=64, beta=0.0, T=1.0, marginal=True),
     # Wide tree with heavy-tailed H (betas 0, -0.25, -1 are run).
+    # The Qwen3-4B shape built node by node by the sequential conditional
+    # best-first heap (the builder that depth batching replaces).
+    "qwen3_4b_best_first": WorkloadConfig("qwen3_4b_best_first", d=2560, V=151936, block=16, g=1024,
+                                          r=256, M=64, K=8, W=8, B=64, beta=0.0, T=1.0,
+                                          builder="best_first"),
     "wide": WorkloadConfig("wide", d=2560, V=151936, block=16, g=1024, r=256,
                            M=256, K=32, W=64, B=512, beta=0.0, T=1.0,
                            h_scale="heavy"),
