@@ -160,12 +160,24 @@ DT_HOST_DEVICE_INLINE size_t stage_bytes(const Shape& sh, int which) {
   return sh.dbuf ? 2 * al16(stage_one(sh, which)) : stage_one(sh, which);
 }
 
+// Bytes of the tensor-core phase B's z rows (high and low parts) and of its
+// (lambda, token) keys.  They share region 1 with the state chunk of phase A
+// (sh, sl): phase A is done with it before phase B starts, and phase B before
+// the next depth's phase A.
+DT_HOST_DEVICE_INLINE size_t zrows_bytes(const Shape& sh) {
+  return sh.mma_b ? al16(static_cast<size_t>(2 * 16 * ((sh.W + 15) / 16)) * (sh.r + 8) * 2) : 0;
+}
+DT_HOST_DEVICE_INLINE size_t lamkey_bytes(const Shape& sh) {
+  return sh.mma_b ? static_cast<size_t>(sh.W) * sh.M * 8 : 0;
+}
+
 DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
   const size_t WK = static_cast<size_t>(sh.W) * sh.K;
   const size_t gp = static_cast<size_t>(kstride(sh.g));
+  const size_t shsl = gp * kPC * 2 * 2, zl = zrows_bytes(sh) + lamkey_bytes(sh);
   const size_t sz[23] = {
       gp * sh.cpad * 2,
-      gp * kPC * 2 * 2,
+      shsl > zl ? shsl : zl,
       static_cast<size_t>(kWarps) * kPC * sh.cpad * 4,
       static_cast<size_t>(sh.n_req) * sh.W * 3 * sh.jper * 4,
       sh.mma_b ? 0 : static_cast<size_t>(kWarps) * sh.r * 4,
@@ -185,8 +197,8 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
       static_cast<size_t>(sh.W) * 4,
       static_cast<size_t>(sh.W) * 4,
       sh.prefetch ? static_cast<size_t>(sh.D) * sh.M * 4 : 0,
-      sh.mma_b ? static_cast<size_t>(2 * 16 * ((sh.W + 15) / 16)) * (sh.r + 8) * 2 : 0,
-      sh.mma_b ? static_cast<size_t>(sh.W) * sh.M * 8 : 0,
+      0,  // (z rows: in region 1)
+      0,  // ((lambda, token) keys: in region 1)
   };
   SmemSizes s;
   size_t o = 0;
@@ -335,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     s.pnode = reinterpret_cast<int*>(smem_raw + L.off[19]);
     s.tok_all = reinterpret_cast<int*>(smem_raw + L.off[20]);
     s.ctk_buf = s.ctk;
-    s.zh = reinterpret_cast<uint16_t*>(smem_raw + L.off[21]);
+    s.zh = reinterpret_cast<uint16_t*>(smem_raw + L.off[1]);
     s.zl = s.zh + static_cast<size_t>(16 * ((W + 15) / 16)) * (r + 8);
-    s.lamkey = reinterpret_cast<uint64_t*>(smem_raw + L.off[22]);
+    s.lamkey = reinterpret_cast<uint64_t*>(smem_raw + L.off[1] + zrows_bytes(sh));
   }
 
   // ---- the owned weight columns, K-major: s.w[c][k] (zero padded) ----
@@ -821,12 +833,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           se = warp_sum(se) + expf(rest - lmax);
           const float logZ = lmax + logf(se);
           int* win = s.crank + b * K;
-          for (int c = lane; c < M; c += 32) {
-            const uint64_t kc = kb[c];
-            int rk = 0;
-#pragma unroll 8
-            for (int c2 = 0; c2 < M; ++c2) rk += kb[c2] > kc ? 1 : 0;
-            if (rk < K) win[rk] = c;
+          // the K best by K rounds of a warp argmax over the keys held in
+          // registers (candidate c = lane + 32 j; keys are distinct)
+          {
+            uint64_t kr[MPL];
+#pragma unroll
+            for (int j = 0; j < MPL; ++j) {
+              const int c = lane + 32 * j;
+              kr[j] = c < M ? kb[c] : 0ull;
+            }
+            for (int kk = 0; kk < K; ++kk) {
+              uint64_t best = 0ull;
+#pragma unroll
+              for (int j = 0; j < MPL; ++j) best = kr[j] > best ? kr[j] : best;
+              best = warp_max_u64(best);
+              int wc = -1;
+#pragma unroll
+              for (int j = 0; j < MPL; ++j)
+                if (best != 0ull && kr[j] == best) {
+                  wc = lane + 32 * j;
+                  kr[j] = 0ull;
+                }
+              const unsigned own = __ballot_sync(0xFFFFFFFFu, wc >= 0);
+              wc = __shfl_sync(0xFFFFFFFFu, wc, own ? __ffs(own) - 1 : 0);
+              if (lane == 0) win[kk] = wc;
+            }
           }
           __syncwarp();
           if (lane < K) {
