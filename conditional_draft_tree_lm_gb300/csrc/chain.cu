@@ -388,14 +388,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     }
   }
   __syncthreads();
-  // stage the first depth's request 0 (overlaps the root step and phase A)
-  select_row_tokens(p, sh, s, 0, p.depth_first);
-  __syncthreads();
+  // Several requests: CTA c selects for requests c, c + G, ... (G CTAs) and
+  // every CTA then updates its state columns of all requests after one more
+  // grid barrier.  One request: every CTA selects for it (identically) and
+  // updates its own columns right away.
+  const bool dist = n_req > 1;
+  const int qfirst = dist ? static_cast<int>(blockIdx.x) : 0;
+  const int qstep = dist ? static_cast<int>(gridDim.x) : 1;
+  // stage the first depth's first request of this CTA (overlaps the root
+  // step and phase A)
   auto buf = [&](int depth) -> Stage { return (depth & 1) ? s.st1 : s.st0; };
   // on a barrier timeout: let the CTA's own copies land before it returns
   auto drain = [&]() { cp_async_wait_all(); };
-  stage_row(p, sh, buf(p.depth_first), s.ctk, static_cast<size_t>(p.depth_first - 1), j0, nj,
-            p.depth_first != D);
+  if (qfirst < n_req) {
+    select_row_tokens(p, sh, s, qfirst, p.depth_first);
+    __syncthreads();
+    stage_row(p, sh, buf(p.depth_first), s.ctk,
+              static_cast<size_t>(qfirst) * D + (p.depth_first - 1), j0, nj, !dist && p.depth_first != D);
+  }
 
   unsigned epoch = 0;
 
@@ -627,13 +637,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     // ================= phase B: corrected log-probs and selections ==========
     const int row_off = p.off[i];
     const int nchild = Lp * K;
-    for (int q = 0; q < n_req; ++q) {
+    for (int q = qfirst; q < n_req; q += qstep) {
       const size_t qrow = static_cast<size_t>(q) * D + (i - 1);
-      if (q > 0) {
+      if (q != qfirst) {
         __syncthreads();
         select_row_tokens(p, sh, s, q, i);
         __syncthreads();
-        stage_row(p, sh, buf(i), s.ctk, qrow, j0, nj, !last);
+        stage_row(p, sh, buf(i), s.ctk, qrow, j0, nj, !dist && !last);
       }
       {
         const Stage cur = buf(i);
@@ -992,8 +1002,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
       __syncthreads();
-      // node arrays of this depth (CTA 0)
-      if (blockIdx.x == 0) {
+      // node arrays of this depth (CTA 0, or the request's CTA)
+      if (dist || blockIdx.x == 0) {
         const size_t nb = static_cast<size_t>(q) * p.N1 + row_off;
         for (int e = tid; e < nchild; e += kThreads) {
           p.node_tok[nb + e] = s.ctok[e];
@@ -1076,7 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           }
         }
         __syncthreads();
-        if (blockIdx.x == 0) {
+        if (dist || blockIdx.x == 0) {
           for (int j = tid; j < W; j += kThreads) {
             const int node = j < Li ? row_off + s.surv[q * W + j] : -1;
             if (j < Li) live_next[static_cast<size_t>(q) * W + j] = node;
@@ -1084,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           }
         }
         // ================= phase C (this request): GRU of the survivors ======
-        for (int idx = tid; idx < Li * nj; idx += kThreads) {
+        for (int idx = tid; idx < (dist ? 0 : Li * nj); idx += kThreads) {
           const int jv = idx / nj, jj = idx - jv * nj;
           const int e = s.surv[q * W + jv];
           const int b = e / K;
@@ -1099,17 +1109,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           if (sh.frag)
             store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
         }
-      } else if (blockIdx.x == 0 && p.live_out) {
+      } else if ((dist || blockIdx.x == 0) && p.live_out) {
         for (int j = tid; j < W; j += kThreads) p.live_out[static_cast<size_t>(q) * W + j] = -1;
       }
     }
+    if (dist && !last) {
+      // ================= phase C (all requests): GRU of the survivors =====
+      // the survivors (node indices) and their tokens come from the
+      // requests' CTAs through global memory
+      if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
+        drain();
+        return;
+      }
+      for (int idx = tid; idx < n_req * Li * nj; idx += kThreads) {
+        const int qv = idx / nj, jj = idx - qv * nj;
+        const int q = qv / Li, jv = qv - q * Li;
+        const int node = __ldcg(live_next + static_cast<size_t>(q) * W + jv);
+        const int e = node - row_off;
+        int tok = __ldcg(p.node_tok + static_cast<size_t>(q) * p.N1 + node);
+        if (e < 0 || e >= Lp * K || tok < 0 || tok >= p.V) {
+          dt_report(p.status, DT_DEV_BOUNDS);
+          continue;
+        }
+        const int b = e / K;
+        const float* x = p.xtab + static_cast<size_t>(tok) * 3 * g + j0 + jj;
+        const float* uu = s.uu + static_cast<size_t>(q * Lp + b) * 3 * sh.jper;
+        const float h = Sprev[static_cast<size_t>(q * W + b) * g + j0 + jj];
+        const float rg = sigmoidf_(x[0] + uu[jj]);
+        const float zg = sigmoidf_(x[g] + uu[nj + jj]);
+        const float ng = tanhf_(x[2 * g] + rg * uu[2 * nj + jj]);
+        Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = (1.0f - zg) * ng + zg * h;
+      }
+    }
     if (i < p.depth_last) {
-      if (!sh.dbuf) {
-        // stage the next depth's request 0 now: the copies overlap the barrier
+      if (!sh.dbuf && qfirst < n_req) {
+        // stage the next depth's first request of this CTA now: the copies
+        // overlap the barrier
         __syncthreads();
-        select_row_tokens(p, sh, s, 0, i + 1);
-        if (!sh.prefetch) __syncthreads();
-        stage_row(p, sh, buf(i + 1), s.ctk, static_cast<size_t>(i), j0, nj, i + 1 != D);
+        select_row_tokens(p, sh, s, qfirst, i + 1);
+        if (!(qfirst == 0 && sh.prefetch)) __syncthreads();
+        stage_row(p, sh, buf(i + 1), s.ctk, static_cast<size_t>(qfirst) * D + i, j0, nj, !dist && i + 1 != D);
       }
       if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
         drain();
