@@ -65,6 +65,9 @@ struct Shape {
   // with frag and the tensor-core phase B: z is published as fragments by the
   // bottleneck-row owners (zfrag) instead of u_W1
   bool zf;
+  // several requests (8-state blocks): phase A copies the states as
+  // ready-made fragments block by block into shared memory
+  bool mfrag;
 };
 
 DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
@@ -74,11 +77,16 @@ DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
 // The candidate tokens of every depth of request 0 are read once, at launch.
 DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096; }
 
+DT_HOST_DEVICE_INLINE bool mfrag_ok(const ChainParams& p) {
+  return !p.marginal && p.n_req > 1 && (p.n_req * p.W) % 8 == 0 && p.g % 16 == 0;
+}
+
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
   const bool fr = !p.marginal && frag_ok(p.n_req, p.W, p.g);
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
                prefetch_tokens(p.D, p.M), p.dbuf != 0, fr,
-               fr && p.mma_b != 0 && p.dbuf != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax};
+               fr && p.mma_b != 0 && p.dbuf != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax,
+               mfrag_ok(p)};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -88,7 +96,7 @@ struct DimsRuntime {
 // The Qwen3-4B shape (g=1024, r=256, M=64, K=W=8, one request, depth 15, 128
 // CTAs): dimensions are literals, so the compiler folds the index arithmetic.
 struct DimsQ4B {
-  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true, true};
+  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true, true, false};
   static DT_DEVINL Shape get(const ChainParams&) { return kShape; }
 };
 
@@ -128,6 +136,8 @@ struct Smem {
   uint16_t* zh;     // [16*ceil(W/16)][r+8] bf16 high part of z (tensor-core phase B)
   uint16_t* zl;     // same, low part
   uint64_t* lamkey; // [W][M] (lambda, token) keys (tensor-core phase B)
+  uint4* mf0;       // fragment blocks of the states, two buffers (several requests)
+  uint4* mf1;
   Stage st0, st1;   // stage buffers of even and odd depths (the same buffer without dbuf)
 };
 
@@ -175,9 +185,11 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
   const size_t WK = static_cast<size_t>(sh.W) * sh.K;
   const size_t gp = static_cast<size_t>(kstride(sh.g));
   const size_t shsl = gp * kPC * 2 * 2, zl = zrows_bytes(sh) + lamkey_bytes(sh);
+  const size_t mblk = sh.mfrag ? static_cast<size_t>(32) * sh.g : 0;  // one 8-state fragment block
+  const size_t r1 = shsl > zl ? shsl : zl;
   const size_t sz[23] = {
       gp * sh.cpad * 2,
-      shsl > zl ? shsl : zl,
+      r1 > mblk ? r1 : mblk,
       static_cast<size_t>(kWarps) * kPC * sh.cpad * 4,
       static_cast<size_t>(sh.n_req) * sh.W * 3 * sh.jper * 4,
       sh.mma_b ? 0 : static_cast<size_t>(kWarps) * sh.r * 4,
@@ -197,8 +209,8 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
       static_cast<size_t>(sh.W) * 4,
       static_cast<size_t>(sh.W) * 4,
       sh.prefetch ? static_cast<size_t>(sh.D) * sh.M * 4 : 0,
-      0,  // (z rows: in region 1)
-      0,  // ((lambda, token) keys: in region 1)
+      mblk,  // the second fragment-block buffer (the first is region 1)
+      0,     // (z rows and (lambda, token) keys: in region 1)
   };
   SmemSizes s;
   size_t o = 0;
@@ -350,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     s.zh = reinterpret_cast<uint16_t*>(smem_raw + L.off[1]);
     s.zl = s.zh + static_cast<size_t>(16 * ((W + 15) / 16)) * (r + 8);
     s.lamkey = reinterpret_cast<uint64_t*>(smem_raw + L.off[1] + zrows_bytes(sh));
+    s.mf0 = reinterpret_cast<uint4*>(smem_raw + L.off[1]);
+    s.mf1 = reinterpret_cast<uint4*>(smem_raw + L.off[21]);
   }
 
   // ---- the owned weight columns, K-major: s.w[c][k] (zero padded) ----
@@ -423,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       const float ng = tanhf_(x[2 * g + jj]);
       const float s0 = (1.0f - zg) * ng;
       p.S[static_cast<size_t>(q * W) * g + jj] = s0;
-      if (sh.frag) store_frag(p.sfrag, q * W, jj, g / 16, s0);  // parity 0 = depth 0
+      if (sh.frag || sh.mfrag) store_frag(p.sfrag, q * W, jj, g / 16, s0);  // parity 0 = depth 0
     }
     if (blockIdx.x == 0) {
       for (int q = tid; q < n_req; q += kThreads) {
@@ -535,7 +549,72 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
     }
-    for (int p0 = 0; p0 < (sh.frag || p.marginal ? 0 : P); p0 += kPC) {
+    if (sh.mfrag) {
+      // several requests: the states as ready-made fragments, block by block
+      // (8 states: rows 0-7 of the tile carry the high parts, rows 8-15 the
+      // low parts), each block copied whole into shared memory with cp.async
+      // two blocks ahead; the k16 steps are split over the warps and their
+      // partial sums added through s.red
+      const int nk16 = g / 16;
+      const int nblk = n_req * W / 8;
+      const int blk4 = 2 * g;  // 16-byte words of one block: 8 states x g words / 4
+      const uint4* fr = reinterpret_cast<const uint4*>(p.sfrag + static_cast<size_t>((i - 1) & 1) * n_req * W * g);
+      auto load_blk = [&](int rb) {
+        uint4* dst = (rb & 1) ? s.mf1 : s.mf0;
+        const uint4* src = fr + static_cast<size_t>(rb) * blk4;
+        for (int idx = tid; idx < blk4; idx += kThreads) cp_async16(dst + idx, src + idx);
+        cp_async_commit();
+      };
+      const int gid = lane >> 2, tig = lane & 3;
+      const int ntiles = cpad / 8;
+      load_blk(0);
+      if (nblk > 1) load_blk(1);
+      for (int rb = 0; rb < nblk; ++rb) {
+        if (rb + 1 < nblk) cp_async_wait_group1();
+        else cp_async_wait_all();
+        __syncthreads();
+        const uint4* fb = (rb & 1) ? s.mf1 : s.mf0;
+        float acc[kMaxNTiles][4];
+#pragma unroll
+        for (int nt = 0; nt < kMaxNTiles; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        for (int kt = warp; kt < nk16; kt += kWarps) {
+          const uint4 f = fb[(gid * nk16 + kt) * 4 + tig];
+          const int k0 = kt * 16 + 2 * tig;
+#pragma unroll
+          for (int nt = 0; nt < kMaxNTiles; ++nt) {
+            if (nt < ntiles) {
+              const uint16_t* wc = s.w + static_cast<size_t>(nt * 8 + gid) * gp + k0;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wc);
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wc + 8);
+              mma_bf16_16816(acc[nt], f.x, f.z, f.y, f.w, b0, b1);
+            }
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < kMaxNTiles; ++nt) {
+          if (nt < ntiles) {
+            float* rw = s.red + (warp * kPC + gid) * cpad + nt * 8 + 2 * tig;
+            rw[0] = acc[nt][0] + acc[nt][2];
+            rw[1] = acc[nt][1] + acc[nt][3];
+          }
+        }
+        __syncthreads();
+        if (rb + 2 < nblk) load_blk(rb + 2);  // into the buffer just read
+        for (int idx = tid; idx < kPC * ncol; idx += kThreads) {
+          const int rr = idx / ncol, c = idx - rr * ncol;
+          const int st = rb * 8 + rr, q = st / W, b = st - q * W;
+          if (b >= Lp) continue;
+          float sum = 0.0f;
+#pragma unroll
+          for (int w8 = 0; w8 < kWarps; ++w8) sum += s.red[(w8 * kPC + rr) * cpad + c];
+          if (c < 3 * nj) s.uu[static_cast<size_t>(q * Lp + b) * 3 * sh.jper + c] = sum;
+          else p.uW1[static_cast<size_t>(q * W + b) * r + r0 + (c - 3 * nj)] = sum;
+        }
+      }
+    }
+    for (int p0 = 0; p0 < (sh.frag || sh.mfrag || p.marginal ? 0 : P); p0 += kPC) {
       const int pc = min(kPC, P - p0);
       __syncthreads();
       // state rows -> bf16 high + low parts (S = hi + lo to ~16 mantissa bits)
@@ -1138,7 +1217,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         const float rg = sigmoidf_(x[0] + uu[jj]);
         const float zg = sigmoidf_(x[g] + uu[nj + jj]);
         const float ng = tanhf_(x[2 * g] + rg * uu[2 * nj + jj]);
-        Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = (1.0f - zg) * ng + zg * h;
+        const float hn = (1.0f - zg) * ng + zg * h;
+        Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = hn;
+        if (sh.mfrag)
+          store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
       }
     }
     if (i < p.depth_last) {
