@@ -78,7 +78,8 @@ DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
 DT_HOST_DEVICE_INLINE bool prefetch_tokens(int D, int M) { return D * M <= 4096; }
 
 DT_HOST_DEVICE_INLINE bool mfrag_ok(const ChainParams& p) {
-  return !p.marginal && p.n_req > 1 && (p.n_req * p.W) % 8 == 0 && p.g % 16 == 0;
+  return !p.marginal && p.n_req > 1 && (p.n_req * p.W) % 8 == 0 && p.g % 16 == 0 &&
+         p.g <= 16 * kWarps * kFragMax;
 }
 
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
@@ -305,6 +306,7 @@ template <int MPL, class Dm>
 __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int s_abort;
+  __shared__ __align__(8) uint64_t s_mbar[2];  // fragment-block copies (several requests)
   __shared__ int s_wcnt[kWarps];
   __shared__ uint32_t s_state[4];
   __shared__ float s_tred[64];  // Top-B min/max partials of the tail
@@ -365,6 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     s.mf0 = reinterpret_cast<uint4*>(smem_raw + L.off[1]);
     s.mf1 = reinterpret_cast<uint4*>(smem_raw + L.off[21]);
   }
+
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(&s_mbar[0], 1);
+    mbar_init(&s_mbar[1], 1);
+    fence_mbar_init();
+  }
+  uint32_t mf_phase = 0;  // completed-phase parity of the two block buffers
 
   // ---- the owned weight columns, K-major: s.w[c][k] (zero padded) ----
   const int gp = kstride(g);
@@ -439,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       p.S[static_cast<size_t>(q * W) * g + jj] = s0;
       if (sh.frag || sh.mfrag) store_frag(p.sfrag, q * W, jj, g / 16, s0);  // parity 0 = depth 0
     }
+    if (sh.mfrag) fence_proxy_async_global();
     if (blockIdx.x == 0) {
       for (int q = tid; q < n_req; q += kThreads) {
         const size_t b = static_cast<size_t>(q) * p.N1;
@@ -486,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
 #pragma unroll
       for (int m = 0; m < kFragMax; ++m) {
         const int kt = warp + kWarps * m;
-        f[m] = kt < nk16 ? __ldcg(fr + (static_cast<size_t>(gid) * nk16 + kt) * 4 + tig) : make_uint4(0u, 0u, 0u, 0u);
+        f[m] = kt < nk16 ? __ldcg(fr + frag_word(gid, kt, tig, nk16)) : make_uint4(0u, 0u, 0u, 0u);
       }
       // one request: the next depth's candidate data is staged now, into the
       // other buffer (its last reader, depth i-1, finished before the
@@ -559,36 +570,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       const int nblk = n_req * W / 8;
       const int blk4 = 2 * g;  // 16-byte words of one block: 8 states x g words / 4
       const uint4* fr = reinterpret_cast<const uint4*>(p.sfrag + static_cast<size_t>((i - 1) & 1) * n_req * W * g);
+      // every CTA reads every block: each starts at a different block, so
+      // that the CTAs do not all read the same lines at the same time
+      const int rot = static_cast<int>(blockIdx.x) % nblk;
+      // one bulk copy per block (thread 0), completing on the buffer's
+      // mbarrier; the fragments were written by generic stores before the
+      // grid barrier
+      if (tid == 0) fence_proxy_async_global();
       auto load_blk = [&](int rb) {
-        uint4* dst = (rb & 1) ? s.mf1 : s.mf0;
-        const uint4* src = fr + static_cast<size_t>(rb) * blk4;
-        for (int idx = tid; idx < blk4; idx += kThreads) cp_async16(dst + idx, src + idx);
-        cp_async_commit();
+        if (tid == 0) {
+          uint4* dst = (rb & 1) ? s.mf1 : s.mf0;
+          const int rbr = rb + rot < nblk ? rb + rot : rb + rot - nblk;
+          mbar_arrive_expect_tx(&s_mbar[rb & 1], static_cast<uint32_t>(blk4) * 16u);
+          bulk_g2s(dst, fr + static_cast<size_t>(rbr) * blk4, static_cast<uint32_t>(blk4) * 16u, &s_mbar[rb & 1]);
+        }
       };
       const int gid = lane >> 2, tig = lane & 3;
       const int ntiles = cpad / 8;
       load_blk(0);
       if (nblk > 1) load_blk(1);
       for (int rb = 0; rb < nblk; ++rb) {
-        if (rb + 1 < nblk) cp_async_wait_group1();
-        else cp_async_wait_all();
+        const int sb = rb & 1;
+        if (!mbar_wait(&s_mbar[sb], (mf_phase >> sb) & 1u, p.status)) s_abort = 1;
+        mf_phase ^= 1u << sb;
         __syncthreads();
-        const uint4* fb = (rb & 1) ? s.mf1 : s.mf0;
+        if (s_abort) {
+          // a copy that never completed: stop here (every CTA times out at
+          // its next grid barrier)
+          drain();
+          return;
+        }
+        const uint4* fb = sb ? s.mf1 : s.mf0;
         float acc[kMaxNTiles][4];
 #pragma unroll
         for (int nt = 0; nt < kMaxNTiles; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-        for (int kt = warp; kt < nk16; kt += kWarps) {
-          const uint4 f = fb[(gid * nk16 + kt) * 4 + tig];
-          const int k0 = kt * 16 + 2 * tig;
+        // the warp's fragments first (g <= 16 * kWarps * kFragMax), then the products
+        uint4 f[kFragMax];
 #pragma unroll
-          for (int nt = 0; nt < kMaxNTiles; ++nt) {
-            if (nt < ntiles) {
-              const uint16_t* wc = s.w + static_cast<size_t>(nt * 8 + gid) * gp + k0;
-              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wc);
-              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wc + 8);
-              mma_bf16_16816(acc[nt], f.x, f.z, f.y, f.w, b0, b1);
+        for (int m = 0; m < kFragMax; ++m) {
+          const int kt = warp + kWarps * m;
+          f[m] = kt < nk16 ? fb[frag_word(gid, kt, tig, nk16)] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int m = 0; m < kFragMax; ++m) {
+          const int kt = warp + kWarps * m;
+          if (kt < nk16) {
+            const int k0 = kt * 16 + 2 * tig;
+#pragma unroll
+            for (int nt = 0; nt < kMaxNTiles; ++nt) {
+              if (nt < ntiles) {
+                const uint16_t* wc = s.w + static_cast<size_t>(nt * 8 + gid) * gp + k0;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wc);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wc + 8);
+                mma_bf16_16816(acc[nt], f[m].x, f[m].z, f[m].y, f[m].w, b0, b1);
+              }
             }
           }
         }
@@ -604,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         if (rb + 2 < nblk) load_blk(rb + 2);  // into the buffer just read
         for (int idx = tid; idx < kPC * ncol; idx += kThreads) {
           const int rr = idx / ncol, c = idx - rr * ncol;
-          const int st = rb * 8 + rr, q = st / W, b = st - q * W;
+          const int rbr = rb + rot < nblk ? rb + rot : rb + rot - nblk;
+          const int st = rbr * 8 + rr, q = st / W, b = st - q * W;
           if (b >= Lp) continue;
           float sum = 0.0f;
 #pragma unroll
@@ -764,16 +802,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         s.pscore[b] = (node >= 0 && node < p.N1) ? p.node_score[static_cast<size_t>(q) * p.N1 + node] : 0.0f;
       }
       if (sh.zf) {
-        // global order [gid][kt][tig] -> shared order [kt][gid][tig]
-        const int nk = r / 16, nzw = kPC * nk * 4;
+        // the block's words, [kt][gid][tig] as in global memory
+        const int nzw = kPC * (r / 16) * 4;
         uint4* zs4 = reinterpret_cast<uint4*>(s.zh);
 #pragma unroll
         for (int u = 0; u < kZPer; ++u) {
           const int idx = tid + u * kThreads;
-          if (idx < nzw) {
-            const int tg = idx & 3, rest4 = idx >> 2, gd = rest4 / nk, kt = rest4 - gd * nk;
-            zs4[(kt * kPC + gd) * 4 + tg] = zq[u];
-          }
+          if (idx < nzw) zs4[idx] = zq[u];
         }
       }
       if (sh.dbuf && i < p.depth_last)
@@ -1222,6 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         if (sh.mfrag)
           store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
       }
+      if (sh.mfrag) fence_proxy_async_global();  // the next depth bulk-copies these fragments
     }
     if (i < p.depth_last) {
       if (!sh.dbuf && qfirst < n_req) {

@@ -84,13 +84,19 @@ DT_DEVINL bool grid_barrier(unsigned* bar, unsigned& epoch, int* status, int* s_
 // Store state value v of (row, column j) into the fragment-ordered copy: its
 // bf16 high part and the bf16 of the remainder, at the places lane group
 // tig = (j mod 8) / 2 of a k16 step reads them as A-fragment registers
-// (a0/a2: columns 2tig, 2tig+1 and 2tig+8, 2tig+9 of the step).
+// (a0/a2: columns 2tig, 2tig+1 and 2tig+8, 2tig+9 of the step).  Rows form
+// blocks of 8 (one MMA tile: rows gid = row mod 8); inside a block the words
+// are ordered [k16 step][gid][tig], so that the 32 lanes of a warp read one
+// step of a block as 512 contiguous bytes.
+DT_DEVINL size_t frag_word(int row, int kt, int tig, int nk16) {
+  return (((static_cast<size_t>(row >> 3) * nk16 + kt) * 8 + (row & 7)) * 4 + tig);
+}
 DT_DEVINL void store_frag(uint32_t* sf, int row, int j, int nk16, float v) {
   const int kt = j >> 4, w = j & 15;
   const int tig = (w & 7) >> 1, half = w & 1, pair = w >> 3;
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
   const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-  uint16_t* u = reinterpret_cast<uint16_t*>(sf + ((static_cast<size_t>(row) * nk16 + kt) * 4 + tig) * 4);
+  uint16_t* u = reinterpret_cast<uint16_t*>(sf + frag_word(row, kt, tig, nk16) * 4);
   u[2 * pair + half] = __bfloat16_as_ushort(hi);
   u[2 * (2 + pair) + half] = __bfloat16_as_ushort(lo);
 }
@@ -145,6 +151,19 @@ DT_DEVINL void warp_sort64_keys_desc(uint64_t& ka, uint64_t& kb) {
 // rows in shared memory: g rounded up to whole k16 steps, plus 8 elements so
 // that consecutive rows start 4 banks apart (conflict-free fragment loads).
 DT_HOST_DEVICE_INLINE int kstride(int g) { return (g + 15) / 16 * 16 + 8; }
+
+// One contiguous global -> shared copy by the bulk-copy engine, completing on
+// the mbarrier (16-byte aligned addresses, a multiple of 16 bytes).
+DT_DEVINL void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Orders this thread's generic-proxy view of global memory with its later
+// bulk copies (async proxy).
+DT_DEVINL void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 }  // namespace cl
 }  // namespace dt
