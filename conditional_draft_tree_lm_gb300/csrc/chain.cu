@@ -68,6 +68,9 @@ struct Shape {
   // several requests (8-state blocks): phase A copies the states as
   // ready-made fragments block by block into shared memory
   bool mfrag;
+  // one request, many branches, SIMT phase B: branches scored by different
+  // CTAs; no GRU-input slices are staged (phase C reads the table)
+  bool bdist;
 };
 
 DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
@@ -82,12 +85,18 @@ DT_HOST_DEVICE_INLINE bool mfrag_ok(const ChainParams& p) {
          p.g <= 16 * kWarps * kFragMax;
 }
 
+// One request with more than 8 live branches on the SIMT phase B: the
+// branches are scored by different CTAs (see the kernel).
+DT_HOST_DEVICE_INLINE bool bdist_ok(const ChainParams& p) {
+  return !p.marginal && p.n_req == 1 && p.mma_b == 0 && p.W > kPC && p.W * p.K >= p.M && p.K <= 32;
+}
+
 DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
   const bool fr = !p.marginal && frag_ok(p.n_req, p.W, p.g);
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
                prefetch_tokens(p.D, p.M), p.dbuf != 0, fr,
                fr && p.mma_b != 0 && p.dbuf != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax,
-               mfrag_ok(p)};
+               mfrag_ok(p), bdist_ok(p)};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -97,7 +106,8 @@ struct DimsRuntime {
 // The Qwen3-4B shape (g=1024, r=256, M=64, K=W=8, one request, depth 15, 128
 // CTAs): dimensions are literals, so the compiler folds the index arithmetic.
 struct DimsQ4B {
-  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true, true, false};
+  static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true, true, false,
+                                false};
   static DT_DEVINL Shape get(const ChainParams&) { return kShape; }
 };
 
@@ -161,7 +171,7 @@ DT_HOST_DEVICE_INLINE int pow2_at_least(int n) {
 DT_HOST_DEVICE_INLINE size_t stage_one(const Shape& sh, int which) {
   switch (which) {
     case 0: return sh.stage_w2 ? static_cast<size_t>(sh.M) * (sh.r + 8) * 2 : 0;
-    case 1: return static_cast<size_t>(sh.M) * 3 * sh.jper * 4;
+    case 1: return sh.bdist ? 0 : static_cast<size_t>(sh.M) * 3 * sh.jper * 4;
     case 2: return static_cast<size_t>(sh.M) * 4;
     case 3: return static_cast<size_t>(sh.r) * 4;
     default: return 16;
@@ -417,6 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   // grid barrier.  One request: every CTA selects for it (identically) and
   // updates its own columns right away.
   const bool dist = n_req > 1;
+  // One request with many live branches and the SIMT phase B: CTA c scores
+  // branches c, c + G, ... and writes their children into the node arrays;
+  // after a grid barrier every CTA reads all children back for the top-W.
+  const bool bdist = sh.bdist;
   const int qfirst = dist ? static_cast<int>(blockIdx.x) : 0;
   const int qstep = dist ? static_cast<int>(gridDim.x) : 1;
   // stage the first depth's first request of this CTA (overlaps the root
@@ -428,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     select_row_tokens(p, sh, s, qfirst, p.depth_first);
     __syncthreads();
     stage_row(p, sh, buf(p.depth_first), s.ctk,
-              static_cast<size_t>(qfirst) * D + (p.depth_first - 1), j0, nj, !dist && p.depth_first != D);
+              static_cast<size_t>(qfirst) * D + (p.depth_first - 1), j0, nj, !dist && !bdist && p.depth_first != D);
   }
 
   unsigned epoch = 0;
@@ -760,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         __syncthreads();
         select_row_tokens(p, sh, s, q, i);
         __syncthreads();
-        stage_row(p, sh, buf(i), s.ctk, qrow, j0, nj, !dist && !last);
+        stage_row(p, sh, buf(i), s.ctk, qrow, j0, nj, !dist && !bdist && !last);
       }
       {
         const Stage cur = buf(i);
@@ -1002,6 +1016,85 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           }
           __syncwarp();
         }
+      } else if (bdist) {
+        float* zv = s.z;           // [r] z of the branch
+        float* lamv = s.clogp;     // [M] lambda, then logp
+        uint64_t* keys = s.wkey;   // [M]
+        int* win = s.crank;        // [K]
+        for (int b = blockIdx.x; b < Lp; b += gridDim.x) {
+          const float* u = p.uW1 + static_cast<size_t>(b) * r;
+          for (int k = tid; k < r; k += kThreads) zv[k] = siluf_(s.h1s[k] + __ldcg(u + k));
+          __syncthreads();
+          // one candidate per thread: its W2 row from L2, z from shared memory
+          float lmax_t = -INFINITY;
+          for (int c = tid; c < M; c += kThreads) {
+            const uint4* w2r = reinterpret_cast<const uint4*>(p.w2 + static_cast<size_t>(s.ctk[c]) * r);
+            float acc = 0.0f;
+#pragma unroll 8
+            for (int k8 = 0; k8 < r / 8; ++k8) {
+              const float4 za = *reinterpret_cast<const float4*>(zv + k8 * 8);
+              const float4 zb = *reinterpret_cast<const float4*>(zv + k8 * 8 + 4);
+              fma8(acc, za, zb, __ldg(w2r + k8));
+            }
+            const float lam = (s.cbs[c] + acc) / p.T;
+            lamv[c] = lam;
+            lmax_t = fmaxf(lmax_t, lam);
+          }
+          lmax_t = warp_max(lmax_t);
+          if (lane == 0) s_tred[warp] = lmax_t;
+          __syncthreads();
+          float lmax = rest;
+          for (int w8 = 0; w8 < kWarps; ++w8) lmax = fmaxf(lmax, s_tred[w8]);
+          float se_t = 0.0f;
+          for (int c = tid; c < M; c += kThreads) se_t += expf(lamv[c] - lmax);
+          se_t = warp_sum(se_t);
+          if (lane == 0) s_tred[32 + warp] = se_t;
+          __syncthreads();
+          float se = expf(rest - lmax);
+          for (int w8 = 0; w8 < kWarps; ++w8) se += s_tred[32 + w8];
+          const float logZ = lmax + logf(se);
+          for (int c = tid; c < M; c += kThreads) {
+            const float lp = lamv[c] - logZ;
+            lamv[c] = lp;
+            keys[c] = rank_key(lp, static_cast<uint32_t>(s.ctk[c]));
+          }
+          __syncthreads();
+          // the K best (ties to the lower token id), then in token order
+          block_rank_all(keys, M, [&](int e, uint64_t, int rk) {
+            if (rk < K) win[rk] = e;
+          });
+          __syncthreads();
+          if (warp == 0) {
+            int c = lane < K ? win[lane] : 0;
+            if (c < 0 || c >= M) {
+              dt_report(p.status, DT_DEV_BOUNDS);
+              c = 0;
+            }
+            const int tok = lane < K ? s.ctk[c] : 0x7FFFFFFF;
+            int trank = 0;
+            for (int m = 0; m < K; ++m) trank += __shfl_sync(0xFFFFFFFFu, tok, m) < tok ? 1 : 0;
+            if (lane < K) {
+              const float lp = lamv[c];
+              const size_t nidx = static_cast<size_t>(row_off) + b * K + trank;
+              p.node_tok[nidx] = tok;
+              p.node_parent[nidx] = s.pnode[b];
+              p.node_logp[nidx] = lp;
+              p.node_score[nidx] = s.pscore[b] + lp;
+            }
+          }
+          __syncthreads();  // z, lambda, keys are free for the next branch
+        }
+        if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
+          drain();
+          return;
+        }
+        // every child of the depth, from the node arrays
+        for (int e = tid; e < nchild; e += kThreads) {
+          const size_t nidx = static_cast<size_t>(row_off) + e;
+          s.ctok[e] = __ldcg(p.node_tok + nidx);
+          s.clogp[e] = __ldcg(p.node_logp + nidx);
+          s.cscore[e] = __ldcg(p.node_score + nidx);
+        }
       } else {
         float* zw = s.z + warp * r;
         for (int b = warp; b < Lp; b += kWarps) {
@@ -1116,8 +1209,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
       __syncthreads();
-      // node arrays of this depth (CTA 0, or the request's CTA)
-      if (dist || blockIdx.x == 0) {
+      // node arrays of this depth (CTA 0, or the request's CTA; written by
+      // the branches' CTAs when those are spread)
+      if (!bdist && (dist || blockIdx.x == 0)) {
         const size_t nb = static_cast<size_t>(q) * p.N1 + row_off;
         for (int e = tid; e < nchild; e += kThreads) {
           p.node_tok[nb + e] = s.ctok[e];
@@ -1212,15 +1306,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           const int jv = idx / nj, jj = idx - jv * nj;
           const int e = s.surv[q * W + jv];
           const int b = e / K;
-          const float* x = s.xs + static_cast<size_t>(s.cslot[e]) * 3 * sh.jper;
+          // the GRU-input slice: staged per candidate, or (branches spread)
+          // read from the table by token
+          const int xst = bdist ? g : nj;
+          const float* x = bdist ? p.xtab + static_cast<size_t>(s.ctok[e]) * 3 * g + j0
+                                 : s.xs + static_cast<size_t>(s.cslot[e]) * 3 * sh.jper;
           const float* uu = s.uu + static_cast<size_t>(q * Lp + b) * 3 * sh.jper;
           const float h = Sprev[static_cast<size_t>(q * W + b) * g + j0 + jj];
           const float rg = sigmoidf_(x[jj] + uu[jj]);
-          const float zg = sigmoidf_(x[nj + jj] + uu[nj + jj]);
-          const float ng = tanhf_(x[2 * nj + jj] + rg * uu[2 * nj + jj]);
+          const float zg = sigmoidf_(x[xst + jj] + uu[nj + jj]);
+          const float ng = tanhf_(x[2 * xst + jj] + rg * uu[2 * nj + jj]);
           const float hn = (1.0f - zg) * ng + zg * h;
           Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = hn;
-          if (sh.frag)
+          if (sh.frag || sh.mfrag)
             store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
         }
       } else if ((dist || blockIdx.x == 0) && p.live_out) {
@@ -1257,8 +1355,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         if (sh.mfrag)
           store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
       }
-      if (sh.mfrag) fence_proxy_async_global();  // the next depth bulk-copies these fragments
     }
+    if (sh.mfrag && !last) fence_proxy_async_global();  // the next depth bulk-copies these fragments
     if (i < p.depth_last) {
       if (!sh.dbuf && qfirst < n_req) {
         // stage the next depth's first request of this CTA now: the copies
@@ -1266,7 +1364,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         __syncthreads();
         select_row_tokens(p, sh, s, qfirst, i + 1);
         if (!(qfirst == 0 && sh.prefetch)) __syncthreads();
-        stage_row(p, sh, buf(i + 1), s.ctk, static_cast<size_t>(qfirst) * D + i, j0, nj, !dist && i + 1 != D);
+        stage_row(p, sh, buf(i + 1), s.ctk, static_cast<size_t>(qfirst) * D + i, j0, nj,
+                  !dist && !bdist && i + 1 != D);
       }
       if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
         drain();
