@@ -64,6 +64,7 @@ struct TopmParams {
   int* status;
   unsigned* clear_word;  // or null: a word the kernel sets to zero (the next chain's barrier counter)
   int pdl;               // 1: launched as a programmatic dependent of the previous kernel
+  int occ2;              // 1: the two-CTAs-per-SM build (grids of several waves)
 };
 void topm_plan(TopmParams& p, int num_sms);
 size_t topm_partial_smem(const TopmParams& p);

@@ -101,7 +101,10 @@ DT_DEVINL void rank_all(const uint64_t* keys, int c, Fn fn) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_topm(const TopmParams p) {
+// kMinBlocks = 2 caps the registers so that two CTAs share an SM: for grids of
+// many waves (many rows), where each CTA's chain of phases is latency-bound.
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams p) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ uint32_t hist[kWarps * 256];
   __shared__ uint32_t state[4];
@@ -435,6 +438,7 @@ void topm_plan(TopmParams& p, int num_sms) {
   S = min(S, max(1, kMaxMerge / p.M));
   p.S = S;
   p.chunk = (p.V + S - 1) / S;
+  p.occ2 = S * p.rows > num_sms ? 1 : 0;  // more than one wave at one CTA per SM
 }
 
 size_t topm_partial_smem(const TopmParams&) {
@@ -443,7 +447,11 @@ size_t topm_partial_smem(const TopmParams&) {
 
 size_t topm_merge_smem(const TopmParams& p) { return topm_partial_smem(p); }
 
-cudaError_t topm_prepare() { return dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm)); }
+cudaError_t topm_prepare() {
+  cudaError_t e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm<1>));
+  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm<2>));
+  return e;
+}
 
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {
   if (p.chunk > kMaxChunk || p.S * p.M > kMaxMerge || p.M > kCandCap) return cudaErrorInvalidValue;
@@ -457,7 +465,7 @@ cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_topm, p);
+  return p.occ2 ? cudaLaunchKernelEx(&cfg, k_topm<2>, p) : cudaLaunchKernelEx(&cfg, k_topm<1>, p);
 }
 
 }  // namespace dt
