@@ -26,22 +26,38 @@ def main():
     ap.add_argument("--rounds", type=int, default=200)
     ap.add_argument("--first-seed", type=int, default=0)
     ap.add_argument("--relevance", type=int, default=30, help="rounds whose near-ties are re-run for relevance")
+    ap.add_argument("--T", type=float, default=None, help="override the workload's temperature")
+    ap.add_argument("--beta", type=float, default=None, help="override the workload's depth penalty")
     ap.add_argument("--out", default=None)
     args = ap.parse_args()
 
     import torch
     from conditional_draft_tree_lm_gb300 import DraftTreeBuilder
+    from oracle.besttree import best_first_tie_report, build_best_first
     from oracle.dartree import Oracle, base_logits, near_tie_report
     from tests.parity import TIE_TOL, to_np, tree_matches, upload_round, upload_weights
     from workloads import get_config, make_round_inputs, make_weights
 
     torch.cuda.set_device(0)
-    cfg = get_config(args.workload)
+    over = {k: v for k, v in (("T", args.T), ("beta", args.beta)) if v is not None}
+    cfg = get_config(args.workload, **over)
+    best_first = getattr(cfg, "builder", "dartree") == "best_first"
+
+    def oracle_tree(Hq, rq, ell, rec=None):
+        if best_first:
+            return build_best_first(orc, Hq, rq, ell=ell, rec=rec, tol=TIE_TOL if rec is not None else None)
+        return orc.build_request(Hq, rq, ell=ell, rec=rec, tol=TIE_TOL if rec is not None else None)
+
+    def relevant_tie(Hq, rq, ell):
+        rep_ = (best_first_tie_report if best_first else near_tie_report)(orc, Hq, rq, tol=TIE_TOL, ell=ell)
+        return rep_["relevant"]
+
     w = make_weights(cfg)
     b = DraftTreeBuilder(cfg, upload_weights(w))
     orc = Oracle(w, cfg)
-    res = dict(workload=cfg.name, rounds=0, requests=0, match=0, excused=0, unexcused=0, literal_tie=0,
-               relevance_sample=0, relevant_tie=0, max_score_err_matching=0.0, unexcused_details=[])
+    res = dict(workload=cfg.name, T=cfg.T, beta=cfg.beta, rounds=0, requests=0, match=0, excused=0,
+               unexcused=0, literal_tie=0, relevance_sample=0, relevant_tie=0, max_score_err_matching=0.0,
+               unexcused_details=[])
     t0 = time.time()
     try:
         for s in range(args.first_seed, args.first_seed + args.rounds):
@@ -52,14 +68,14 @@ def main():
                 res["requests"] += 1
                 ell = base_logits(H[q][1:], w["lm_head"])
                 rec = []
-                t = orc.build_request(H[q], int(root[q]), ell=ell, rec=rec, tol=TIE_TOL)
+                t = oracle_tree(H[q], int(root[q]), ell, rec=rec)
                 literal = bool(rec)
                 res["literal_tie"] += int(literal)
                 ok, why = tree_matches(out, q, t)
                 sampled = res["relevance_sample"] < args.relevance
                 relevant = None
                 if (not ok or sampled) and literal:
-                    relevant = near_tie_report(orc, H[q], int(root[q]), tol=TIE_TOL, ell=ell)["relevant"]
+                    relevant = relevant_tie(H[q], int(root[q]), ell)
                 if sampled:
                     res["relevance_sample"] += 1
                     res["relevant_tie"] += int(bool(relevant))
