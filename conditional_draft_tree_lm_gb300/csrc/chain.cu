@@ -27,6 +27,19 @@
 //        r = sigmoid(x_r + u_r), z = sigmoid(x_z + u_z), n = tanh(x_n + r u_n),
 //        h' = (1 - z) n + z h, with x = X[token] = E[token] W_ih^T + b_ih.
 //   --   grid barrier
+// Routes through the same kernel (fixed per launch by the shape):
+//   one request, <= 8 live branches   phase A reads the states as ready-made
+//        mma.sync A fragments from global memory (hi/lo parts in rows 0-7 /
+//        8-15 of the tile: one MMA per k16 step), z is published the same way,
+//        the next depth's candidate data is staged a depth ahead;
+//   several requests                  phase A copies 8-state fragment blocks
+//        whole into shared memory (one bulk copy each, two ahead); CTA c
+//        selects for requests c, c + G, ... only, and after one more grid
+//        barrier every CTA updates its columns of all requests' survivors;
+//   one request, > 8 branches, SIMT phase B   CTA c scores branches c, c + G,
+//        ... and writes their children into the node arrays; after one more
+//        grid barrier every CTA reads them back for the top-W;
+//   marginal scoring                  one CTA, no state, no correction.
 // The kernel is instantiated twice over the same code: with every dimension
 // fixed at compile time for the Qwen3-4B shape (index arithmetic folds to
 // constants, loops unroll), and with dimensions read from the parameters.
