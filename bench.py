@@ -50,7 +50,8 @@ def _config_dict(cfg, n_inputs):
 
 
 def algorithmic_bytes(cfg):
-    """HBM bytes one round must move (roofline)."""
+    """HBM bytes one launch of the LM-head GEMM and one whole round must move
+    (weights read once, gathered rows, hidden states; the roofline numerators)."""
     D = cfg.block - 1
     lm = cfg.V * cfg.d * 2
     w1h = cfg.r * cfg.d * 2

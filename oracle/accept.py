@@ -34,7 +34,7 @@ import numpy as np
 
 
 @dataclass
-class Verdict:
+class WalkResult:
     target_tok: np.ndarray  # [S] int64: y_a per slot
     accepted: list           # accepted slots in path order (root excluded)
     bonus: int               # the target's token at the last accepted slot
@@ -47,7 +47,7 @@ def target_argmax(Z: np.ndarray) -> np.ndarray:
     return np.argmax(np.asarray(Z), axis=1).astype(np.int64)
 
 
-def accept_walk(tok, parent, Z) -> Verdict:
+def accept_walk(tok, parent, Z) -> WalkResult:
     """Greedy verification of one tree.  tok, parent: [S] with parent[0] = -1
     and parent[c] < c; Z: [S, V] target logits per slot."""
     tok = np.asarray(tok, dtype=np.int64)
@@ -67,7 +67,7 @@ def accept_walk(tok, parent, Z) -> Verdict:
             raise ValueError("siblings share a token")
         a = nxt[0]
         accepted.append(a)
-    return Verdict(target_tok=y, accepted=accepted, bonus=int(y[a]), tau=len(accepted) + 1)
+    return WalkResult(target_tok=y, accepted=accepted, bonus=int(y[a]), tau=len(accepted) + 1)
 
 
 def accept_walk_rounds(tok, parent, Z):

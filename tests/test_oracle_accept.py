@@ -184,14 +184,14 @@ def _planted(name):
                     break
                 a = nxt[0]
                 acc.append(a)
-            return oa.Verdict(y, acc, int(y[a]), len(acc) + 1)
+            return oa.WalkResult(y, acc, int(y[a]), len(acc) + 1)
         return {"accept_walk": w}
     if name == "one_step_only":
         def w(tok, parent, Z):
             v = real_walk(tok, parent, Z)
             acc = v.accepted[:1]
             last = acc[-1] if acc else 0
-            return oa.Verdict(v.target_tok, acc, int(v.target_tok[last]), len(acc) + 1)
+            return oa.WalkResult(v.target_tok, acc, int(v.target_tok[last]), len(acc) + 1)
         return {"accept_walk": w}
     if name == "bonus_from_root":
         def w(tok, parent, Z):
