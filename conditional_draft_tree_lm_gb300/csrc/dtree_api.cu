@@ -445,7 +445,9 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->acc.D = c->t.D;
   accept_plan(c->acc, c->num_sms);
   layout(*cfg, c->t, c->topm, c->lay);
-  e = cudaMalloc(&c->ws, c->lay.total);
+  // host-side fault injection: DT_FAULT_INJECT_ALLOC set in the environment
+  // makes the workspace allocation fail as an out-of-memory would
+  e = getenv("DT_FAULT_INJECT_ALLOC") ? cudaErrorMemoryAllocation : cudaMalloc(&c->ws, c->lay.total);
   if (e == cudaSuccess) e = cudaMalloc(&c->xtab, c->lay.xtab);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->ws, 0, c->lay.total, st);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
@@ -723,6 +725,18 @@ dt_status dt_build_round_host(dt_ctx* c, const void* H_host, const int32_t* root
   DT_TRY(cudaMemcpyAsync(logp_cum_host, logp, k.n_req * S1 * 4, cudaMemcpyDeviceToHost, st));
   DT_TRY(cudaMemcpyAsync(mask_host, mask, k.n_req * S1 * S1, cudaMemcpyDeviceToHost, st));
   DT_TRY(cudaStreamSynchronize(st));
+  return DT_OK;
+}
+
+dt_status dt_check_bounded_waits(dt_ctx* c, int which, void* stream) {
+  if (!c || (which != 0 && which != 1)) return DT_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* bar = c->at<unsigned>(c->lay.bar);
+  DT_TRY(cudaMemsetAsync(bar, 0, sizeof(unsigned), st));
+  DT_TRY(launch_wait_check(bar, c->at<int>(c->lay.status), which, st));
+  // leave the barrier counter as the next launch expects it
+  DT_TRY(cudaMemsetAsync(bar, 0, sizeof(unsigned), st));
+  c->last_stream = st;
   return DT_OK;
 }
 

@@ -215,4 +215,7 @@ void accept_plan(AcceptParams& p, int num_sms);
 size_t accept_smem_bytes(const AcceptParams& p);
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- bounded-wait self-check
+cudaError_t launch_wait_check(unsigned* bar, int* status, int which, cudaStream_t stream);
+
 }  // namespace dt

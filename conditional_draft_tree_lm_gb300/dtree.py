@@ -72,6 +72,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dt_build_round": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_build_round_host": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_get_device_status": (c_int, [vp]),
+        "dt_check_bounded_waits": (c_int, [vp, c_int, vp]),
         "dt_round_kernel_count": (c_int, [vp]),
         "dt_topm_noalloc": (c_int, [vp, c_int, c_int, c_int, c_float, vp, vp, vp, vp]),
     }
@@ -317,6 +318,12 @@ class DraftTreeBuilder:
             hp(out_host["mask"], torch.uint8, cfg.n_req * s1 * s1, "mask"), _stream(stream)),
             "dt_build_round_host")
         return out_host
+
+    def check_bounded_waits(self, which: int, stream=None):
+        """Launch the bounded-wait self-check (0: grid barrier with a missing
+        participant, 1: an mbarrier nothing arrives on); read the outcome with
+        device_status()."""
+        _check(self.lib.dt_check_bounded_waits(self.ctx, int(which), _stream(stream)), "dt_check_bounded_waits")
 
     def device_status(self) -> int:
         return int(self.lib.dt_get_device_status(self.ctx))

@@ -299,6 +299,18 @@ dt_status dt_topm_noalloc(const float* logits, int rows, int V, int M, float T, 
  * word: DT_OK, DT_ERR_TIMEOUT or DT_ERR_DEVICE. */
 dt_status dt_get_device_status(dt_ctx* ctx);
 
+/* Self-check of the bounded device-side waits, on the context's status word:
+ * which = 0 launches a grid barrier of two CTAs that one CTA never reaches,
+ * which = 1 a wait on an mbarrier phase that nothing completes.  The waiting
+ * thread gives up after the wait limit (2 s), records the timeout and returns;
+ * dt_get_device_status then returns DT_ERR_TIMEOUT and the context stays
+ * usable.  Returns DT_ERR_INVALID_ARG for another `which`.
+ *
+ * Host-side fault injection: with DT_FAULT_INJECT_ALLOC set in the
+ * environment, dt_create fails its workspace allocation as an out-of-memory
+ * would (DT_ERR_OOM, nothing leaked). */
+dt_status dt_check_bounded_waits(dt_ctx* ctx, int which, void* stream);
+
 /* Number of kernel launches one dt_build_round replay performs. */
 int dt_round_kernel_count(const dt_ctx* ctx);
 
