@@ -116,10 +116,14 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   L.xtab = static_cast<size_t>(c.V) * 3 * c.g * 4;
 }
 
+// Tile width of the LM-head GEMM over the H rows (the swap-AB N dimension):
+// up to 256 rows in one tile; more rows in several 256-wide tiles, which keeps
+// four pipeline stages and double-buffered accumulators (the two tiles of a
+// vocabulary block run on neighbouring CTAs, so its weights come from HBM once).
 int logits_bn(const dt_config& c) {
   const int n = c.n_req * c.block;
   int bn = (n + 15) / 16 * 16;
-  if (bn > 256) bn = 512;
+  if (bn > 256) bn = 256;
   return bn;
 }
 
@@ -186,7 +190,7 @@ dt_status enqueue_base_logits(dt_ctx* c, const void* H, float* logits, cudaStrea
   p.K = k.d;
   p.m_tiles_a = (k.V + 127) / 128;
   p.m_tiles_a2 = (k.r + 127) / 128;
-  p.n_tiles = 1;
+  p.n_tiles = (k.n_req * k.block + BN - 1) / BN;
   p.n_valid = k.n_req * k.block;
   p.a_evict_first = 1;
   p.rows_a = k.V;

@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // fully unrolled with predicated stores: v stays in registers
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int n = c0 + j;
+            const int n = nt * p.BN + c0 + j;  // the H row (request q, block position i)
             const int q = n / p.block, i = n - q * p.block;
             if (n < p.n_valid && i > 0 && valid)
               dst[static_cast<size_t>(q * p.D + i - 1) * nrows + row] = __uint_as_float(v[j]);
