@@ -15,6 +15,10 @@
  *     Lemma 1): all live branches of a depth are corrected in one batch, the W
  *     best children live on, and one global Top-B over score + beta*depth
  *     (beta <= 0) picks the tree handed to tree-attention verification.
+ *   Also: the greedy acceptance walk through an emitted tree given the target
+ *   model's logits (dt_accept_walk); marginal scoring, the correction left out
+ *   (DT_FLAG_MARGINAL); and the node-by-node conditional best-first builder
+ *   that depth batching replaces (DT_FLAG_BEST_FIRST).
  *
  * Conventions of every entry point:
  *   - All device pointers are plain CUDA device addresses owned by the caller
