@@ -20,9 +20,11 @@
 //   B    every CTA (identically): z = SiLU(h1_i + u_W1); lambda_c = (base_c +
 //        z . W2[c]) / T on the Top-M candidates (one tensor-core product over
 //        all branches); logp = lambda - logsumexp(rest, lambda); per-branch
-//        top-K (ties to the lower token id) by rank counting; children sorted
-//        by token id; top-W of the depth by cumulative score (ties to the
-//        lower node index).  CTA 0 writes the node arrays and the live list.
+//        top-K (ties to the lower token id: a register sort of packed keys for
+//        M = 64, else K rounds of a warp argmax); children sorted by token id;
+//        top-W of the depth by cumulative score (ties to the lower node index:
+//        ranks counted by one warp or by the block, or a sorting network for
+//        many children).  CTA 0 writes the node arrays and the live list.
 //   C    GRU update of the survivors' state columns J:
 //        r = sigmoid(x_r + u_r), z = sigmoid(x_z + u_z), n = tanh(x_n + r u_n),
 //        h' = (1 - z) n + z h, with x = X[token] = E[token] W_ih^T + b_ih.
