@@ -190,6 +190,50 @@ def time_accept_walk(builder, cfg, trees, stream, peak, n_launch=200):
             "inputs": "target logits N(0,1) per slot, the draft followed at 80 % of slots (synthetic)"}
 
 
+def time_two_streams(builder, cfg, wd, Hs, roots, n_rounds):
+    """Throughput mode: independent rounds alternate between two contexts on two
+    streams, so that one round's kernels may overlap the other's; timed with
+    CUDA events from a common start to the end of both streams."""
+    import torch
+    from conditional_draft_tree_lm_gb300 import DraftTreeBuilder
+    b2 = DraftTreeBuilder(cfg, wd)
+    try:
+        streams = (torch.cuda.Stream(), torch.cuda.Stream())
+        builders = (builder, b2)
+        outs = [[b.new_tree() for _ in range(len(Hs))] for b in builders]
+        for k in range(2 * len(Hs)):  # capture every pointer set of both contexts first
+            j = k % len(Hs)
+            builders[k % 2].build_round(Hs[j], roots[j], outs[k % 2][j], stream=streams[k % 2])
+        torch.cuda.synchronize()
+        main = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_wall = time.perf_counter()
+        e0.record(main)
+        for st in streams:
+            st.wait_stream(main)
+        for k in range(n_rounds):
+            j = k % len(Hs)
+            builders[k % 2].build_round(Hs[j], roots[j], outs[k % 2][j], stream=streams[k % 2])
+            if k == 7:
+                # a first chunk far slower than a round means the contexts do not
+                # share the GPU well: stop there rather than time the rest
+                torch.cuda.synchronize()
+                if time.perf_counter() - t_wall > 0.5:
+                    n_rounds = 8
+                    break
+        for st in streams:
+            main.wait_stream(st)
+        e1.record(main)
+        torch.cuda.synchronize()
+        status = b2.device_status()
+    finally:
+        b2.close()
+    us = e0.elapsed_time(e1) * 1e3 / n_rounds
+    return {"value": 1e6 / us, "unit": "builds/s", "us_per_round": us, "streams": 2, "contexts": 2,
+            "rounds": n_rounds, "device_status": status,
+            "note": "independent rounds alternating over two contexts and streams; latency mode is the headline"}
+
+
 def replica_seeds(rank, n_inputs):
     """Round seeds of one replica: every rank builds trees of its own inputs."""
     return [rank * 100000 + s for s in range(n_inputs)]
@@ -348,6 +392,8 @@ def bench_gpu(args):
     lm_ms = e0.elapsed_time(e1) / nk
     peak, peak_kind = _peaks()
     walk = time_accept_walk(builder, cfg, outs, stream, peak) if not args.no_walk else None
+    thr = time_two_streams(builder, cfg, wd, Hs, roots, max(10, min(args.steps, 200))) \
+        if args.throughput else None
     clk = clocks.stop()
     # end to end through the public API with host buffers (pinned)
     Hh = [torch.from_numpy(np.ascontiguousarray(make_round_inputs(cfg, s)[0]).view(np.int16))
@@ -408,6 +454,7 @@ def bench_gpu(args):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": builder.round_kernel_count() * args.steps,
         "accept_walk": walk,
+        "throughput_mode": thr,
         "clocks": clk,
         "device_status": status,
     }
@@ -455,6 +502,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-walk", action="store_true", help="skip the acceptance-walk measurement")
+    ap.add_argument("--throughput", action="store_true",
+                    help="also measure throughput mode (two contexts on two streams)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
