@@ -40,6 +40,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
+from . import dartree as _dartree
 from .dartree import (Oracle, _select, compact_tree, correction, corrected_logprobs, gru_input,
                       gru_step, widen)
 
@@ -141,9 +142,7 @@ def best_first_tie_report(orc: Oracle, H_req, root_tok, tol=1e-3, B=None, beta=N
         except (ValueError, KeyError):
             relevant.append(t)
             continue
-        same = (alt.tok.shape == base.tok.shape and np.array_equal(alt.tok, base.tok)
-                and np.array_equal(alt.parent, base.parent) and np.array_equal(alt.depth, base.depth))
-        if not same:
+        if not _dartree._same_tree(alt, base):
             relevant.append(t)
-    return dict(literal=bool(rec), relevant=bool(relevant), n_ties=len(rec), relevant_ties=relevant,
+    return dict(literal=bool(rec), relevant=bool(relevant), n_ties=len(rec), ties=rec, relevant_ties=relevant,
                 tree=base)

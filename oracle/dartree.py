@@ -115,7 +115,10 @@ def top_m(ell: np.ndarray, M: int, T: float, swap=None):
     ids = order[:M].copy()
     if swap is not None:
         a, b = swap
-        ids[np.where(ids == a)[0][0]] = b
+        at = np.where(ids == a)[0]
+        if at.size != 1 or np.any(ids == b):
+            raise ValueError("the flip does not apply to this candidate set")
+        ids[at[0]] = b
         ids = ids[np.lexsort((ids, -ell[ids]))]
     mask = np.ones(V, dtype=bool)
     mask[ids] = False
@@ -198,6 +201,8 @@ def _select(keys: np.ndarray, ids: np.ndarray, n: int, tol, rec, tag, swap=None)
     if swap is not None:
         pos = {int(ids[j]): j for j in range(ids.shape[0])}
         a, b = swap
+        if a not in pos or b not in pos or pos[a] not in sel or pos[b] in sel:
+            raise ValueError("the flip does not apply to this selection")
         sel[sel.index(pos[a])] = pos[b]
     return np.array(sel, dtype=np.int64)
 
@@ -428,10 +433,13 @@ def near_tie_report(oracle: Oracle, H_req, root_tok, tol=1e-3, beta=None, T=None
         except ValueError:
             relevant.append(t)
             continue
-        same = (alt.tok.shape == base.tok.shape and np.array_equal(alt.tok, base.tok)
-                and np.array_equal(alt.parent, base.parent)
-                and np.array_equal(alt.depth, base.depth))
-        if not same:
+        if not _same_tree(alt, base):
             relevant.append(t)
     return dict(literal=bool(rec), relevant=bool(relevant), n_ties=len(rec),
-                relevant_ties=relevant, tree=base)
+                ties=rec, relevant_ties=relevant, tree=base)
+
+
+def _same_tree(a, b) -> bool:
+    """The emitted trees agree: same tokens, parent slots and depths."""
+    return (a.tok.shape == b.tok.shape and np.array_equal(a.tok, b.tok)
+            and np.array_equal(a.parent, b.parent) and np.array_equal(a.depth, b.depth))
