@@ -66,19 +66,49 @@ def _config_dict(cfg, n_inputs):
 
 def algorithmic_bytes(cfg):
     """HBM bytes one launch of the LM-head GEMM and one whole round must move
-    (weights read once, gathered rows, hidden states; the roofline numerators)."""
+    (weights read once, gathered rows, hidden states; the roofline numerators).
+    The logits are not counted: the method needs only their Top-M."""
     D = cfg.block - 1
     lm = cfg.V * cfg.d * 2
     w1h = cfg.r * cfg.d * 2
     h = cfg.n_req * cfg.block * cfg.d * 2
-    logits_out = cfg.n_req * D * cfg.V * 4 + cfg.n_req * D * cfg.r * 4
-    kernel = lm + w1h + h + logits_out
+    kernel = lm + w1h + h
+    round_bytes = kernel + chain_bytes(cfg)
+    return kernel, round_bytes
+
+
+def _live_counts(cfg):
+    """Live branches entering each depth: L_0 = 1, L_i = min(W, L_{i-1} K)."""
+    L, out = 1, []
+    for _ in range(cfg.block - 1):
+        out.append(L)
+        L = min(cfg.W, L * cfg.K)
+    return out
+
+
+def chain_bytes(cfg):
+    """HBM bytes of the depth chain: the GRU hidden weights and the S-half of
+    W1 once, the W2 rows of every depth's candidates, the GRU-input rows of
+    the root and of every surviving child (fp32 table rows of 3g)."""
+    D = cfg.block - 1
     w_hh = 3 * cfg.g * cfg.g * 2
     w1s = cfg.r * cfg.g * 2
     w2 = cfg.n_req * D * cfg.M * cfg.r * 2
-    xrows = cfg.n_req * (1 + (D - 1) * cfg.W) * 3 * cfg.g * 4
-    round_bytes = lm + w1h + h + w_hh + w1s + w2 + xrows
-    return kernel, round_bytes
+    xrows = cfg.n_req * (1 + sum(min(cfg.W, L * cfg.K) for L in _live_counts(cfg)[:-1])) * 3 * cfg.g * 4
+    return w_hh + w1s + w2 + xrows
+
+
+def chain_flops(cfg):
+    """Multiply-add work of the depth chain (2 FLOP each): per live branch the
+    projection of its state through [W_hh | W1_S] and its correction over the
+    M candidates."""
+    per = sum(2 * L * (cfg.g * (3 * cfg.g + cfg.r) + cfg.r * cfg.M) for L in _live_counts(cfg))
+    return cfg.n_req * per
+
+
+def topm_bytes(cfg):
+    """HBM bytes of Top-M over materialised logits: every logit read once."""
+    return cfg.n_req * (cfg.block - 1) * cfg.V * 4
 
 
 class ClockSampler:
@@ -234,6 +264,72 @@ def time_two_streams(builder, cfg, wd, Hs, roots, n_rounds):
             "note": "independent rounds alternating over two contexts and streams; latency mode is the headline"}
 
 
+def time_stages(builder, cfg, H, root, stream, n=50):
+    """Each kernel of the round timed alone: the LM-head GEMM (dt_base_logits),
+    Top-M (dt_topm) and the expansion with its Top-B/tree tail
+    (dt_expand_prune), each captured in a CUDA graph of one call and replayed
+    n times between CUDA events on the launching stream."""
+    import torch
+    out = builder.new_tree()
+    side = torch.cuda.Stream()
+    calls = {
+        "lm_head": lambda st: builder.base_logits(H, stream=st),
+        "topm": lambda st: builder.topm(stream=st),
+        "chain": lambda st: builder.expand_prune(root, out, stream=st),
+    }
+    res = {}
+    for name, fn in calls.items():
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            fn(side)  # warm (and leaves the workspace in the state the next stage reads)
+            with torch.cuda.graph(g, stream=side):
+                fn(side)
+        stream.wait_stream(side)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) * 1e3 / n
+    return res
+
+
+def kernel_rooflines(cfg, us, peak, peak_kind, tpeak, tpeak_kind):
+    """One roofline entry per kernel of the round (bytes or FLOPs per launch
+    over its CUDA-event time), largest time first."""
+    kb, _ = algorithmic_bytes(cfg)
+    ents = []
+    gf = gemm_flops(cfg)
+    t = us["lm_head"] * 1e-6
+    hbm, ten = kb / t / 1e9, gf / t / 1e12
+    ents.append({"kernel": "k_gemm_tc (LM head + W1_H, tcgen05/TMA)", "us_per_launch": us["lm_head"],
+                 "bound": "hbm" if hbm / peak >= ten / tpeak else "tensor",
+                 "algorithmic_bytes_per_launch": kb, "hbm_gbs": hbm, "hbm_frac": hbm / peak,
+                 "algorithmic_flops_per_launch": gf, "tflops": ten, "tensor_frac": ten / tpeak})
+    tb = topm_bytes(cfg)
+    t = us["topm"] * 1e-6
+    ents.append({"kernel": "k_topm (Top-M + rest log-partition over the logits)", "us_per_launch": us["topm"],
+                 "bound": "hbm", "algorithmic_bytes_per_launch": tb, "hbm_gbs": tb / t / 1e9,
+                 "hbm_frac": tb / t / 1e9 / peak})
+    cb, cf = chain_bytes(cfg), chain_flops(cfg)
+    t = us["chain"] * 1e-6
+    ents.append({"kernel": "depth chain (all depths + Top-B + tree/mask)", "us_per_launch": us["chain"],
+                 "bound": "hbm", "algorithmic_bytes_per_launch": cb, "hbm_gbs": cb / t / 1e9,
+                 "hbm_frac": cb / t / 1e9 / peak, "algorithmic_flops_per_launch": cf,
+                 "tflops": cf / t / 1e12, "tensor_frac": cf / t / 1e12 / tpeak,
+                 "note": "latency-bound: a sequence of dependent depths, each a few MFLOP"})
+    for e in ents:
+        e["peak_hbm_gbs"] = peak
+        e["peak_source"] = f"{peak_kind} hbm_gbs; {tpeak_kind} bf16_tflops"
+    ents.sort(key=lambda e: -e["us_per_launch"])
+    return ents
+
+
 def replica_seeds(rank, n_inputs):
     """Round seeds of one replica: every rank builds trees of its own inputs."""
     return [rank * 100000 + s for s in range(n_inputs)]
@@ -336,7 +432,11 @@ def bench_gpu(args):
     cfg = get_config(args.workload)
     w = make_weights(cfg)
     wd = {k: bf16_tensor(v) for k, v in w.items()}
+    torch.cuda.synchronize()
+    t_create = time.perf_counter()
     builder = DraftTreeBuilder(cfg, wd)
+    torch.cuda.synchronize()
+    create_ms = (time.perf_counter() - t_create) * 1e3
     n_inputs = args.inputs
     seeds = replica_seeds(rank, n_inputs)
     Hs, roots = [], []
@@ -378,18 +478,9 @@ def bench_gpu(args):
         b.record(stream)
         b.synchronize()
         lat.append(a.elapsed_time(b) * 1e3)
-    # dominant kernel (LM head GEMM) timed alone with events on its stream
-    logits = torch.empty(cfg.n_req, cfg.block - 1, cfg.V, dtype=torch.float32, device="cuda")
-    for k in range(3):
-        builder.base_logits(Hs[k % n_inputs], logits)
-    nk = max(10, min(args.steps, 100))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(nk):
-        builder.base_logits(Hs[k % n_inputs], logits)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    lm_ms = e0.elapsed_time(e1) / nk
+    # every kernel of the round timed alone (graph replays, events on the stream)
+    stage_us = time_stages(builder, cfg, Hs[0], roots[0], stream, n=max(20, min(args.steps, 100)))
+    lm_ms = stage_us["lm_head"] / 1e3
     peak, peak_kind = _peaks()
     walk = time_accept_walk(builder, cfg, outs, stream, peak) if not args.no_walk else None
     thr = time_two_streams(builder, cfg, wd, Hs, roots, max(10, min(args.steps, 200))) \
@@ -419,6 +510,7 @@ def bench_gpu(args):
     achieved = kbytes / (lm_ms / 1e3) / 1e9
     tpeak, tpeak_kind = _tensor_peak()
     tflops = gemm_flops(cfg) / (lm_ms / 1e3) / 1e12
+    kernels = kernel_rooflines(cfg, stage_us, peak, peak_kind, tpeak, tpeak_kind)
     traffic = None
     prof = os.path.join(ROOT, "profiles", f"lm_head_gemm_{cfg.name}_traffic.json")
     if os.path.exists(prof):
@@ -430,16 +522,31 @@ def bench_gpu(args):
         except Exception:
             traffic = None
     us_round = 1e6 * elapsed / args.steps
+    top = kernels[0]
+    if top["kernel"].startswith("k_gemm_tc"):
+        roofline = None  # filled below (the GEMM's own object, with its ncu traffic)
+    else:
+        roofline = {"bound": "hbm", "kernel": top["kernel"], "achieved": top["hbm_gbs"], "peak": peak,
+                    "unit": "GB/s", "frac": top["hbm_frac"], "peak_source": f"{peak_kind} hbm_gbs",
+                    "traffic": None, "algorithmic_bytes_per_launch": top["algorithmic_bytes_per_launch"],
+                    "avg_launch_us": top["us_per_launch"], "tensor_frac": top.get("tensor_frac"),
+                    "note": top.get("note")}
     line = {
         "metric": METRIC, "value": value, "unit": "builds/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "us_per_round": us_round,
-        "us_per_round_p10_p50_p90": [float(np.percentile(lat, q)) for q in (10, 50, 90)],
+        "us_per_round_note": "mean of back-to-back graph replays (pipelined rounds); the 60 % HBM "
+                             "target is judged on it; isolated_round_us_* are single synchronised rounds",
+        "isolated_round_us_p10_p50_p90": [float(np.percentile(lat, q)) for q in (10, 50, 90)],
+        "isolated_round_hbm_frac_p50": rbytes / (float(np.percentile(lat, 50)) * 1e-6) / 1e9 / peak,
         "round_hbm_gbs": rbytes / (us_round * 1e-6) / 1e9,
         "round_hbm_frac": rbytes / (us_round * 1e-6) / 1e9 / peak,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1/fan_in) weights, N(0,1) hidden states)",
         "config": _config_dict(cfg, n_inputs),
-        "roofline": ({"bound": "hbm", "kernel": "k_gemm_tc (LM head + W1_H, tcgen05/TMA)",
+        "kernels": kernels,
+        "create": {"ms": create_ms, "gru_input_table_bytes": cfg.V * 3 * cfg.g * 4,
+                   "note": "dt_create: workspace + GRU input table X = E W_ih^T + b_ih (one tcgen05 GEMM)"},
+        "roofline": roofline if roofline is not None else ({"bound": "hbm", "kernel": "k_gemm_tc (LM head + W1_H, tcgen05/TMA)",
                       "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                       "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
                       "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": lm_ms * 1e3,

@@ -285,17 +285,16 @@ PruneParams prune_params(dt_ctx* c, const float* nscore, int32_t* sel) {
   return p;
 }
 
-dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* tok, int32_t* parent,
-                        int32_t* depth, float* logp_cum, uint8_t* mask, cudaStream_t st) {
-  float* logits = c->at<float>(c->lay.logits);
-  dt_status s = enqueue_base_logits(c, H, logits, st);
-  if (s != DT_OK) return s;
-  // Top-M and the chain launch as programmatic dependents (each waits for its
-  // predecessor's end before reading its results); Top-M also clears the
-  // chain's barrier counter, so the round needs no memset
+// Steps 3-5 of a round from the workspace's Top-M results: the depth-batched
+// expansion (or the best-first builder) with the global Top-B and the
+// tree/mask.  chained: launched right after Top-M in the same round, as
+// programmatic dependents, with the barrier counter already cleared by Top-M;
+// otherwise the counter is cleared here and the launches are ordinary.
+dt_status enqueue_build(dt_ctx* c, const int32_t* root, int32_t* tok, int32_t* parent, int32_t* depth,
+                        float* logp_cum, uint8_t* mask, cudaStream_t st, bool chained) {
   unsigned* bar = c->at<unsigned>(c->lay.bar);
-  s = enqueue_topm(c, logits, st, bar, 1);
-  if (s != DT_OK) return s;
+  if (!chained) DT_TRY(cudaMemsetAsync(bar, 0, sizeof(unsigned), st));
+  const int pdl = chained ? 1 : 0;
   int32_t* sel = c->at<int32_t>(c->lay.sel);
   if (c->best_first) {
     BestParams bp = c->best;
@@ -312,7 +311,7 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
     bp.zrow = c->at<float>(c->lay.uW1);
     bp.bar = bar;
     bp.status = c->at<int>(c->lay.status);
-    bp.pdl = 1;
+    bp.pdl = pdl;
     bp.sel = sel;
     bp.pops = nullptr;
     bp.tok = tok;
@@ -330,7 +329,7 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
   ChainParams cp = chain_params(c, root, ntok, npar, nlogp, nscore, nullptr);
   cp.depth_first = 1;
   cp.depth_last = c->t.D;
-  cp.pdl = 1;
+  cp.pdl = pdl;
   if (chain_can_fuse_tree(cp)) {
     // single request: the chain kernel's CTA 0 also prunes and emits the tree
     cp.fuse_tree = 1;
@@ -344,7 +343,7 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
     cp.mask = mask;
     return enqueue_chain(c, cp, st, true);
   }
-  s = enqueue_chain(c, cp, st, true);
+  dt_status s = enqueue_chain(c, cp, st, true);
   if (s != DT_OK) return s;
   PruneParams pp = prune_params(c, nscore, sel);
   DT_TRY(launch_prune(pp, st));
@@ -357,6 +356,19 @@ dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* 
   pp.mask = mask;
   DT_TRY(launch_tree_mask(pp, st));
   return DT_OK;
+}
+
+dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* tok, int32_t* parent,
+                        int32_t* depth, float* logp_cum, uint8_t* mask, cudaStream_t st) {
+  float* logits = c->at<float>(c->lay.logits);
+  dt_status s = enqueue_base_logits(c, H, logits, st);
+  if (s != DT_OK) return s;
+  // Top-M and the chain launch as programmatic dependents (each waits for its
+  // predecessor's end before reading its results); Top-M also clears the
+  // chain's barrier counter, so the round needs no memset
+  s = enqueue_topm(c, logits, st, c->at<unsigned>(c->lay.bar), 1);
+  if (s != DT_OK) return s;
+  return enqueue_build(c, root, tok, parent, depth, logp_cum, mask, st, true);
 }
 
 }  // namespace
@@ -442,6 +454,11 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->topm.M = cfg->M;
   c->topm.T = cfg->T;
   topm_plan(c->topm, c->num_sms);
+  if (const char* why = topm_unsupported(c->topm)) {
+    set_last_error(why);
+    delete c;
+    return DT_ERR_SHAPE;
+  }
   c->acc = AcceptParams{};
   c->acc.n_req = cfg->n_req;
   c->acc.S = cfg->B + 1;
@@ -635,6 +652,17 @@ dt_status dt_tree_mask(dt_ctx* c, const int32_t* sel, const int32_t* node_tok, c
   p.logp_cum = logp_cum;
   p.mask = mask;
   DT_TRY(launch_tree_mask(p, st));
+  c->last_stream = st;
+  return DT_OK;
+}
+
+dt_status dt_expand_prune(dt_ctx* c, const int32_t* root_tok, int32_t* tok, int32_t* parent, int32_t* depth,
+                          float* logp_cum, uint8_t* mask, void* stream) {
+  if (!c || !root_tok || !tok || !parent || !depth || !logp_cum || !mask) return DT_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  dt_status s = enqueue_build(c, root_tok, tok, parent, depth, logp_cum, mask, st, false);
+  if (s != DT_OK) return s;
+  c->next_depth = 1;
   c->last_stream = st;
   return DT_OK;
 }

@@ -70,6 +70,9 @@ void topm_plan(TopmParams& p, int num_sms);
 size_t topm_partial_smem(const TopmParams& p);
 size_t topm_merge_smem(const TopmParams& p);
 cudaError_t topm_prepare();
+// Why a planned Top-M launch cannot run (too many rows for the grid, a chunk
+// or a merge beyond the kernel's capacity), or null when it can.
+const char* topm_unsupported(const TopmParams& p);
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream);
 
 // Text returned by dt_last_error() on the calling thread.

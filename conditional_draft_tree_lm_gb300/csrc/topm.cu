@@ -453,8 +453,16 @@ cudaError_t topm_prepare() {
   return e;
 }
 
+const char* topm_unsupported(const TopmParams& p) {
+  if (p.rows < 1 || p.rows > 65535) return "rows must be 1..65535 (one grid row per logit row)";
+  if (p.M > kCandCap) return "M above 512";
+  if (p.chunk > kMaxChunk) return "V too large for M: a chunk would exceed 16384 logits (V <= 8192 * 16384 / M)";
+  if (p.S * p.M > kMaxMerge) return "chunks x M above the 8192 merged entries of a row";
+  return nullptr;
+}
+
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {
-  if (p.chunk > kMaxChunk || p.S * p.M > kMaxMerge || p.M > kCandCap) return cudaErrorInvalidValue;
+  if (topm_unsupported(p)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, p.rows);
   cfg.blockDim = dim3(kThreads);

@@ -92,6 +92,12 @@ extern "C" dt_status dt_topm_noalloc(const float* logits, int rows, int V, int M
   p.M = M;
   p.T = T;
   topm_plan(p, dev->num_sms);
+  if (const char* why = topm_unsupported(p)) {
+    char msg[200];
+    snprintf(msg, sizeof(msg), "dt_topm_noalloc: %d rows x %d logits with M=%d: %s", rows, V, M, why);
+    set_last_error(msg);
+    return DT_ERR_SHAPE;
+  }
   // carve the scratch: partial ids / values, per-chunk statistics, row counters
   const size_t rs = static_cast<size_t>(rows) * p.S;
   size_t off = 0;

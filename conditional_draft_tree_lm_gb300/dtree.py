@@ -68,6 +68,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dt_expand_depth": (c_int, [vp, c_int, i32p, vp, vp, vp, vp, vp, vp]),
         "dt_prune_topB": (c_int, [vp, vp, vp, vp]),
         "dt_tree_mask": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "dt_expand_prune": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_accept_walk": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_build_round": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dt_build_round_host": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
@@ -233,6 +234,22 @@ class DraftTreeBuilder:
                                      _ptr(logp_cum, torch.float32, cfg.n_req * s1, "logp_cum"),
                                      _ptr(mask, torch.uint8, cfg.n_req * s1 * s1, "mask"), _stream(stream)),
                "dt_tree_mask")
+
+    def expand_prune(self, root_tok, out=None, stream=None):
+        """Steps 3-5 (all depths, Top-B, tree/mask) from the last topm()'s
+        candidates, in one launch for a single request (``dt_expand_prune``)."""
+        import torch
+        cfg = self.cfg
+        out = out if out is not None else self.new_tree(root_tok.device)
+        s1 = cfg.B + 1
+        _check(self.lib.dt_expand_prune(self.ctx, _ptr(root_tok, torch.int32, cfg.n_req, "root_tok"),
+                                        _ptr(out["tok"], torch.int32, cfg.n_req * s1, "tok"),
+                                        _ptr(out["parent"], torch.int32, cfg.n_req * s1, "parent"),
+                                        _ptr(out["depth"], torch.int32, cfg.n_req * s1, "depth"),
+                                        _ptr(out["logp_cum"], torch.float32, cfg.n_req * s1, "logp_cum"),
+                                        _ptr(out["mask"], torch.uint8, cfg.n_req * s1 * s1, "mask"),
+                                        _stream(stream)), "dt_expand_prune")
+        return out
 
     def accept_walk(self, target_logits, tok, parent, accepted=None, accept_len=None, bonus=None,
                     target_tok=None, stream=None):

@@ -250,6 +250,16 @@ dt_status dt_accept_walk(dt_ctx* ctx, const float* target_logits, const int32_t*
                          const int32_t* parent, int32_t* target_tok, int32_t* accepted,
                          int32_t* accept_len, int32_t* bonus, void* stream);
 
+/* Steps 3-5 in as few launches as the shape allows (one for a single request):
+ * every depth of the expansion, the global Top-B and the tree/mask, from the
+ * Top-M results that the last dt_topm left in the workspace (or, with
+ * DT_FLAG_BEST_FIRST, the best-first builder).  Node arrays and the selection
+ * stay in the workspace.
+ *   root_tok: [n_req] int32; outputs as dt_tree_mask.
+ * A later dt_expand_depth starts a new round at depth 1. */
+dt_status dt_expand_prune(dt_ctx* ctx, const int32_t* root_tok, int32_t* tok, int32_t* parent, int32_t* depth,
+                          float* logp_cum, uint8_t* mask, void* stream);
+
 /* --------------------------------------------------------------------------
  * Whole round.
  * ------------------------------------------------------------------------ */
@@ -284,9 +294,14 @@ dt_status dt_build_round_host(dt_ctx* ctx, const void* H_host, const int32_t* ro
  *   rest_lse:  [rows] fp32 out, log sum over the non-candidates of exp(logit/T).
  * It allocates nothing: its scratch is one fixed 4 MiB array of device memory
  * inside the library, which every GPU that loads the library keeps until the
- * process exits.  Sizes whose scratch would exceed it (roughly rows * chunks *
- * (8 M + 16) bytes, chunks ~ 2 * SMs / rows, at least V / 16384) are rejected
- * with DT_ERR_SHAPE and a message in dt_last_error(); M <= 512.
+ * process exits.  A call needs about rows * S * (8 M + 16) + 4 rows bytes of
+ * it, where S, the chunks each row is split into, is
+ *   S = min(max(SMs / rows, ceil(V / 16384), 1), max(V / (2 M), 1),
+ *           max(8192 / M, 1))          (integer divisions, SMs = the device's)
+ * and each chunk must hold at most 16384 logits.  Calls beyond the array, with
+ * rows > 65535, M > 512, or a chunk above 16384 logits (V > 8192 * 16384 / M)
+ * are rejected with DT_ERR_SHAPE and a message in dt_last_error(), before any
+ * work is queued.
  * The first call on each device does a one-time set-up (it looks up the
  * array's device address and sets a kernel attribute), so make that first
  * call before any stream capture.  All calls on a device share that device's

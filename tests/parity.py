@@ -63,3 +63,16 @@ def check_round(orc, gpu: dict, H_bits, root, beta=None, T=None, ells=None):
         else:
             res.append(("MISMATCH", why))
     return res
+
+
+def report_counts(label: str, counts: dict, details=None) -> str:
+    """One line with a test's round verdicts (printed, and used in assertion
+    messages, so the number of bit-exact rounds shows in every run)."""
+    line = (f"{label}: {counts.get('match', 0)} bit-exact, {counts.get('excused', 0)} excused, "
+            f"{counts.get('MISMATCH', 0)} mismatched")
+    print(line, flush=True)
+    if details:
+        bad = [d for d in details if "match" not in d]
+        if bad:
+            line += f" {bad}"
+    return line

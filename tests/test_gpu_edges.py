@@ -19,7 +19,7 @@ scores within 2e-3; a mismatch only excused by an outcome-relevant near-tie):
 import numpy as np
 import pytest
 
-from tests.parity import TIE_TOL, check_round, to_np, tree_matches, upload_round, upload_weights
+from tests.parity import TIE_TOL, check_round, report_counts, to_np, tree_matches, upload_round, upload_weights
 from workloads import get_config, make_round_inputs, make_weights
 
 pytestmark = pytest.mark.gpu
@@ -60,8 +60,9 @@ def test_edge_rounds(case):
         status = b.device_status()
     finally:
         b.close()
-    assert counts["MISMATCH"] == 0, details
-    assert counts["match"] >= counts["excused"], details
+    line = report_counts(f"edge {case}", counts, details)
+    assert counts["MISMATCH"] == 0, line
+    assert counts["match"] >= counts["excused"], line
     assert status == 0
     if case == "chain_w1_k1":
         assert all(d[2] == "match" for d in details)

@@ -612,3 +612,28 @@ def test_planted_mistakes_are_caught(monkeypatch, name, fn):
             caught = True
             break
     assert caught, f"planted mistake {fn.__name__} in {name} passed every pin"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["qwen3_4b", "wide"])
+def test_lemma1_full_scale(name):
+    """Lemma 1 at the benchmarked sizes (DARTree page, Poda Diferida,
+    Equivalencia Teórica): over the oracle's own super-tree of seeds 0-2 at the
+    Qwen3-4B shape (904 nodes, B = 64) and the wide tree (27 680 nodes,
+    B = 512), the global Top-B equals the oracle's heap and an independent heap
+    for beta in {0, -0.25, -1}, and the selection is ancestor-closed."""
+    cfg = get_config(name)
+    w = make_weights(cfg)
+    orc = od.Oracle(w, cfg)
+    for s in range(3):
+        H, root = make_round_inputs(cfg, s)
+        t = orc.build_request(H[0], int(root[0]), beta=0.0)
+        assert t.node_tok.size == od.node_count(cfg.K, cfg.W, cfg.block - 1) + 1
+        for beta in (0.0, -0.25, -1.0):
+            key = t.node_score + beta * t.node_depth
+            sel = od.top_b(t.node_score, t.node_depth, cfg.B, beta)
+            heap = od.heap_best_first(t.node_parent, t.node_score, t.node_depth, cfg.B, beta)
+            assert sel.tolist() == heap.tolist(), (name, s, beta)
+            assert sel.tolist() == _independent_heap(t.node_parent, key, cfg.B), (name, s, beta)
+            chosen = set(sel.tolist()) | {0}
+            assert all(int(t.node_parent[v]) in chosen for v in sel), (name, s, beta)
