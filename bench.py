@@ -560,6 +560,7 @@ def bench_gpu(args):
         "e2e": {"value": e2e_value, "unit": "builds/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": builder.round_kernel_count() * args.steps,
+        "plan": builder.plan(),
         "accept_walk": walk,
         "throughput_mode": thr,
         "clocks": clk,

@@ -48,11 +48,14 @@ def needs_build() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not needs_build():
+def build_library(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str | None = None) -> str:
+    """Compile every csrc/*.cu and link libdtree.so (or, with lib_path, a
+    variant built with extra_flags, e.g. an instrumented copy, beside it)."""
+    out = lib_path or LIB_PATH
+    if lib_path is None and not force and not needs_build():
         return LIB_PATH
     nvcc = nvcc_path()
-    obj_dir = os.path.join(LIB_DIR, "obj")
+    obj_dir = os.path.join(LIB_DIR, "obj" if lib_path is None else "obj_" + os.path.basename(out).split(".")[0])
     os.makedirs(obj_dir, exist_ok=True)
 
     def compile_one(src):
@@ -68,13 +71,13 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
     srcs = _sources()
     with ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + ".tmp"
+    tmp = out + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

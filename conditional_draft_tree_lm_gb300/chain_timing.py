@@ -1,0 +1,125 @@
+"""Per-depth phase breakdown of the clustered depth chain (a profiling tool).
+
+Builds an instrumented copy of libdtree (``-DDT_DCHAIN_TIMING``: thread 0 of
+CTA 0 and of the last CTA record ``clock64()`` at every phase boundary of every
+depth) beside the normal library, replays whole rounds of a workload through
+it, and prints the mean cycles of each phase: X (waiting for and gathering the
+previous depth's states), A1 (W1_S projection and z), A2 (partial
+correction), A3 (W_hh projection), R (the cluster reduction of the
+correction), B (corrected log-probs, top-K, node arrays), C (top-W, GRU update,
+publication), and the kernel's prologue and tail.  The normal library is not
+touched; the instrumented one is only loaded by this process.
+
+    python -m conditional_draft_tree_lm_gb300.chain_timing [--workload qwen3_4b] [--rounds 20]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import os
+import sys
+
+import numpy as np
+
+# phase k runs from stamp k to stamp k+1 of the same depth (the last one to
+# the next depth's stamp 0); the last depth ends at stamp LAST_END
+PHASES = ["X", "A1", "A2", "A3", "R", "B.lse", "B.sort", "B.nodes", "topW", "C", "next"]
+SLOTS = 66          # kMaxDepth + 2
+NPH = 20
+LAST_END = 8
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="qwen3_4b")
+    ap.add_argument("--rounds", type=int, default=20)
+    ap.add_argument("--mhz", type=float, default=0.0, help="SM clock for the microsecond column "
+                                                           "(default 2070, the GB300's maximum)")
+    ap.add_argument("--save", default="", help="also save the raw stamps (numpy .npy) here")
+    args = ap.parse_args()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import torch
+
+    from . import dtree
+    from .build import LIB_DIR, build_library
+    from workloads import get_config, make_round_inputs, make_weights
+
+    path = build_library(force=True, extra_flags=["-DDT_DCHAIN_TIMING"],
+                         lib_path=os.path.join(LIB_DIR, "libdtree_timing.so"))
+    dtree._lib = None
+    lib = dtree.load_library(path)
+    dtree._lib = lib  # the builder below runs on the instrumented copy
+    lib.dt_dchain_stamps.restype = ctypes.c_int
+    lib.dt_dchain_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+
+    torch.cuda.set_device(0)
+    cfg = get_config(args.workload)
+    w = make_weights(cfg)
+    wd = {k: dtree.bf16_tensor(v) for k, v in w.items()}
+    b = dtree.DraftTreeBuilder(cfg, wd)
+    print("plan:", b.plan())
+    if "clustered" not in b.plan():
+        raise SystemExit("the workload does not run the clustered depth chain")
+    D = cfg.block - 1
+    buf = np.zeros(2 * SLOTS * NPH, dtype=np.uint64)
+    acc = []
+    for s in range(args.rounds + 3):
+        H, r = make_round_inputs(cfg, s)
+        Hd = dtree.bf16_tensor(H)
+        rd = torch.from_numpy(r.astype(np.int32)).cuda()
+        b.build_round(Hd, rd)
+        torch.cuda.synchronize()
+        n = lib.dt_dchain_stamps(buf.ctypes.data, buf.size)
+        if n != buf.size:
+            raise SystemExit("dt_dchain_stamps failed")
+        if s >= 3:
+            acc.append(buf.reshape(2, SLOTS, NPH).astype(np.int64).copy())
+    st = np.stack(acc)  # [rounds, cta, slot, phase]
+    if args.save:
+        np.save(args.save, st)
+    mhz = args.mhz or 2070.0
+    us = 1.0 / mhz
+    print(f"{len(acc)} rounds of {cfg.name}; cycles (us at {mhz:.0f} MHz), mean over rounds")
+    for c, name in ((0, "CTA 0"), (1, "last CTA")):
+        k = st[:, c]
+        pro = (k[:, 0, 4] - k[:, 0, 0]).mean()
+        gw = (k[:, 0, 5] - k[:, 0, 4]).mean()
+        first = (k[:, 1, 0] - k[:, 0, 5]).mean()
+        loop = (k[:, 0, 1] - k[:, 1, 0]).mean()
+        print(f"\n{name}: prologue {pro:.0f} ({pro * us:.2f}), wait for the previous kernel {gw:.0f} "
+              f"({gw * us:.2f}), to depth 1 {first:.0f} ({first * us:.2f}), depth loop {loop:.0f} "
+              f"({loop * us:.2f})" + (f", tail {(k[:, 0, 2] - k[:, 0, 1]).mean() * us:.2f} us" if c == 0 else ""))
+        print("depth " + " ".join(f"{p:>7s}" for p in PHASES) + "    total(us)")
+        nph = len(PHASES)
+        tot = np.zeros(nph)
+        for i in range(1, D + 1):
+            row = []
+            for ph in range(nph):
+                if i == D and ph >= LAST_END:
+                    row.append(0.0)  # the last depth ends after its node arrays
+                    continue
+                if i == D and ph == LAST_END - 1:
+                    nxt = k[:, 0, 1]
+                elif ph + 1 < nph:
+                    nxt = k[:, i, ph + 1]
+                else:
+                    nxt = k[:, i + 1, 0]
+                row.append((nxt - k[:, i, ph]).mean())
+            tot += np.array(row)
+            end = k[:, i + 1, 0] if i < D else k[:, 0, 1]
+            print(f"{i:5d} " + " ".join(f"{v:7.0f}" for v in row) + f"  {(end - k[:, i, 0]).mean() * us:8.2f}")
+        print("mean  " + " ".join(f"{v / D:7.0f}" for v in tot) + "  (cycles per depth)")
+        print("us    " + " ".join(f"{v / D * us:7.2f}" for v in tot))
+        # finer split of three phases (depths 2..D-1), from the extra stamps
+        mid = slice(2, D)
+        sub = lambda a, b: (k[:, mid, b] - k[:, mid, a]).mean()
+        print(f"  A1: loads + MMAs {sub(1, 11):.0f}, partial sums {sub(11, 12):.0f}, barrier {sub(12, 13):.0f}, "
+              f"z {sub(13, 2):.0f};  B.lse: operands {sub(5, 15):.0f}, max/sum/log {sub(15, 6):.0f};  "
+              f"topW: keys + ranks {sub(8, 14):.0f}, ballots + barrier {sub(14, 9):.0f};  "
+              f"X: staging {sub(0, 16):.0f}, poll {sub(16, 17):.0f}, barrier + copies {sub(17, 1):.0f}")
+    b.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -66,7 +66,7 @@ struct Layout {
   size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, part_kth, cand_tok, cand_base, rest_lse,
       row_done, S, sfrag, zfrag,
       uW1, live, node_tok, node_parent, node_logp, node_score, sel, bar, status, H_dev, root_dev,
-      out_tok, out_parent, out_depth, out_logp, out_mask, acc_key, acc_done, total;
+      out_tok, out_parent, out_depth, out_logp, out_mask, acc_key, acc_done, xch, xch_words, total;
   size_t xtab;
 };
 
@@ -103,6 +103,10 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   put(L.sel, static_cast<size_t>(c.n_req) * c.B * 4);
   put(L.bar, 256);
   put(L.status, 256);
+  // clustered chain: [2][g/8][8 rows][4] 16-byte tagged words, then its epoch
+  // and abort words
+  put(L.xch, 2ull * (c.g / 8) * 8 * 4 * 16);
+  put(L.xch_words, 256);
   put(L.H_dev, static_cast<size_t>(c.n_req) * c.block * c.d * 2);
   put(L.root_dev, static_cast<size_t>(c.n_req) * 4);
   put(L.out_tok, c.n_req * S1 * 4);
@@ -144,6 +148,10 @@ struct dt_ctx {
   BestParams best;
   int best_first = 0;
   int chain_grid = 0;
+  int use_dchain = 0;  // one request: the clustered depth chain (dchain.cu)
+  int dchain_cs = 0;
+  int dchain_jc = 0;
+  char plan[256] = "";  // which kernels a round runs (dt_plan_string)
   const float* logits_src = nullptr;
   int next_depth = 1;
   cudaStream_t cap_stream = nullptr;
@@ -263,6 +271,50 @@ ChainParams chain_params(dt_ctx* c, const int32_t* root, int32_t* ntok, int32_t*
   return p;
 }
 
+DchainParams dchain_params(dt_ctx* c, const int32_t* root, int32_t* ntok, int32_t* npar, float* nlogp,
+                           float* nscore, int32_t* live_out) {
+  const dt_config& k = c->cfg;
+  DchainParams p = {};
+  p.D = c->t.D;
+  p.g = k.g;
+  p.r = k.r;
+  p.M = k.M;
+  p.K = k.K;
+  p.W = k.W;
+  p.V = k.V;
+  p.d = k.d;
+  p.ldw1 = k.d + k.g;
+  p.N1 = c->t.N + 1;
+  p.T = k.T;
+  p.w_hh = static_cast<const uint16_t*>(c->w.w_hh);
+  p.w1 = static_cast<const uint16_t*>(c->w.w1);
+  p.w2 = static_cast<const uint16_t*>(c->w.w2);
+  p.xtab = c->xtab;
+  p.h1 = c->ws ? c->at<float>(c->lay.h1) : nullptr;
+  p.cand_tok = c->ws ? c->at<int>(c->lay.cand_tok) : nullptr;
+  p.cand_base = c->ws ? c->at<float>(c->lay.cand_base) : nullptr;
+  p.rest_lse = c->ws ? c->at<float>(c->lay.rest_lse) : nullptr;
+  p.root_tok = root;
+  p.S = c->ws ? c->at<float>(c->lay.S) : nullptr;
+  p.live = c->ws ? c->at<int>(c->lay.live) : nullptr;
+  p.xch = c->ws ? c->at<void>(c->lay.xch) : nullptr;
+  p.epoch = c->ws ? c->at<unsigned>(c->lay.xch_words) : nullptr;
+  p.abort_word = p.epoch ? p.epoch + 1 : nullptr;
+  p.node_tok = ntok;
+  p.node_parent = npar;
+  p.node_logp = nlogp;
+  p.node_score = nscore;
+  p.live_out = live_out;
+  p.status = c->ws ? c->at<int>(c->lay.status) : nullptr;
+  p.cs = c->dchain_cs;
+  p.jc = c->dchain_jc;
+  p.B = k.B;
+  p.beta = k.beta;
+  for (int i = 0; i <= kMaxDepth; ++i) p.L[i] = c->t.L[i];
+  for (int i = 0; i <= kMaxDepth + 1; ++i) p.off[i] = c->t.off[i];
+  return p;
+}
+
 // counter_cleared: the preceding Top-M kernel already zeroed the barrier
 // counter (the whole-round path), so no memset is enqueued.
 dt_status enqueue_chain(dt_ctx* c, const ChainParams& p, cudaStream_t st, bool counter_cleared = false) {
@@ -326,6 +378,22 @@ dt_status enqueue_build(dt_ctx* c, const int32_t* root, int32_t* tok, int32_t* p
   int32_t* npar = c->at<int32_t>(c->lay.node_parent);
   float* nlogp = c->at<float>(c->lay.node_logp);
   float* nscore = c->at<float>(c->lay.node_score);
+  if (c->use_dchain) {
+    // one request: all depths, the Top-B and the tree/mask in one clustered launch
+    DchainParams dp = dchain_params(c, root, ntok, npar, nlogp, nscore, nullptr);
+    dp.depth_first = 1;
+    dp.depth_last = c->t.D;
+    dp.pdl = pdl;
+    dp.fuse_tree = 1;
+    dp.sel = sel;
+    dp.tok = tok;
+    dp.parent = parent;
+    dp.depth = depth;
+    dp.logp_cum = logp_cum;
+    dp.mask = mask;
+    DT_TRY(launch_dchain(dp, st));
+    return DT_OK;
+  }
   ChainParams cp = chain_params(c, root, ntok, npar, nlogp, nscore, nullptr);
   cp.depth_first = 1;
   cp.depth_last = c->t.D;
@@ -444,6 +512,7 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   if (e == cudaSuccess) e = chain_prepare();
   if (e == cudaSuccess) e = prune_prepare();
   if (e == cudaSuccess) e = best_prepare();
+  if (e == cudaSuccess) e = dchain_prepare();
   if (e != cudaSuccess) {
     delete c;
     return cuda_status(e, "dt_create: kernel attributes");
@@ -529,6 +598,28 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
       return DT_ERR_SHAPE;
     }
   }
+  // one request with conditional scoring: the clustered depth chain when the
+  // shape fits it and every cluster can be resident at once
+  char why[160] = "";
+  if (cfg->n_req == 1 && !(cfg->flags & (DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST))) {
+    DchainParams dp = dchain_params(c, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+    dp.fuse_tree = 1;
+    if (dchain_plan(dp, c->num_sms, why, sizeof(why))) {
+      c->use_dchain = 1;
+      c->dchain_cs = dp.cs;
+      c->dchain_jc = dp.jc;
+    }
+    cudaGetLastError();  // an occupancy query that failed leaves no error behind
+  } else {
+    snprintf(why, sizeof(why), "%s", cfg->n_req != 1 ? "several requests" : "marginal or best-first mode");
+  }
+  if (c->best_first)
+    snprintf(c->plan, sizeof(c->plan), "best-first builder on %d CTAs", c->chain_grid);
+  else if (c->use_dchain)
+    snprintf(c->plan, sizeof(c->plan), "clustered depth chain on %d CTAs: %s", cfg->g / c->dchain_jc, why);
+  else
+    snprintf(c->plan, sizeof(c->plan), "grid-barrier depth chain on %d CTAs (clustered chain not used: %s)",
+             c->chain_grid, why);
 
   // tensor maps of the weights
   const dt_config& k = *cfg;
@@ -617,6 +708,15 @@ dt_status dt_expand_depth(dt_ctx* c, int depth, const int32_t* root_tok, int32_t
   if (depth == 1 && !root_tok) return DT_ERR_INVALID_ARG;
   if (depth != 1 && depth != c->next_depth) return DT_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->use_dchain) {
+    DchainParams p = dchain_params(c, root_tok, node_tok, node_parent, node_logp, node_score, live);
+    p.depth_first = depth;
+    p.depth_last = depth;
+    DT_TRY(launch_dchain(p, st));
+    c->next_depth = depth + 1;
+    c->last_stream = st;
+    return DT_OK;
+  }
   ChainParams p = chain_params(c, root_tok, node_tok, node_parent, node_logp, node_score, live);
   p.depth_first = depth;
   p.depth_last = depth;
@@ -787,9 +887,12 @@ dt_status dt_get_device_status(dt_ctx* c) {
 int dt_round_kernel_count(const dt_ctx* c) {
   if (!c) return -1;
   if (c->best_first) return 3;  // LM head GEMM, Top-M, best-first builder (tree and mask in its tail)
+  if (c->use_dchain) return 3;  // LM head GEMM, Top-M, clustered chain (Top-B and tree/mask in its tail)
   // LM head GEMM, Top-M, depth chain (+ Top-B, tree/mask unless the chain's tail does them)
   ChainParams cp = chain_params(const_cast<dt_ctx*>(c), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
   return chain_can_fuse_tree(cp) ? 3 : 5;
 }
 
 }  // extern "C"
+
+extern "C" const char* dt_plan_string(const dt_ctx* c) { return c ? c->plan : ""; }

@@ -139,6 +139,57 @@ bool chain_can_fuse_tree(const ChainParams& p);
 cudaError_t chain_prepare();
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream);
 
+// ---------------------------------------------------------------- clustered depth chain
+// One request, <= 8 live branches, M <= 64: the depth chain on thread-block
+// clusters with one tagged state exchange per depth (dchain.cu).
+struct DchainParams {
+  int D, g, r, M, K, W, V, ldw1, d;
+  int N1;  // nodes including the root
+  float T;
+  const uint16_t* w_hh;   // [3g, g]
+  const uint16_t* w1;     // [r, d+g]
+  const uint16_t* w2;     // [V, r]
+  const float* xtab;      // [V, 3g]
+  const float* h1;        // [D, r]
+  const int* cand_tok;    // [D, M]
+  const float* cand_base; // [D, M]
+  const float* rest_lse;  // [D]
+  const int* root_tok;    // [1]
+  float* S;               // [2][W][g] fp32 states handed from one launch to the next (depth parity)
+  int* live;              // [2][W] live node lists handed over the same way
+  void* xch;              // [2][g/8][8][4] 16-byte tagged words: the per-depth state exchange
+  unsigned* epoch;        // launch counter (part of every tag)
+  unsigned* abort_word;   // the epoch of a launch whose wait gave up
+  int* node_tok;
+  int* node_parent;
+  float* node_logp;
+  float* node_score;      // [N1]
+  int* live_out;          // [W] or null
+  int* status;
+  int depth_first, depth_last;
+  int pdl;
+  int cs;                 // cluster size (dchain_plan)
+  int jc;                 // state columns per CTA, 8 or 16 (dchain_plan)
+  int fuse_tree;          // CTA 0 runs the global Top-B and the tree/mask after depth D
+  int B;
+  float beta;
+  int* sel;
+  int* tok;
+  int* parent;
+  int* depth;
+  float* logp_cum;
+  uint8_t* mask;
+  int off[kMaxDepth + 2];
+  int L[kMaxDepth + 1];
+};
+// Picks the cluster size (16, 8, 4, 2 or 1) for the shape and checks that all
+// clusters fit on the device at once; false when the shape is not supported.
+// why (optional) receives the choice or the reason for none.
+bool dchain_plan(DchainParams& p, int num_sms, char* why = nullptr, size_t why_len = 0);
+size_t dchain_smem_bytes(const DchainParams& p);
+cudaError_t dchain_prepare();
+cudaError_t launch_dchain(const DchainParams& p, cudaStream_t stream);
+
 // ---------------------------------------------------------------- Top-B and tree
 struct PruneParams {
   int n_req, N1, B, D;

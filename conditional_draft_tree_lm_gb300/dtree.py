@@ -75,6 +75,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dt_get_device_status": (c_int, [vp]),
         "dt_check_bounded_waits": (c_int, [vp, c_int, vp]),
         "dt_round_kernel_count": (c_int, [vp]),
+        "dt_plan_string": (c_char_p, [vp]),
         "dt_topm_noalloc": (c_int, [vp, c_int, c_int, c_int, c_float, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -347,6 +348,10 @@ class DraftTreeBuilder:
 
     def round_kernel_count(self) -> int:
         return int(self.lib.dt_round_kernel_count(self.ctx))
+
+    def plan(self) -> str:
+        """Which kernels this context's rounds run (``dt_plan_string``)."""
+        return self.lib.dt_plan_string(self.ctx).decode(errors="replace")
 
 
 def topm_noalloc(logits, M, T, cand_tok, cand_base, rest_lse, stream=None):

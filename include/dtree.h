@@ -333,6 +333,12 @@ dt_status dt_check_bounded_waits(dt_ctx* ctx, int which, void* stream);
 /* Number of kernel launches one dt_build_round replay performs. */
 int dt_round_kernel_count(const dt_ctx* ctx);
 
+/* Which kernels the context's rounds run, chosen at dt_create from the shape
+ * and the device (for one request: the clustered depth chain, with its cluster
+ * size, or the grid-barrier chain and the reason).  Owned by the context;
+ * "" for NULL. */
+const char* dt_plan_string(const dt_ctx* ctx);
+
 #ifdef __cplusplus
 }
 #endif
