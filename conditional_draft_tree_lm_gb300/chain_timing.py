@@ -89,7 +89,10 @@ def main():
         loop = (k[:, 0, 1] - k[:, 1, 0]).mean()
         print(f"\n{name}: prologue {pro:.0f} ({pro * us:.2f}), wait for the previous kernel {gw:.0f} "
               f"({gw * us:.2f}), to depth 1 {first:.0f} ({first * us:.2f}), depth loop {loop:.0f} "
-              f"({loop * us:.2f})" + (f", tail {(k[:, 0, 2] - k[:, 0, 1]).mean() * us:.2f} us" if c == 0 else ""))
+              f"({loop * us:.2f})" + (f", tail {(k[:, 0, 2] - k[:, 0, 1]).mean() * us:.2f} us (last nodes "
+                                       f"{(k[:, 0, 6] - k[:, 0, 1]).mean() * us:.2f}, Top-B "
+                                       f"{(k[:, 0, 7] - k[:, 0, 6]).mean() * us:.2f}, tree/mask "
+                                       f"{(k[:, 0, 2] - k[:, 0, 7]).mean() * us:.2f})" if c == 0 else ""))
         print("depth " + " ".join(f"{p:>7s}" for p in PHASES) + "    total(us)")
         nph = len(PHASES)
         tot = np.zeros(nph)

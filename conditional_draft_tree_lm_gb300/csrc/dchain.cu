@@ -245,7 +245,7 @@ DT_HOST_DEVICE_INLINE Lay make_lay(int jc, int g, int r, int K, int D, int cs) {
   L.stage_sz = s;
   put(L.stage, kNS * s);
   put(L.tok, static_cast<size_t>(D) * kMP * 4);
-  put(L.child, static_cast<size_t>(kP) * K * 16);
+  put(L.child, static_cast<size_t>(2) * kP * K * 16);  // two depths' children
   put(L.misc, 256);
   L.total = o;
   return L;
@@ -320,13 +320,33 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
   float* uhh = reinterpret_cast<float*>(sm + L.uhh);
   float* sown = reinterpret_cast<float*>(sm + L.sown);  // [2][kP][JC], by depth parity
   int* tok_all = reinterpret_cast<int*>(sm + L.tok);
-  int* ctok = reinterpret_cast<int*>(sm + L.child);
-  int* cslot = ctok + kP * K;
-  float* clogp = reinterpret_cast<float*>(cslot + kP * K);
-  float* cscore = clogp + kP * K;
+  // children of a depth (token, candidate index, log-prob, score), by depth
+  // parity: CTA 0 writes a depth's node arrays once it has published the
+  // depth's states (every CTA waits for CTA 0's words, so work before that
+  // would delay the whole grid)
+  int* const child0 = reinterpret_cast<int*>(sm + L.child);
+  auto child_tok = [&](int par) { return child0 + par * 4 * kP * K; };
+  auto child_slot = [&](int par) { return child0 + par * 4 * kP * K + kP * K; };
+  auto child_logp = [&](int par) { return reinterpret_cast<float*>(child0 + par * 4 * kP * K + 2 * kP * K); };
+  auto child_score = [&](int par) { return reinterpret_cast<float*>(child0 + par * 4 * kP * K + 3 * kP * K); };
   int* surv = reinterpret_cast<int*>(sm + L.misc);           // [kP]
   int* pnode = surv + kP;                                     // [2][kP] live node indices, by depth parity
   float* pscore = reinterpret_cast<float*>(pnode + 2 * kP);  // [2][kP] their scores
+  // node arrays of depth dep from its children (CTA 0)
+  auto write_nodes = [&](int dep) {
+    const int par = dep & 1, nch = p.L[dep - 1] * K, off = p.off[dep];
+    const int* pt = child_tok(par);
+    const float* pl = child_logp(par);
+    const float* ps = child_score(par);
+    const int* pn = pnode + ((dep - 1) & 1) * kP;
+    for (int e = tid; e < nch; e += kT) {
+      const size_t nidx = static_cast<size_t>(off) + e;
+      p.node_tok[nidx] = pt[e];
+      p.node_parent[nidx] = pn[e / K];
+      p.node_logp[nidx] = pl[e];
+      p.node_score[nidx] = ps[e];
+    }
+  };
   auto stage = [&](int depth) -> Stage {
     uint8_t* b = sm + L.stage + static_cast<size_t>(depth % kNS) * L.stage_sz;
     return Stage{reinterpret_cast<uint16_t*>(b), reinterpret_cast<float*>(b + L.st_xs),
@@ -367,49 +387,10 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     }
   }
 
-  // everything below reads the previous kernels' results
-  DCH_STAMP(0, 4);
-  dt_grid_wait();
-  DCH_STAMP(0, 5);
-  const uint32_t E = ld_relaxed_u32(p.epoch) + 1u;
-
-  for (int idx = tid; idx < D * M; idx += kT) {
-    const int i = idx / M, c = idx - i * M;
-    int t = p.cand_tok[idx];
-    if (t < 0 || t >= p.V) {
-      dt_report(p.status, DT_DEV_BOUNDS);
-      t = 0;
-    }
-    tok_all[i * kMP + c] = t;
-  }
-  __syncthreads();
-
-  // stage the candidate data of one depth (one cp.async group, possibly empty)
-  auto stage_depth = [&](int i) {
-    if (i <= p.depth_last) {
-      const Stage b = stage(i);
-      const int* tk = tok_all + (i - 1) * kMP;
-      const int r8 = RQ / 8;
-      for (int idx = tid; idx < M * r8; idx += kT) {
-        const int c = idx / r8, k8 = idx - c * r8;
-        cp_async16(b.w2 + static_cast<size_t>(c) * RQP + 8 * k8, p.w2 + static_cast<size_t>(tk[c]) * r + r0 + 8 * k8);
-      }
-      constexpr int kQ4 = JC / 4;  // 16-byte pieces of one gate's owned columns
-      for (int idx = tid; idx < M * 3 * kQ4; idx += kT) {
-        const int c = idx / (3 * kQ4), rem = idx - c * 3 * kQ4, gate = rem / kQ4, h = rem - gate * kQ4;
-        cp_async16(b.xs + c * 3 * JC + gate * JC + 4 * h,
-                   p.xtab + static_cast<size_t>(tk[c]) * 3 * g + gate * g + j0 + 4 * h);
-      }
-      for (int c = tid; c < M; c += kT) cp_async4(b.cbs + c, p.cand_base + static_cast<size_t>(i - 1) * M + c);
-      for (int k4 = tid; k4 < RQ / 4; k4 += kT)
-        cp_async16(b.h1 + 4 * k4, p.h1 + static_cast<size_t>(i - 1) * r + r0 + 4 * k4);
-      if (tid == 0) cp_async4(b.rest, p.rest_lse + (i - 1));
-    }
-    cp_async_commit();
-  };
-  stage_depth(p.depth_first);
-
-  // ---- the states entering the launch's first depth, in every CTA ----
+  // ---- the states entering the launch's first depth, in every CTA (none of
+  // it is written by the kernels this launch may overlap: the root token and
+  // the GRU-input table are inputs; a previous launch of this kernel ended
+  // before this one started) ----
   const int f0 = p.depth_first;
   {
     const int pf = (f0 - 1) & 1;
@@ -477,6 +458,48 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     }
   }
 
+  // everything below reads the previous kernels' results
+  DCH_STAMP(0, 4);
+  dt_grid_wait();
+  DCH_STAMP(0, 5);
+  const uint32_t E = ld_relaxed_u32(p.epoch) + 1u;
+
+  for (int idx = tid; idx < D * M; idx += kT) {
+    const int i = idx / M, c = idx - i * M;
+    int t = p.cand_tok[idx];
+    if (t < 0 || t >= p.V) {
+      dt_report(p.status, DT_DEV_BOUNDS);
+      t = 0;
+    }
+    tok_all[i * kMP + c] = t;
+  }
+  __syncthreads();
+
+  // stage the candidate data of one depth (one cp.async group, possibly empty)
+  auto stage_depth = [&](int i) {
+    if (i <= p.depth_last) {
+      const Stage b = stage(i);
+      const int* tk = tok_all + (i - 1) * kMP;
+      const int r8 = RQ / 8;
+      for (int idx = tid; idx < M * r8; idx += kT) {
+        const int c = idx / r8, k8 = idx - c * r8;
+        cp_async16(b.w2 + static_cast<size_t>(c) * RQP + 8 * k8, p.w2 + static_cast<size_t>(tk[c]) * r + r0 + 8 * k8);
+      }
+      constexpr int kQ4 = JC / 4;  // 16-byte pieces of one gate's owned columns
+      for (int idx = tid; idx < M * 3 * kQ4; idx += kT) {
+        const int c = idx / (3 * kQ4), rem = idx - c * 3 * kQ4, gate = rem / kQ4, h = rem - gate * kQ4;
+        cp_async16(b.xs + c * 3 * JC + gate * JC + 4 * h,
+                   p.xtab + static_cast<size_t>(tk[c]) * 3 * g + gate * g + j0 + 4 * h);
+      }
+      for (int c = tid; c < M; c += kT) cp_async4(b.cbs + c, p.cand_base + static_cast<size_t>(i - 1) * M + c);
+      for (int k4 = tid; k4 < RQ / 4; k4 += kT)
+        cp_async16(b.h1 + 4 * k4, p.h1 + static_cast<size_t>(i - 1) * r + r0 + 4 * k4);
+      if (tid == 0) cp_async4(b.rest, p.rest_lse + (i - 1));
+    }
+    cp_async_commit();
+  };
+  stage_depth(p.depth_first);
+
   const int nkw = (L.nk16 - warp + kNW - 1) / kNW;  // k16 steps of this warp (kt = warp + kNW m)
   // lambda = (base + dL) / T as a product with 1/T (exact at T = 1; within an
   // ulp of the quotient otherwise)
@@ -493,14 +516,16 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     const int Li = p.L[i];      // branches that live on
     const int ip = (i - 1) & 1, in = i & 1;
     const bool last = i == D;
+    int* ctok = child_tok(in);
+    int* cslot = child_slot(in);
+    float* clogp = child_logp(in);
+    float* cscore = child_score(in);
 
     DCH_STAMP(i, 0);
-    // the next depth's candidate data, into the buffer depth i-1 used (once
-    // every thread is past depth i-1); the copies fly while this CTA waits for
-    // the states
+    // (the next depth's candidate data goes into the buffer depth i-1 used:
+    // every thread must be past depth i-1)
     if (i > f0) __syncthreads();
-    stage_depth(i + 1);
-    DCH_STAMP(i, 16);
+    bool staged = false;
     // ================= X: the previous depth's states from every CTA =========
     // the words are laid out as the fragments themselves: word w is uint2 w of
     // the A-fragment array (k16 step, row, lane group, half), so a word that
@@ -519,6 +544,10 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
             pending |= 1u << j;
           }
         }
+        // the next depth's candidate data, issued while the loads fly
+        stage_depth(i + 1);
+        staged = true;
+        DCH_STAMP(i, 16);
         uint64_t t0 = 0;
         uint32_t n = 0;
         const uint64_t tag2 = static_cast<uint64_t>(tag) << 32;
@@ -556,6 +585,7 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
       __syncthreads();
       aborted = s_abort != 0;
     }
+    if (!staged) stage_depth(i + 1);
     cp_async_wait_group1();  // this depth's staged data (issued a depth ago) has landed
     const Stage st = stage(i);
 
@@ -772,24 +802,45 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
       DCH_STAMP(i, 7);
     }
     __syncthreads();
-    if (cta == 0 && !aborted) {
-      for (int e = tid; e < nchild; e += kT) {
-        const size_t nidx = static_cast<size_t>(row_off) + e;
-        p.node_tok[nidx] = ctok[e];
-        p.node_parent[nidx] = pnode[ip * kP + e / K];
-        p.node_logp[nidx] = clogp[e];
-        p.node_score[nidx] = cscore[e];
-      }
-    }
     DCH_STAMP(i, 8);
     if (last) {
       if (cta == 0 && p.live_out)
         for (int j = tid; j < W; j += kT) p.live_out[j] = -1;
       break;
     }
-    // top-W of the depth by (score desc, node index asc), ranks counted by the
-    // whole block (4 threads per child up to 64 children); survivors ascending
-    {
+    // top-W of the depth by (score desc, node index asc); survivors ascending.
+    // Up to 64 children: warp 0 takes the Li best by rounds of two warp max
+    // reductions over (score key, inverted index); more: ranks counted by the
+    // block
+    if (nchild <= 64) {
+      if (warp == 0) {
+        const int e0 = 2 * lane, e1 = 2 * lane + 1;
+        uint32_t ha = e0 < nchild ? f32_key(cscore[e0]) : 0u, la = e0 < nchild ? 0xFFFFFFFFu - e0 : 0u;
+        uint32_t hb = e1 < nchild ? f32_key(cscore[e1]) : 0u, lb = e1 < nchild ? 0xFFFFFFFFu - e1 : 0u;
+        int mine = 0x7FFFFFFF;
+        for (int w = 0; w < Li; ++w) {
+          const uint32_t gh = __reduce_max_sync(0xFFFFFFFFu, ha > hb ? ha : hb);
+          const uint32_t mla = ha == gh ? la : 0u, mlb = hb == gh ? lb : 0u;
+          const uint32_t gl = __reduce_max_sync(0xFFFFFFFFu, mla > mlb ? mla : mlb);
+          if (ha == gh && la == gl) {
+            ha = 0u;
+            la = 0u;
+          } else if (hb == gh && lb == gl) {
+            hb = 0u;
+            lb = 0u;
+          }
+          if (lane == w) mine = static_cast<int>(0xFFFFFFFFu - gl);
+        }
+        DCH_STAMP(i, 14);
+        int pos = 0;
+#pragma unroll
+        for (int m = 0; m < kP; ++m) {
+          const int t2 = __shfl_sync(0xFFFFFFFFu, mine, m);
+          pos += (m < Li && t2 < mine) ? 1 : 0;
+        }
+        if (lane < Li) surv[pos] = mine;
+      }
+    } else {
       const int tp = nchild <= 64 ? 4 : 1;
       const int e = tid / tp, part4 = tid - e * tp;
       int rk = 0;
@@ -805,7 +856,6 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
         rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 1);
         rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 2);
       }
-      DCH_STAMP(i, 14);
       const bool alive = e < nchild && part4 == 0 && rk < Li;
       const unsigned bal = __ballot_sync(0xFFFFFFFFu, alive);
       if (lane == 0) s_wcnt[warp] = __popc(bal);
@@ -872,11 +922,14 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
         p.live_out[w] = -1;
       }
     }
+    if (cta == 0 && !aborted) write_nodes(i);
     DCH_STAMP(i, 10);
     // (the next depth's barriers order these shared-memory writes)
   }
 
   DCH_STAMP(0, 1);
+  // the node arrays of depth D (which ends after its selections)
+  if (cta == 0 && !aborted && p.depth_last == D) write_nodes(D);
   cp_async_wait_all();
   cluster_sync();  // no CTA leaves while a peer may read its shared memory
   // the next launch tags its words with a new epoch (also after an abort, so
@@ -898,8 +951,10 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     uint32_t* hist = tb_keys + a16(static_cast<size_t>(p.N1 - 1) * 4) / 4;
     for (int k = tid; k <= D + 1; k += kT) offs[k] = p.off[k];
     __syncthreads();
+    DCH_STAMP(0, 6);
     topb_select(p.node_score, p.N1, p.B, p.beta, D, offs, tb_keys, tb_cands, p.N1 - 1, hist, kNW * 256, s_state,
                 s_tred, s_tscan, p.sel);
+    DCH_STAMP(0, 7);
     tree_and_mask(p.sel, p.N1, p.B, D, offs, p.node_tok, p.node_parent, p.node_score, nullptr, nodes, par, dep, anc,
                   p.tok, p.parent, p.depth, p.logp_cum, p.mask, p.status);
   }
