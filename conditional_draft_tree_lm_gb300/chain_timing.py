@@ -6,9 +6,12 @@ depth) beside the normal library, replays whole rounds of a workload through
 it, and prints the mean cycles of each phase: X (waiting for and gathering the
 previous depth's states), A1 (W1_S projection and z), A2 (partial
 correction), A3 (W_hh projection), R (the cluster reduction of the
-correction), B (corrected log-probs, top-K, node arrays), C (top-W, GRU update,
-publication), and the kernel's prologue and tail.  The normal library is not
-touched; the instrumented one is only loaded by this process.
+correction), B (corrected log-probs and top-K: B.sel; the children: B.out; the
+block barrier: B.bar), top-W, C (GRU update, publication), and the kernel's prologue and tail.  Every CTA also records the
+global timer when it has published a depth's states and when it holds all of
+them, which shows the spread of the publications and the exchange latency.
+The normal library is not touched; the instrumented one is only loaded by this
+process.
 
     python -m conditional_draft_tree_lm_gb300.chain_timing [--workload qwen3_4b] [--rounds 20]
 """
@@ -23,9 +26,10 @@ import numpy as np
 
 # phase k runs from stamp k to stamp k+1 of the same depth (the last one to
 # the next depth's stamp 0); the last depth ends at stamp LAST_END
-PHASES = ["X", "A1", "A2", "A3", "R", "B.lse", "B.sort", "B.nodes", "topW", "C", "next"]
+PHASES = ["X", "A1", "A2", "A3", "R", "B.sel", "B.out", "B.bar", "topW", "C", "next"]
 SLOTS = 66          # kMaxDepth + 2
 NPH = 20
+XCTAS = 128         # CTAs with exchange stamps
 LAST_END = 8
 
 
@@ -52,6 +56,8 @@ def main():
     dtree._lib = lib  # the builder below runs on the instrumented copy
     lib.dt_dchain_stamps.restype = ctypes.c_int
     lib.dt_dchain_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.dt_dchain_xstamps.restype = ctypes.c_int
+    lib.dt_dchain_xstamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
 
     torch.cuda.set_device(0)
     cfg = get_config(args.workload)
@@ -63,7 +69,8 @@ def main():
         raise SystemExit("the workload does not run the clustered depth chain")
     D = cfg.block - 1
     buf = np.zeros(2 * SLOTS * NPH, dtype=np.uint64)
-    acc = []
+    xbuf = np.zeros(2 * SLOTS * XCTAS, dtype=np.uint64)
+    acc, xacc = [], []
     for s in range(args.rounds + 3):
         H, r = make_round_inputs(cfg, s)
         Hd = dtree.bf16_tensor(H)
@@ -73,8 +80,11 @@ def main():
         n = lib.dt_dchain_stamps(buf.ctypes.data, buf.size)
         if n != buf.size:
             raise SystemExit("dt_dchain_stamps failed")
+        if lib.dt_dchain_xstamps(xbuf.ctypes.data, xbuf.size) != xbuf.size:
+            raise SystemExit("dt_dchain_xstamps failed")
         if s >= 3:
             acc.append(buf.reshape(2, SLOTS, NPH).astype(np.int64).copy())
+            xacc.append(xbuf.reshape(2, SLOTS, XCTAS).astype(np.int64).copy())
     st = np.stack(acc)  # [rounds, cta, slot, phase]
     if args.save:
         np.save(args.save, st)
@@ -118,10 +128,45 @@ def main():
         mid = slice(2, D)
         sub = lambda a, b: (k[:, mid, b] - k[:, mid, a]).mean()
         print(f"  A1: loads + MMAs {sub(1, 11):.0f}, partial sums {sub(11, 12):.0f}, barrier {sub(12, 13):.0f}, "
-              f"z {sub(13, 2):.0f};  B.lse: operands {sub(5, 15):.0f}, max/sum/log {sub(15, 6):.0f};  "
-              f"topW: keys + ranks {sub(8, 14):.0f}, ballots + barrier {sub(14, 9):.0f};  "
+              f"z {sub(13, 2):.0f};  B.sel: operands {sub(5, 15):.0f}, top-K rounds + log-partition {sub(15, 6):.0f};  "
+              f"topW: rounds {sub(8, 14):.0f}, survivor order {sub(14, 9):.0f};  "
               f"X: staging {sub(0, 16):.0f}, poll {sub(16, 17):.0f}, barrier + copies {sub(17, 1):.0f}")
+    exchange_report(np.stack(xacc), D, b.plan())
     b.close()
+
+
+def exchange_report(xs, D, plan):
+    """The state exchange seen by the global timer: for each depth, the spread
+    of the CTAs' publication times and how long after the last publication
+    each CTA held every state."""
+    import re
+    m = re.search(r"on (\d+) CTAs", plan)
+    G = min(int(m.group(1)), XCTAS) if m else XCTAS
+    pub, got = xs[:, 0, :, :G], xs[:, 1, :, :G]  # [rounds, depth, cta]
+    print(f"\nexchange (global timer, ns; {G} CTAs, mean over rounds)")
+    print("depth  pub spread  last-pub CTA (mode)  got - last pub: min / median / max")
+    spreads, lat_med, lat_max = [], [], []
+    for i in range(1, D):
+        p, q = pub[:, i], got[:, i]
+        last = p.max(axis=1)
+        spread = (last - p.min(axis=1)).mean()
+        lat = q - last[:, None]
+        who = np.bincount(p.argmax(axis=1), minlength=G).argmax()
+        spreads.append(spread)
+        lat_med.append(np.median(lat, axis=1).mean())
+        lat_max.append(lat.max(axis=1).mean())
+        print(f"{i:5d}  {spread:10.0f}  {who:19d}  {lat.min(axis=1).mean():7.0f} / {lat_med[-1]:7.0f} / "
+              f"{lat_max[-1]:7.0f}")
+    print(f"mean   {np.mean(spreads):10.0f}  {'':19s}  {'':7s}   {np.mean(lat_med):7.0f} / {np.mean(lat_max):7.0f}")
+    # the publication order: mean lateness of each CTA against the first one
+    late = (pub[:, 1:D] - pub[:, 1:D].min(axis=2, keepdims=True)).mean(axis=(0, 1))
+    order = np.argsort(-late)
+    print("latest publishers (CTA: mean ns after the first): " +
+          ", ".join(f"{c}: {late[c]:.0f}" for c in order[:8]))
+    print("earliest publishers: " + ", ".join(f"{c}: {late[c]:.0f}" for c in order[-4:]))
+    d = np.diff(np.sort(np.unique(pub[0, 1:D].ravel())))
+    if d.size:
+        print(f"timer step (smallest nonzero difference seen): {d[d > 0].min() if (d > 0).any() else 0} ns")
 
 
 if __name__ == "__main__":

@@ -35,8 +35,8 @@
 //       lambda - log(e^rest + sum e^lambda), per-branch top-K by K rounds of two
 //       warp max reductions over packed (lambda, token, candidate) keys (ties to
 //       the lower token id), children in token order, cumulative scores, top-W
-//       by (score, node index) with ranks counted by the whole block.  CTA 0
-//       writes the node arrays.
+//       by (score, node index) the same way in each warp that needs it.  CTA 0
+//       writes the node arrays once it has published its states.
 //   C   GRU update of the survivors' owned columns, r = sigmoid(x_r + u_r),
 //       z = sigmoid(x_z + u_z), n = tanh(x_n + r u_n), h' = (1 - z) n + z h with
 //       x = X[token] from the GRU-input table; published as the next X.
@@ -111,6 +111,10 @@ DT_DEVINL void st_async_f4(uint32_t a, float4 v, uint32_t mbar) {
                "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(mbar)
                : "memory");
 }
+// Named CTA barrier `id` over n threads: sync waits (and acquires), arrive
+// only signals (and releases the caller's shared-memory writes).
+DT_DEVINL void named_bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+DT_DEVINL void named_bar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 DT_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -173,9 +177,20 @@ __device__ unsigned long long g_dchain_stamps[2][kMaxDepth + 2][kStampPhases];
     if (tid == 0 && (cta == 0 || cta == L.G - 1))                                              \
       g_dchain_stamps[cta == 0 ? 0 : 1][depth][k] = static_cast<unsigned long long>(clock64()); \
   } while (0)
+// and every CTA's thread 0 records %globaltimer when it has published a
+// depth's states ([0][depth][cta]) and when it holds everyone's ([1][depth][cta])
+constexpr int kXStampCtas = 128;
+__device__ unsigned long long g_dchain_xstamps[2][kMaxDepth + 2][kXStampCtas];
+#define DCH_XSTAMP(which, depth)                                                   \
+  do {                                                                             \
+    if (tid == 0 && cta < kXStampCtas) g_dchain_xstamps[which][depth][cta] = dt_globaltimer(); \
+  } while (0)
 #else
 #define DCH_STAMP(depth, k) \
   do {                      \
+  } while (0)
+#define DCH_XSTAMP(which, depth) \
+  do {                           \
   } while (0)
 #endif
 
@@ -475,30 +490,32 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
   }
   __syncthreads();
 
-  // stage the candidate data of one depth (one cp.async group, possibly empty)
-  auto stage_depth = [&](int i) {
+  // stage the candidate data of one depth with threads t0 .. t0 + nt - 1 (one
+  // cp.async group each, possibly empty)
+  auto stage_depth = [&](int i, int t0, int nt) {
+    const int t = tid - t0;
     if (i <= p.depth_last) {
       const Stage b = stage(i);
       const int* tk = tok_all + (i - 1) * kMP;
       const int r8 = RQ / 8;
-      for (int idx = tid; idx < M * r8; idx += kT) {
+      for (int idx = t; idx < M * r8; idx += nt) {
         const int c = idx / r8, k8 = idx - c * r8;
         cp_async16(b.w2 + static_cast<size_t>(c) * RQP + 8 * k8, p.w2 + static_cast<size_t>(tk[c]) * r + r0 + 8 * k8);
       }
       constexpr int kQ4 = JC / 4;  // 16-byte pieces of one gate's owned columns
-      for (int idx = tid; idx < M * 3 * kQ4; idx += kT) {
+      for (int idx = t; idx < M * 3 * kQ4; idx += nt) {
         const int c = idx / (3 * kQ4), rem = idx - c * 3 * kQ4, gate = rem / kQ4, h = rem - gate * kQ4;
         cp_async16(b.xs + c * 3 * JC + gate * JC + 4 * h,
                    p.xtab + static_cast<size_t>(tk[c]) * 3 * g + gate * g + j0 + 4 * h);
       }
-      for (int c = tid; c < M; c += kT) cp_async4(b.cbs + c, p.cand_base + static_cast<size_t>(i - 1) * M + c);
-      for (int k4 = tid; k4 < RQ / 4; k4 += kT)
+      for (int c = t; c < M; c += nt) cp_async4(b.cbs + c, p.cand_base + static_cast<size_t>(i - 1) * M + c);
+      for (int k4 = t; k4 < RQ / 4; k4 += nt)
         cp_async16(b.h1 + 4 * k4, p.h1 + static_cast<size_t>(i - 1) * r + r0 + 4 * k4);
-      if (tid == 0) cp_async4(b.rest, p.rest_lse + (i - 1));
+      if (t == 0) cp_async4(b.rest, p.rest_lse + (i - 1));
     }
     cp_async_commit();
   };
-  stage_depth(p.depth_first);
+  stage_depth(p.depth_first, 0, kT);
 
   const int nkw = (L.nk16 - warp + kNW - 1) / kNW;  // k16 steps of this warp (kt = warp + kNW m)
   // lambda = (base + dL) / T as a product with 1/T (exact at T = 1; within an
@@ -522,10 +539,7 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     float* cscore = child_score(in);
 
     DCH_STAMP(i, 0);
-    // (the next depth's candidate data goes into the buffer depth i-1 used:
-    // every thread must be past depth i-1)
     if (i > f0) __syncthreads();
-    bool staged = false;
     // ================= X: the previous depth's states from every CTA =========
     // the words are laid out as the fragments themselves: word w is uint2 w of
     // the A-fragment array (k16 step, row, lane group, half), so a word that
@@ -544,9 +558,6 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
             pending |= 1u << j;
           }
         }
-        // the next depth's candidate data, issued while the loads fly
-        stage_depth(i + 1);
-        staged = true;
         DCH_STAMP(i, 16);
         uint64_t t0 = 0;
         uint32_t n = 0;
@@ -584,9 +595,11 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
       DCH_STAMP(i, 17);
       __syncthreads();
       aborted = s_abort != 0;
+      DCH_XSTAMP(1, i - 1);
     }
-    if (!staged) stage_depth(i + 1);
-    cp_async_wait_group1();  // this depth's staged data (issued a depth ago) has landed
+    // this depth's candidate data (issued a depth ago) has landed; the
+    // barrier after A1 shows it to every thread
+    cp_async_wait_all();
     const Stage st = stage(i);
 
     DCH_STAMP(i, 1);
@@ -757,20 +770,26 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
       key[0] = c0 < M ? cand_key(lam[0], tk[c0], c0) : 0ull;
       key[1] = c0 + 1 < M ? cand_key(lam[1], tk[c0 + 1], c0 + 1) : 0ull;
       DCH_STAMP(i, 15);
-      const float lmax = warp_max(fmaxf(rest, fmaxf(lam[0], lam[1])));
-      float se = (c0 < M ? expf(lam[0] - lmax) : 0.0f) + (c0 + 1 < M ? expf(lam[1] - lmax) : 0.0f);
-      se = warp_sum(se) + expf(rest - lmax);
-      const float logZ = lmax + logf(se);
-      DCH_STAMP(i, 6);
       // the K best keys in descending order: K rounds of two warp max
       // reductions (value part, then the (token, candidate) part among the
       // elements that reach the maximum value; keys are distinct, so exactly
-      // one element wins); the winner of round w is kept by lane w
+      // one element wins); the winner of round w is kept by lane w.  Round 0
+      // gives the largest lambda, and the rounds after it carry the butterfly
+      // levels of the log-partition's sum (offsets 16, 8, 4, 2, 1)
       uint32_t ha = static_cast<uint32_t>(key[0] >> 32), la = static_cast<uint32_t>(key[0]);
       uint32_t hb = static_cast<uint32_t>(key[1] >> 32), lb = static_cast<uint32_t>(key[1]);
       uint64_t wk = 0ull;
+      float lmax = 0.0f, se = 0.0f;
+      int lev = 0;
       for (int w = 0; w < K; ++w) {
         const uint32_t gh = __reduce_max_sync(0xFFFFFFFFu, ha > hb ? ha : hb);
+        if (w == 0) {
+          lmax = fmaxf(rest, key_f32(gh));
+          se = (c0 < M ? expf(lam[0] - lmax) : 0.0f) + (c0 + 1 < M ? expf(lam[1] - lmax) : 0.0f);
+        } else if (lev < 5) {
+          se += __shfl_xor_sync(0xFFFFFFFFu, se, 16 >> lev);
+          ++lev;
+        }
         const uint32_t mla = ha == gh ? la : 0u, mlb = hb == gh ? lb : 0u;
         const uint32_t gl = __reduce_max_sync(0xFFFFFFFFu, mla > mlb ? mla : mlb);
         if (ha == gh && la == gl) {
@@ -782,6 +801,10 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
         }
         if (lane == w) wk = (static_cast<uint64_t>(gh) << 32) | gl;
       }
+      for (; lev < 5; ++lev) se += __shfl_xor_sync(0xFFFFFFFFu, se, 16 >> lev);
+      se += expf(rest - lmax);
+      const float logZ = lmax + logf(se);
+      DCH_STAMP(i, 6);
       const int tok = lane < K ? cand_key_tok(wk) : 0x7FFFFFFF;
       int trank = 0;
       for (int m0 = 0; m0 < K; m0 += 8) {
@@ -810,9 +833,12 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     }
     // top-W of the depth by (score desc, node index asc); survivors ascending.
     // Up to 64 children: warp 0 takes the Li best by rounds of two warp max
-    // reductions over (score key, inverted index); more: ranks counted by the
+    // reductions over (score key, inverted index) and keeps them in its own
+    // scratch (the only warp that reads them); more: ranks counted by the
     // block
-    if (nchild <= 64) {
+    const bool spec = nchild <= 64;
+    const int* sv = surv;
+    if (spec) {
       if (warp == 0) {
         const int e0 = 2 * lane, e1 = 2 * lane + 1;
         uint32_t ha = e0 < nchild ? f32_key(cscore[e0]) : 0u, la = e0 < nchild ? 0xFFFFFFFFu - e0 : 0u;
@@ -838,25 +864,24 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
           const int t2 = __shfl_sync(0xFFFFFFFFu, mine, m);
           pos += (m < Li && t2 < mine) ? 1 : 0;
         }
-        if (lane < Li) surv[pos] = mine;
+        int* ws = reinterpret_cast<int*>(red1);
+        if (lane < Li) ws[pos] = mine;
+        __syncwarp();
+        sv = ws;
       }
     } else {
-      const int tp = nchild <= 64 ? 4 : 1;
-      const int e = tid / tp, part4 = tid - e * tp;
+      // one thread per child (nchild <= kP * 32 = kT)
+      const int e = tid;
       int rk = 0;
       if (e < nchild) {
         const float se = cscore[e];
 #pragma unroll 4
-        for (int f2 = part4; f2 < nchild; f2 += tp) {
+        for (int f2 = 0; f2 < nchild; ++f2) {
           const float sf = cscore[f2];
           rk += (sf > se || (sf == se && f2 < e)) ? 1 : 0;
         }
       }
-      if (tp == 4) {
-        rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 1);
-        rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 2);
-      }
-      const bool alive = e < nchild && part4 == 0 && rk < Li;
+      const bool alive = e < nchild && rk < Li;
       const unsigned bal = __ballot_sync(0xFFFFFFFFu, alive);
       if (lane == 0) s_wcnt[warp] = __popc(bal);
       __syncthreads();
@@ -865,15 +890,58 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
         for (int w2 = 0; w2 < warp; ++w2) pos += s_wcnt[w2];
         surv[pos] = e;
       }
+      __syncthreads();
     }
-    __syncthreads();
     DCH_STAMP(i, 9);
     // ================= C: GRU update of the survivors' owned columns =========
-    if (tid < kWP) {
-      const int w = tid / kHP, pair = tid - w * kHP;
-      float hn[2] = {0.0f, 0.0f};
-      if (w < Li) {
-        const int e = surv[w], b = e / K;
+    // Warps 1.. compute the new owned columns of every child (up to 64
+    // children: while warp 0 still selects, their rows being ready when it
+    // needs them) or of the survivors, into hrow [row][JC] (the A3 partial
+    // sums' area, free since uhh); warp 0 then takes the survivors' rows,
+    // publishes them and keeps them for the next depth.
+    float* hrow = red2;
+    if (warp == 0) {
+      if (lane < kP) {
+        const int w = lane;
+        if (w < Li) {
+          const int e = sv[w];
+          pnode[in * kP + w] = row_off + e;
+          pscore[in * kP + w] = cscore[e];
+          if (cta == 0 && !aborted) {
+            if (i == p.depth_last) p.live[in * W + w] = row_off + e;
+            if (p.live_out) p.live_out[w] = row_off + e;
+          }
+        } else if (w < W && cta == 0 && p.live_out) {
+          p.live_out[w] = -1;
+        }
+      }
+      named_bar_sync(1, kT);  // the rows of warps 1..
+      for (int t = lane; t < kWP; t += 32) {
+        const int w = t / kHP, pair = t - w * kHP;
+        float2 hn = make_float2(0.0f, 0.0f);
+        if (w < Li) hn = *reinterpret_cast<const float2*>(hrow + (spec ? sv[w] : w) * JC + 2 * pair);
+        *reinterpret_cast<float2*>(sown + (in * kP + w) * JC + 2 * pair) = hn;
+        if (i < p.depth_last) {
+          if (!aborted) {
+            const uint2 hl = hilo_pair(hn.x, hn.y);
+            const uint64_t tag = static_cast<uint64_t>(make_tag(E, i)) << 32;
+            // word index = the fragment position of columns col, col + 1 of row w
+            const int col = j0 + 2 * pair;
+            const int wi = (((col >> 4) * 8 + w) * 4 + ((col & 7) >> 1)) * 2 + ((col & 15) >> 3);
+            st_tagged(xch + (static_cast<size_t>(in) * nwords + wi) * 2, tag | hl.x, tag | hl.y);
+          }
+        } else if (w < Li && !aborted) {
+          // the launch ends before depth D: fp32 states for the next launch
+          float* Sg = p.S + static_cast<size_t>(in) * W * g + static_cast<size_t>(w) * g + j0 + 2 * pair;
+          Sg[0] = hn.x;
+          Sg[1] = hn.y;
+        }
+      }
+    } else {
+      const int nrows = spec ? nchild : Li;
+      for (int idx = tid - 32; idx < nrows * kHP; idx += kT - 32) {
+        const int row = idx / kHP, pair = idx - row * kHP;
+        const int e = spec ? row : surv[row], b = e / K;
         int c = cslot[e];
         if (c < 0 || c >= M) {
           dt_report(p.status, DT_DEV_BOUNDS);
@@ -882,6 +950,7 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
         const float* x = st.xs + c * 3 * JC;
         const float* uu = uhh + b * 3 * JC;
         const float* hp = sown + (ip * kP + b) * JC;
+        float hn[2];
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int jj = 2 * pair + e2;
@@ -890,38 +959,14 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
           const float ng = tanhf_(x[2 * JC + jj] + rg * uu[2 * JC + jj]);
           hn[e2] = (1.0f - zg) * ng + zg * hp[jj];
         }
+        *reinterpret_cast<float2*>(hrow + row * JC + 2 * pair) = make_float2(hn[0], hn[1]);
       }
-      sown[(in * kP + w) * JC + 2 * pair] = hn[0];
-      sown[(in * kP + w) * JC + 2 * pair + 1] = hn[1];
-      if (i < p.depth_last) {
-        if (!aborted) {
-          const uint2 hl = hilo_pair(hn[0], hn[1]);
-          const uint64_t tag = static_cast<uint64_t>(make_tag(E, i)) << 32;
-          // word index = the fragment position of columns col, col + 1 of row w
-          const int col = j0 + 2 * pair;
-          const int wi = (((col >> 4) * 8 + w) * 4 + ((col & 7) >> 1)) * 2 + ((col & 15) >> 3);
-          st_tagged(xch + (static_cast<size_t>(in) * nwords + wi) * 2, tag | hl.x, tag | hl.y);
-        }
-      } else if (w < Li && !aborted) {
-        // the launch ends before depth D: fp32 states for the next launch
-        float* Sg = p.S + static_cast<size_t>(in) * W * g + static_cast<size_t>(w) * g + j0 + 2 * pair;
-        Sg[0] = hn[0];
-        Sg[1] = hn[1];
-      }
-    } else if (tid >= 128 && tid < 128 + kP) {
-      const int w = tid - 128;
-      if (w < Li) {
-        const int e = surv[w];
-        pnode[in * kP + w] = row_off + e;
-        pscore[in * kP + w] = cscore[e];
-        if (cta == 0 && !aborted) {
-          if (i == p.depth_last) p.live[in * W + w] = row_off + e;
-          if (p.live_out) p.live_out[w] = row_off + e;
-        }
-      } else if (w < W && cta == 0 && p.live_out) {
-        p.live_out[w] = -1;
-      }
+      named_bar_arrive(1, kT);
+      // the next depth's candidate data, into the buffer depth i-1 used (every
+      // thread has passed depth i-1: the barriers of this depth's X and A1)
+      stage_depth(i + 1, 32, kT - 32);
     }
+    DCH_XSTAMP(0, i);
     if (cta == 0 && !aborted) write_nodes(i);
     DCH_STAMP(i, 10);
     // (the next depth's barriers order these shared-memory writes)
@@ -1061,15 +1106,24 @@ cudaError_t launch_dchain(const DchainParams& p, cudaStream_t stream) {
 }  // namespace dt
 
 #ifdef DT_DCHAIN_TIMING
-// The phase stamps of the last clustered-chain launch: 2 x 65 x 12 clock64()
+// The phase stamps of the last clustered-chain launch: 2 x 66 x 20 clock64()
 // values ([CTA 0 / last CTA][slot][phase]; slot 0: kernel start, end of the
 // depth loop, end of the tail, before and after the wait for the previous
-// kernel; slot i: the starts of depth i's X, A1, A2, A3, R, B, B's sort, B's
-// writes done, top-W, C, and C's end).
+// kernel, before Top-B and before the tree; slot i: the starts of depth i's
+// X, A1, A2, A3, R, B, B's sort, B's writes done, top-W, C, C's end, and the
+// finer boundaries 11-17 inside A1, top-W, B and X).
 // Returns the number of values copied, or -1.
 extern "C" int dt_dchain_stamps(unsigned long long* out, int n) {
   const int total = 2 * (dt::kMaxDepth + 2) * dt::kStampPhases;
   if (!out || n < total) return -1;
   return cudaMemcpyFromSymbol(out, dt::g_dchain_stamps, sizeof(dt::g_dchain_stamps)) == cudaSuccess ? total : -1;
+}
+// The exchange stamps of the last launch, [published / received][depth][CTA]
+// (%globaltimer, ns; CTAs beyond 128 are not recorded).  Returns the number of
+// values copied, or -1.
+extern "C" int dt_dchain_xstamps(unsigned long long* out, int n) {
+  const int total = 2 * (dt::kMaxDepth + 2) * dt::kXStampCtas;
+  if (!out || n < total) return -1;
+  return cudaMemcpyFromSymbol(out, dt::g_dchain_xstamps, sizeof(dt::g_dchain_xstamps)) == cudaSuccess ? total : -1;
 }
 #endif
