@@ -901,20 +901,6 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     // publishes them and keeps them for the next depth.
     float* hrow = red2;
     if (warp == 0) {
-      if (lane < kP) {
-        const int w = lane;
-        if (w < Li) {
-          const int e = sv[w];
-          pnode[in * kP + w] = row_off + e;
-          pscore[in * kP + w] = cscore[e];
-          if (cta == 0 && !aborted) {
-            if (i == p.depth_last) p.live[in * W + w] = row_off + e;
-            if (p.live_out) p.live_out[w] = row_off + e;
-          }
-        } else if (w < W && cta == 0 && p.live_out) {
-          p.live_out[w] = -1;
-        }
-      }
       named_bar_sync(1, kT);  // the rows of warps 1..
       for (int t = lane; t < kWP; t += 32) {
         const int w = t / kHP, pair = t - w * kHP;
@@ -937,29 +923,57 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
           Sg[1] = hn.y;
         }
       }
+      // the live list (read by the next depth, after its barriers)
+      if (lane < kP) {
+        const int w = lane;
+        if (w < Li) {
+          const int e = sv[w];
+          pnode[in * kP + w] = row_off + e;
+          pscore[in * kP + w] = cscore[e];
+          if (cta == 0 && !aborted) {
+            if (i == p.depth_last) p.live[in * W + w] = row_off + e;
+            if (p.live_out) p.live_out[w] = row_off + e;
+          }
+        } else if (w < W && cta == 0 && p.live_out) {
+          p.live_out[w] = -1;
+        }
+      }
     } else {
       const int nrows = spec ? nchild : Li;
-      for (int idx = tid - 32; idx < nrows * kHP; idx += kT - 32) {
-        const int row = idx / kHP, pair = idx - row * kHP;
-        const int e = spec ? row : surv[row], b = e / K;
-        int c = cslot[e];
-        if (c < 0 || c >= M) {
-          dt_report(p.status, DT_DEV_BOUNDS);
-          c = 0;
-        }
-        const float* x = st.xs + c * 3 * JC;
-        const float* uu = uhh + b * 3 * JC;
-        const float* hp = sown + (ip * kP + b) * JC;
-        float hn[2];
+      // at most kIt rows per thread; unrolled so that their loads and
+      // activations overlap
+      constexpr int kIt = (kMP * kHP + kT - 33) / (kT - 32);
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int jj = 2 * pair + e2;
-          const float rg = sigmoidf_(x[jj] + uu[jj]);
-          const float zg = sigmoidf_(x[JC + jj] + uu[JC + jj]);
-          const float ng = tanhf_(x[2 * JC + jj] + rg * uu[2 * JC + jj]);
-          hn[e2] = (1.0f - zg) * ng + zg * hp[jj];
+      for (int it = 0; it < kIt; ++it) {
+        const int idx = tid - 32 + it * (kT - 32);
+        if (idx < nrows * kHP) {
+          const int row = idx / kHP, pair = idx - row * kHP;
+          const int e = spec ? row : surv[row], b = e / K;
+          int c = cslot[e];
+          if (c < 0 || c >= M) {
+            dt_report(p.status, DT_DEV_BOUNDS);
+            c = 0;
+          }
+          const float* x = st.xs + c * 3 * JC + 2 * pair;
+          const float* uu = uhh + b * 3 * JC + 2 * pair;
+          const float2 xr = *reinterpret_cast<const float2*>(x), xz = *reinterpret_cast<const float2*>(x + JC),
+                       xn = *reinterpret_cast<const float2*>(x + 2 * JC);
+          const float2 ur = *reinterpret_cast<const float2*>(uu), uz = *reinterpret_cast<const float2*>(uu + JC),
+                       un = *reinterpret_cast<const float2*>(uu + 2 * JC);
+          const float2 hp = *reinterpret_cast<const float2*>(sown + (ip * kP + b) * JC + 2 * pair);
+          float2 hn;
+          {
+            const float rg = sigmoidf_(xr.x + ur.x), zg = sigmoidf_(xz.x + uz.x);
+            const float ng = tanhf_(xn.x + rg * un.x);
+            hn.x = (1.0f - zg) * ng + zg * hp.x;
+          }
+          {
+            const float rg = sigmoidf_(xr.y + ur.y), zg = sigmoidf_(xz.y + uz.y);
+            const float ng = tanhf_(xn.y + rg * un.y);
+            hn.y = (1.0f - zg) * ng + zg * hp.y;
+          }
+          *reinterpret_cast<float2*>(hrow + row * JC + 2 * pair) = hn;
         }
-        *reinterpret_cast<float2*>(hrow + row * JC + 2 * pair) = make_float2(hn[0], hn[1]);
       }
       named_bar_arrive(1, kT);
       // the next depth's candidate data, into the buffer depth i-1 used (every
