@@ -49,7 +49,7 @@ def main():
     from .build import LIB_DIR, build_library
     from workloads import get_config, make_round_inputs, make_weights
 
-    path = build_library(force=True, extra_flags=["-DDT_DCHAIN_TIMING"],
+    path = build_library(force=True, extra_flags=["-DDT_DCHAIN_TIMING", "-DDT_TOPM_TIMING"],
                          lib_path=os.path.join(LIB_DIR, "libdtree_timing.so"))
     dtree._lib = None
     lib = dtree.load_library(path)
@@ -58,6 +58,8 @@ def main():
     lib.dt_dchain_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
     lib.dt_dchain_xstamps.restype = ctypes.c_int
     lib.dt_dchain_xstamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.dt_topm_stamps.restype = ctypes.c_int
+    lib.dt_topm_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
 
     torch.cuda.set_device(0)
     cfg = get_config(args.workload)
@@ -70,7 +72,8 @@ def main():
     D = cfg.block - 1
     buf = np.zeros(2 * SLOTS * NPH, dtype=np.uint64)
     xbuf = np.zeros(2 * SLOTS * XCTAS, dtype=np.uint64)
-    acc, xacc = [], []
+    tbuf = np.zeros(2 * 64 * 16, dtype=np.uint64)
+    acc, xacc, tacc = [], [], []
     for s in range(args.rounds + 3):
         H, r = make_round_inputs(cfg, s)
         Hd = dtree.bf16_tensor(H)
@@ -82,9 +85,12 @@ def main():
             raise SystemExit("dt_dchain_stamps failed")
         if lib.dt_dchain_xstamps(xbuf.ctypes.data, xbuf.size) != xbuf.size:
             raise SystemExit("dt_dchain_xstamps failed")
+        if lib.dt_topm_stamps(tbuf.ctypes.data, tbuf.size) != tbuf.size:
+            raise SystemExit("dt_topm_stamps failed")
         if s >= 3:
             acc.append(buf.reshape(2, SLOTS, NPH).astype(np.int64).copy())
             xacc.append(xbuf.reshape(2, SLOTS, XCTAS).astype(np.int64).copy())
+            tacc.append(tbuf.reshape(2, 64, 16).astype(np.int64).copy())
     st = np.stack(acc)  # [rounds, cta, slot, phase]
     if args.save:
         np.save(args.save, st)
@@ -132,7 +138,28 @@ def main():
               f"topW: rounds {sub(8, 14):.0f}, survivor order {sub(14, 9):.0f};  "
               f"X: staging {sub(0, 16):.0f}, poll {sub(16, 17):.0f}, barrier + copies {sub(17, 1):.0f}")
     exchange_report(np.stack(xacc), D, b.plan())
+    topm_report(np.stack(tacc))
     b.close()
+
+
+def topm_report(ts):
+    """Top-M of row 0 by the global timer: the chunk CTAs' phases and the merge."""
+    part, mrg = ts[:, 0], ts[:, 1, 0]  # [rounds, split, k], [rounds, k]
+    S = int((part[0, :, 1] > 0).sum())
+    part = part[:, :S]
+    t1 = part[:, :, 1].min(axis=1)  # the earliest chunk CTA past the wait
+    d = lambda a, b: (part[:, :, b] - part[:, :, a]).mean()
+    print(f"\nTop-M, row 0 ({S} chunk CTAs; ns, mean over CTAs and rounds)")
+    print(f"chunk CTAs: stats {d(1, 2):.0f}, rung {d(2, 3):.0f}, collect {d(3, 4):.0f}, M-th key [range {d(4, 10):.0f}, "
+          f"histogram {d(10, 11):.0f}, bin {d(11, 12):.0f}, gather {d(12, 13):.0f}, rank {d(13, 14):.0f}], "
+          f"losers {d(7, 8):.0f}, winners {d(8, 9):.0f}, their ranks {d(9, 5):.0f}, rest + arrival {d(5, 6):.0f}")
+    print(f"chunk CTAs past the wait: last {(part[:, :, 1] - t1[:, None]).max(axis=1).mean():.0f} ns after the first; "
+          f"arrivals: first {(part[:, :, 6].min(axis=1) - t1).mean():.0f}, last "
+          f"{(part[:, :, 6].max(axis=1) - t1).mean():.0f}")
+    m = lambda a, b: (mrg[:, b] - mrg[:, a]).mean()
+    print(f"merge: starts {(mrg[:, 0] - t1).mean():.0f}; entries + range {m(0, 10):.0f}, histogram {m(10, 11):.0f}, "
+          f"bin {m(11, 12):.0f}, gather {m(12, 13):.0f}, rank {m(13, 14):.0f}, winners {m(1, 2):.0f}, "
+          f"their ranks {m(2, 3):.0f}, rest + writes {m(3, 4):.0f}; ends {(mrg[:, 4] - t1).mean():.0f}")
 
 
 def exchange_report(xs, D, plan):

@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
   __shared__ float s_tred[64];
   __shared__ int s_tscan[40];
   __shared__ __align__(8) uint64_t s_mbar[2];  // the two rounds of the cluster's correction exchange
+  __shared__ __align__(8) uint64_t s_mbar_w;   // the resident weights' bulk copies
   constexpr int kHP = JC / 2;      // column pairs per CTA
   constexpr int kT2 = 3 * JC / 8;  // W_hh tiles per CTA
   constexpr int kWP = kP * kHP;    // 16-byte words one CTA publishes per depth
@@ -373,27 +374,29 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     s_abort = 0;
     mbar_init(&s_mbar[0], 1);
     mbar_init(&s_mbar[1], 1);
+    mbar_init(&s_mbar_w, 1);
     fence_mbar_init();
   }
   uint32_t mb_phase = 0;
   DCH_STAMP(0, 0);
 
-  // ---- resident weights: rows 0..RQ-1 = W1_S(R), rows RQ.. = W_hh gate rows of J ----
+  // ---- resident weights: rows 0..RQ-1 = W1_S(R), rows RQ.. = W_hh gate rows
+  // of J, one bulk copy of g bf16 per row (all in flight at once; waited for
+  // before the first projection) ----
   {
-    const int g8 = gp / 8;
     const int nrow = RQ + 3 * JC;
-    for (int idx = tid; idx < nrow * g8; idx += kT) {
-      const int row = idx / g8, k8 = idx - row * g8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (8 * k8 < g) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&s_mbar_w, static_cast<uint32_t>(nrow * g * 2));
+      for (int row = 0; row < nrow; ++row) {
+        const uint16_t* src;
         if (row < RQ) {
-          v = *reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(r0 + row) * p.ldw1 + p.d + 8 * k8);
+          src = p.w1 + static_cast<size_t>(r0 + row) * p.ldw1 + p.d;
         } else {
           const int rr = row - RQ, gate = rr / JC, jj = rr - gate * JC;
-          v = *reinterpret_cast<const uint4*>(p.w_hh + static_cast<size_t>(gate * g + j0 + jj) * g + 8 * k8);
+          src = p.w_hh + static_cast<size_t>(gate * g + j0 + jj) * g;
         }
+        bulk_g2s(w_s + static_cast<size_t>(row) * gp, src, static_cast<uint32_t>(g * 2), &s_mbar_w);
       }
-      *reinterpret_cast<uint4*>(w_s + static_cast<size_t>(row) * gp + 8 * k8) = v;
     }
     // candidate slots beyond M hold zero W2 rows in every stage buffer
     for (int s = 0; s < kNS; ++s) {
@@ -527,6 +530,10 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
 
   // the peers' barriers are initialised before anyone pushes into them
   cluster_sync();
+  if (!mbar_wait(&s_mbar_w, 0, p.status)) {
+    st_relaxed_u32(p.abort_word, E);
+    aborted = true;
+  }
 
   for (int i = f0; i <= p.depth_last; ++i) {
     const int Lp = p.L[i - 1];  // live branches entering this depth

@@ -13,16 +13,17 @@
 //      shared-memory atomic per warp) and collected; too few (< M) moves to
 //      the next rung and counts again, too many (> 512) or none left falls back
 //      to a radix select of the whole chunk;
-//   4. the candidates are ranked exactly by counting (a group of threads per
-//      candidate): a candidate's rank is its position in the sorted top-M.
+//   4. the M-th largest candidate is found with a 256-bin histogram of the
+//      candidates' values (its bin's few keys ranked exactly); the M best are
+//      gathered and ranked among themselves by counting, which gives the
+//      sorted list.
 // The chunk also reports the max of logit/T and the sum of exp(logit/T - max)
-// over its non-selected tokens.
+// over its non-selected tokens, each thread adding its own values in a fixed
+// order (no result bit depends on the order of atomics).
 //
 // The last CTA of a row (a per-row arrival counter; nothing waits) merges the
-// S sorted lists.  The M-th largest key among the first t entries of every
-// list is a lower bound on the row's M-th largest (a subset's M-th largest
-// never exceeds the whole set's), so only entries at or above it can win;
-// those few are ranked exactly and written in order, and
+// S sorted lists the same way: the M-th largest of the S*M entries by the
+// histogram, the M best ranked among themselves, and
 //   rest_lse = log( sum_chunks part_sum e^{part_max} + sum_{losing entries} e^{logit/T} ),
 // so every non-candidate token enters the log-partition exactly once.
 #include "common.cuh"
@@ -42,6 +43,24 @@ constexpr int kSample = 4;            // values per thread in the sample
 constexpr int kRungs = 8;             // threshold ladder
 constexpr int kCandCap = kThreads;    // candidates ranked in the partial phase
 constexpr int kMergeCap = 2048;       // merge candidates ranked among themselves
+
+// Phase stamps (built with -DDT_TOPM_TIMING only): %globaltimer at the phase
+// boundaries of row 0: [0][split][k] for the chunk CTAs, [1][0][k] for the CTA
+// that merges the row; dt_topm_stamps copies them out.
+#ifdef DT_TOPM_TIMING
+constexpr int kTopmStampSplits = 64;
+constexpr int kTopmStamps = 16;
+__device__ unsigned long long g_topm_stamps[2][kTopmStampSplits][kTopmStamps];
+#define TOPM_STAMP(which, k)                                                                        \
+  do {                                                                                             \
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.x < kTopmStampSplits)                      \
+      g_topm_stamps[which][(which) ? 0 : blockIdx.x][k] = dt_globaltimer();                         \
+  } while (0)
+#else
+#define TOPM_STAMP(which, k) \
+  do {                       \
+  } while (0)
+#endif
 
 DT_DEVINL float rung_c(int k) {
   return k < 5 ? 1.0f + 0.25f * static_cast<float>(k) : (k == 5 ? 2.5f : (k == 6 ? 3.0f : 4.0f));
@@ -101,6 +120,121 @@ DT_DEVINL void rank_all(const uint64_t* keys, int c, Fn fn) {
   }
 }
 
+// The m-th largest of the nonzero keys among keys[0, n) in shared memory
+// (distinct; 1 <= m), or 0 when there are fewer than m of them.  A 256-bin
+// histogram over the value range puts the m-th key into one bin (bins are
+// monotone in the value, so every key of an earlier bin is larger); that
+// bin's keys are gathered into bnd (kMergeCap keys) and ranked among
+// themselves, or, when more than that share the bin, each is ranked over the
+// whole array.  hist: 256 words; sc: 4 ints; red: 2 kWarps floats; s_key: one
+// key.  Every thread of the block calls; all get the key.
+template <int kWhich>  // stamp set of the timing build: 0 chunk, 1 merge
+DT_DEVINL uint64_t block_kth_key(const uint64_t* keys, int n, int m, uint32_t* hist, int* sc, uint64_t* bnd,
+                                 float* red, uint64_t* s_key) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float lo = INFINITY, hi = -INFINITY;
+  for (int e = tid; e < n; e += kThreads) {
+    const uint64_t k = keys[e];
+    if (k != 0ull) {
+      const float v = key_f32(static_cast<uint32_t>(k >> 32));
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+  }
+  lo = -warp_max(-lo);
+  hi = warp_max(hi);
+  if (lane == 0) {
+    red[warp] = lo;
+    red[kWarps + warp] = hi;
+  }
+  for (int b = tid; b < 256; b += kThreads) hist[b] = 0u;
+  if (tid == 0) {
+    sc[0] = -1;
+    sc[2] = 0;
+    *s_key = 0ull;
+  }
+  __syncthreads();
+  TOPM_STAMP(kWhich, 10);
+  lo = INFINITY;
+  hi = -INFINITY;
+  for (int w = 0; w < kWarps; ++w) {
+    lo = fminf(lo, red[w]);
+    hi = fmaxf(hi, red[kWarps + w]);
+  }
+  const float scale = hi > lo ? 256.0f / (hi - lo) : 0.0f;
+  auto bin_of = [&](uint64_t k) {
+    return min(255, max(0, __float2int_rz((hi - key_f32(static_cast<uint32_t>(k >> 32))) * scale)));
+  };
+  for (int e = tid; e < n; e += kThreads) {
+    const uint64_t k = keys[e];
+    if (k != 0ull) atomicAdd(&hist[bin_of(k)], 1u);
+  }
+  __syncthreads();
+  TOPM_STAMP(kWhich, 11);
+  if (warp == 0) {
+    // lane l totals bins 8l .. 8l+7; the first bin where the running count
+    // reaches m holds the m-th key
+    uint32_t c8[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c8[j] = hist[8 * lane + j];
+      sum += c8[j];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(m));
+    if (hit && lane == __ffs(hit) - 1) {
+      uint32_t cum = incl - sum;
+      for (int j = 0; j < 8; ++j) {
+        if (cum + c8[j] >= static_cast<uint32_t>(m)) {
+          sc[0] = 8 * lane + j;
+          sc[1] = static_cast<int>(cum);
+          break;
+        }
+        cum += c8[j];
+      }
+    }
+  }
+  __syncthreads();
+  TOPM_STAMP(kWhich, 12);
+  const int bt = sc[0];
+  if (bt < 0) return 0ull;  // fewer than m keys: every one is among the best m (uniform)
+  const int need = m - sc[1];  // the need-th largest key of bin bt
+  for (int e = tid; e < n; e += kThreads) {
+    const uint64_t k = keys[e];
+    if (k != 0ull && bin_of(k) == bt) {
+      const int at = atomicAdd(&sc[2], 1);
+      if (at < kMergeCap) bnd[at] = k;
+    }
+  }
+  __syncthreads();
+  TOPM_STAMP(kWhich, 13);
+  const int nb = sc[2];
+  if (nb <= kMergeCap) {
+    rank_all(bnd, nb, [&](int, uint64_t ke, int rk) {
+      if (rk == need - 1) *s_key = ke;
+    });
+  } else {
+    for (int e = tid; e < n; e += kThreads) {
+      const uint64_t k = keys[e];
+      if (k == 0ull || bin_of(k) != bt) continue;
+      int rk = 0;
+      for (int f = 0; f < n; ++f) {
+        const uint64_t kf = keys[f];
+        rk += (kf > k && bin_of(kf) == bt) ? 1 : 0;
+      }
+      if (rk == need - 1) *s_key = k;
+    }
+  }
+  __syncthreads();
+  TOPM_STAMP(kWhich, 14);
+  return *s_key;
+}
+
 // kMinBlocks = 2 caps the registers so that two CTAs share an SM: for grids of
 // many waves (many rows), where each CTA's chain of phases is latency-bound.
 template <int kMinBlocks>
@@ -114,10 +248,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
   __shared__ int rung_cnt[kWarps][kRungs];
   __shared__ int s_rung, s_ncand, s_last;
   __shared__ uint64_t s_lb;
-  // exp terms of losing candidates, stored at their rank and summed in rank
-  // order: the slot order of a candidate (claimed by atomics) never changes a
-  // result bit
-  __shared__ float s_term[kMergeCap];
 
   // dynamic shared memory: a 64 KB area (chunk keys of the fallback, merge
   // entries) followed by the candidate keys
@@ -135,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
   const int nv = n > tid ? min(kVPT, (n - tid + kThreads - 1) / kThreads) : 0;  // valid values of this thread
 
   // the logits come from the previous kernel; the next one may then launch
+  TOPM_STAMP(0, 0);
   dt_grid_wait();
+  TOPM_STAMP(0, 1);
   dt_grid_release();
   if (p.clear_word && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *p.clear_word = 0u;
 
@@ -188,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
   const float sigma = nsamp > 0.0f ? sqrtf(fmaxf(red4[2][kWarps] / nsamp - mean * mean, 0.0f)) : 0.0f;
   const float mxT = mx * invT;
 
+  TOPM_STAMP(0, 2);
   // ---------------- 2. the first rung to try, from the sample ----------------
   if (mloc < n && sigma > 0.0f) {
     int cnt[kRungs];
@@ -217,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
   }
   __syncthreads();
 
+  TOPM_STAMP(0, 3);
   // ---------------- 3. exact count and collection above the threshold ----------------
   float rest = 0.0f;
   int k = s_rung;
@@ -249,24 +383,37 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
     fast = false;                               // too many, or the ladder is exhausted
   }
   __syncthreads();
+  TOPM_STAMP(0, 4);
 
   if (fast) {
-#pragma unroll
-    for (int j = 0; j < kVPT; ++j)
-      if (!((flags >> j) & 1u)) rest += __expf(vals[j] * invT - mxT);  // padding gives 0
-    // ---------------- 4. exact ranks: the sorted partial list ----------------
-    rank_all(cand, c, [&](int, uint64_t ke, int rk) {
-      const float v = key_f32(static_cast<uint32_t>(ke >> 32));
-      if (rk < mloc) {
-        p.part_id[q * p.M + rk] = static_cast<int>(rank_key_id(ke));
-        p.part_val[q * p.M + rk] = v;
-        if (rk == mloc - 1) p.part_kth[q] = (mloc < n) ? v : -INFINITY;
-      } else {
-        s_term[rk] = expf(v * invT - mxT);
-      }
-    });
+    // ---------------- 4. the M-th candidate; the sorted partial list ----------------
+    if (tid == 0) s_ncand = 0;  // (c is held in registers) counts the winners below
+    const uint64_t kth = c > mloc ? block_kth_key<0>(cand, c, mloc, hist, scan, big, &red4[0][0], &s_lb) : 0ull;
     __syncthreads();
-    if (tid >= mloc && tid < c) rest += s_term[tid];  // c <= kCandCap = kThreads
+    TOPM_STAMP(0, 7);
+    // each thread's values outside the best M feed the log-partition (in its
+    // own fixed order); the best M are gathered and ranked among themselves
+#pragma unroll
+    for (int j = 0; j < kVPT; ++j) {
+      if (!((flags >> j) & 1u)) {
+        rest += __expf(vals[j] * invT - mxT);  // padding gives 0
+      } else if (rank_key(vals[j], static_cast<uint32_t>(v0 + tid + j * kThreads)) < kth) {
+        rest += expf(vals[j] * invT - mxT);
+      }
+    }
+    TOPM_STAMP(0, 8);
+    for (int e = tid; e < c; e += kThreads) {
+      const uint64_t k2 = cand[e];
+      if (k2 >= kth) big[atomicAdd(&s_ncand, 1)] = k2;
+    }
+    __syncthreads();
+    TOPM_STAMP(0, 9);
+    rank_all(big, s_ncand, [&](int, uint64_t ke, int rk) {
+      const float v = key_f32(static_cast<uint32_t>(ke >> 32));
+      p.part_id[q * p.M + rk] = static_cast<int>(rank_key_id(ke));
+      p.part_val[q * p.M + rk] = v;
+      if (rk == mloc - 1) p.part_kth[q] = (mloc < n) ? v : -INFINITY;
+    });
   } else {
     // ---------------- fallback: radix select over the whole chunk ----------------
     uint32_t* keys = reinterpret_cast<uint32_t*>(big);
@@ -320,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
       if (rk == mloc - 1) p.part_kth[q] = (mloc < n) ? v : -INFINITY;
     });
   }
+  TOPM_STAMP(0, 5);
   rest = block_sum(rest, red);
   if (tid == 0) {
     p.part_max[q] = mxT;
@@ -337,7 +485,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
     __threadfence();
   }
   __syncthreads();
+  TOPM_STAMP(0, 6);
   if (!s_last) return;
+  TOPM_STAMP(1, 0);
 
   const size_t rb = static_cast<size_t>(row) * p.S;
   const int S = p.S, M = p.M;
@@ -354,77 +504,47 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
     const int cnt = p.part_cnt[rb + s2];
     big[e] = j < cnt ? rank_key(v, static_cast<uint32_t>(id)) : 0ull;
   }
-  if (tid == 0) {
-    s_lb = 0ull;
-    s_ncand = 0;
-  }
+  if (tid == 0) s_ncand = 0;
   __syncthreads();
-  // lower bound: the M-th largest key among the first t entries of every list
-  const int t = min(M, max(1, (2 * M + S - 1) / S));
-  const int nsub = S * t;  // <= 2M + S <= kMergeCap
-  if (nsub >= M) {
-    for (int u = tid; u < nsub; u += kThreads) {
-      const int s2 = u / t, j = u - s2 * t;
-      cand[u] = big[s2 * M + j];
-    }
-    __syncthreads();
-    rank_all(cand, nsub, [&](int, uint64_t ke, int rk) {
-      if (ke != 0ull && rk == M - 1) s_lb = ke;
-    });
-  }
-  __syncthreads();
-  const uint64_t lb = s_lb;
-  // candidates: entries at or above the bound; the others feed the log-partition
+  // the row's M-th largest entry; the best M are gathered and ranked among
+  // themselves, every other entry feeds the log-partition (each thread over
+  // its own fixed range of entries)
+  const uint64_t kth = block_kth_key<1>(big, total, M, hist, scan, cand, &red4[0][0], &s_lb);
+  TOPM_STAMP(1, 1);
   float rest2 = 0.0f;
   const int per = (total + kThreads - 1) / kThreads;
   const int e0 = min(total, tid * per), e1 = min(total, e0 + per);
-  int mine_c = 0;
   for (int e = e0; e < e1; ++e) {
     const uint64_t k2 = big[e];
     if (k2 == 0ull) continue;
-    if (k2 >= lb) ++mine_c;
-    else rest2 += expf(key_f32(static_cast<uint32_t>(k2 >> 32)) * invT - gmax);
-  }
-  int at = claim_slots(mine_c, &s_ncand);
-  for (int e = e0; e < e1; ++e) {
-    const uint64_t k2 = big[e];
-    if (k2 != 0ull && k2 >= lb) {
+    if (k2 >= kth) {
+      const int at = atomicAdd(&s_ncand, 1);
       if (at < kMergeCap) cand[at] = k2;
-      ++at;
+    } else {
+      rest2 += expf(key_f32(static_cast<uint32_t>(k2 >> 32)) * invT - gmax);
     }
   }
   __syncthreads();
   const int nc = s_ncand;
-  // exact ranks of the candidates: among themselves, or (many candidates)
-  // against every entry, where entries below the bound never outrank one
-  const bool compact = nc <= kMergeCap;
-  const uint64_t* pool = compact ? cand : big;
-  const int npool = compact ? nc : total;
-  rank_all(pool, npool, [&](int, uint64_t ke, int rk) {
-    if (ke == 0ull || ke < lb) return;
+  TOPM_STAMP(1, 2);
+  rank_all(cand, min(nc, kMergeCap), [&](int, uint64_t ke, int rk) {
     if (rk < M) {
       p.cand_tok[static_cast<size_t>(row) * M + rk] = static_cast<int>(rank_key_id(ke));
       p.cand_base[static_cast<size_t>(row) * M + rk] = key_f32(static_cast<uint32_t>(ke >> 32));
-    } else {
-      const float term = expf(key_f32(static_cast<uint32_t>(ke >> 32)) * invT - gmax);
-      if (compact) s_term[rk] = term;  // rk < nc <= kMergeCap
-      else rest2 += term;              // entry order: already deterministic
     }
   });
-  if (compact) {
-    __syncthreads();
-    for (int i = M + tid; i < nc; i += kThreads) rest2 += s_term[i];
-  }
   for (int s2 = tid; s2 < S; s2 += kThreads) {
     const float ps = p.part_sum[rb + s2];
     if (ps > 0.0f) rest2 += ps * expf(p.part_max[rb + s2] - gmax);
   }
+  TOPM_STAMP(1, 3);
   rest2 = block_sum(rest2, red);
   if (tid == 0) {
     if (nc < M) dt_report(p.status, DT_DEV_BOUNDS);
     p.rest_lse[row] = rest2 > 0.0f ? gmax + logf(rest2) : -INFINITY;
     p.row_done[row] = 0u;  // ready for the next round
   }
+  TOPM_STAMP(1, 4);
 }
 
 }  // namespace
@@ -477,3 +597,18 @@ cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {
 }
 
 }  // namespace dt
+
+#ifdef DT_TOPM_TIMING
+// The Top-M phase stamps of row 0 in the last launch: 2 x 64 x 8 %globaltimer
+// values ([chunk CTAs / merging CTA][split][k]; chunk CTA k: start, after the
+// wait for the previous kernel, after the chunk's statistics, after the rung
+// choice, after the candidate collection, after the ranks, after the arrival;
+// merging CTA k: start, after the bound, after the candidates, after the
+// ranks, end).  Returns the number of values copied, or -1.
+extern "C" int dt_topm_stamps(unsigned long long* out, int n) {
+  const int total = 2 * dt::kTopmStampSplits * dt::kTopmStamps;
+  if (!out || n < total) return -1;
+  return cudaMemcpyFromSymbol(out, dt::g_topm_stamps, sizeof(dt::g_topm_stamps)) == cudaSuccess ? total : -1;
+}
+#endif
+
