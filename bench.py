@@ -64,6 +64,10 @@ def _config_dict(cfg, n_inputs):
     }
 
 
+GEMM_NAME = "k_gemm_tc (LM head + W1_H, tcgen05/TMA)"
+GEMM_NAME_FUSED = "k_gemm_tc + k_topm_merge (LM head + W1_H with the Top-M in the epilogue, tcgen05/TMA; merge)"
+
+
 def algorithmic_bytes(cfg):
     """HBM bytes one launch of the LM-head GEMM and one whole round must move
     (weights read once, gathered rows, hidden states; the roofline numerators).
@@ -265,18 +269,21 @@ def time_two_streams(builder, cfg, wd, Hs, roots, n_rounds):
 
 
 def time_stages(builder, cfg, H, root, stream, n=50):
-    """Each kernel of the round timed alone: the LM-head GEMM (dt_base_logits),
-    Top-M (dt_topm) and the expansion with its Top-B/tree tail
-    (dt_expand_prune), each captured in a CUDA graph of one call and replayed
-    n times between CUDA events on the launching stream."""
+    """The stages of the round timed alone, each captured in a CUDA graph of
+    one call and replayed n times between CUDA events on the launching stream:
+    the LM-head GEMM writing the logits (dt_base_logits); with the Top-M in the
+    GEMM's epilogue, that GEMM and the merge of its lists as a round runs them
+    (dt_base_topm, key lm_head_topm), else the Top-M kernel (dt_topm); and the
+    expansion with its Top-B/tree tail (dt_expand_prune)."""
     import torch
     out = builder.new_tree()
     side = torch.cuda.Stream()
-    calls = {
-        "lm_head": lambda st: builder.base_logits(H, stream=st),
-        "topm": lambda st: builder.topm(stream=st),
-        "chain": lambda st: builder.expand_prune(root, out, stream=st),
-    }
+    calls = {"lm_head": lambda st: builder.base_logits(H, stream=st)}
+    if "epilogue" in builder.plan():
+        calls["lm_head_topm"] = lambda st: builder.base_topm(H, stream=st)
+    else:
+        calls["topm"] = lambda st: builder.topm(stream=st)
+    calls["chain"] = lambda st: builder.expand_prune(root, out, stream=st)
     res = {}
     for name, fn in calls.items():
         side.wait_stream(stream)
@@ -305,17 +312,23 @@ def kernel_rooflines(cfg, us, peak, peak_kind, tpeak, tpeak_kind):
     kb, _ = algorithmic_bytes(cfg)
     ents = []
     gf = gemm_flops(cfg)
-    t = us["lm_head"] * 1e-6
+    fused = "lm_head_topm" in us
+    t = (us["lm_head_topm"] if fused else us["lm_head"]) * 1e-6
     hbm, ten = kb / t / 1e9, gf / t / 1e12
-    ents.append({"kernel": "k_gemm_tc (LM head + W1_H, tcgen05/TMA)", "us_per_launch": us["lm_head"],
-                 "bound": "hbm" if hbm / peak >= ten / tpeak else "tensor",
-                 "algorithmic_bytes_per_launch": kb, "hbm_gbs": hbm, "hbm_frac": hbm / peak,
-                 "algorithmic_flops_per_launch": gf, "tflops": ten, "tensor_frac": ten / tpeak})
-    tb = topm_bytes(cfg)
-    t = us["topm"] * 1e-6
-    ents.append({"kernel": "k_topm (Top-M + rest log-partition over the logits)", "us_per_launch": us["topm"],
-                 "bound": "hbm", "algorithmic_bytes_per_launch": tb, "hbm_gbs": tb / t / 1e9,
-                 "hbm_frac": tb / t / 1e9 / peak})
+    ent = {"kernel": GEMM_NAME_FUSED if fused else GEMM_NAME, "us_per_launch": t * 1e6,
+           "bound": "hbm" if hbm / peak >= ten / tpeak else "tensor",
+           "algorithmic_bytes_per_launch": kb, "hbm_gbs": hbm, "hbm_frac": hbm / peak,
+           "algorithmic_flops_per_launch": gf, "tflops": ten, "tensor_frac": ten / tpeak}
+    if fused:
+        ent["note"] = ("the LM-head GEMM with the Top-M in its epilogue and the merge kernel, timed together as "
+                       "a round runs them; the GEMM alone, writing the logits: %.1f us" % us["lm_head"])
+    ents.append(ent)
+    if not fused:
+        tb = topm_bytes(cfg)
+        t = us["topm"] * 1e-6
+        ents.append({"kernel": "k_topm (Top-M + rest log-partition over the logits)", "us_per_launch": us["topm"],
+                     "bound": "hbm", "algorithmic_bytes_per_launch": tb, "hbm_gbs": tb / t / 1e9,
+                     "hbm_frac": tb / t / 1e9 / peak})
     cb, cf = chain_bytes(cfg), chain_flops(cfg)
     t = us["chain"] * 1e-6
     ents.append({"kernel": "depth chain (all depths + Top-B + tree/mask)", "us_per_launch": us["chain"],
@@ -480,7 +493,7 @@ def bench_gpu(args):
         lat.append(a.elapsed_time(b) * 1e3)
     # every kernel of the round timed alone (graph replays, events on the stream)
     stage_us = time_stages(builder, cfg, Hs[0], roots[0], stream, n=max(20, min(args.steps, 100)))
-    lm_ms = stage_us["lm_head"] / 1e3
+    lm_ms = stage_us.get("lm_head_topm", stage_us["lm_head"]) / 1e3
     peak, peak_kind = _peaks()
     walk = time_accept_walk(builder, cfg, outs, stream, peak) if not args.no_walk else None
     thr = time_two_streams(builder, cfg, wd, Hs, roots, max(10, min(args.steps, 200))) \
@@ -523,6 +536,7 @@ def bench_gpu(args):
             traffic = None
     us_round = 1e6 * elapsed / args.steps
     top = kernels[0]
+    gname = GEMM_NAME_FUSED if "lm_head_topm" in stage_us else GEMM_NAME
     if top["kernel"].startswith("k_gemm_tc"):
         roofline = None  # filled below (the GEMM's own object, with its ncu traffic)
     else:
@@ -546,13 +560,13 @@ def bench_gpu(args):
         "kernels": kernels,
         "create": {"ms": create_ms, "gru_input_table_bytes": cfg.V * 3 * cfg.g * 4,
                    "note": "dt_create: workspace + GRU input table X = E W_ih^T + b_ih (one tcgen05 GEMM)"},
-        "roofline": roofline if roofline is not None else ({"bound": "hbm", "kernel": "k_gemm_tc (LM head + W1_H, tcgen05/TMA)",
+        "roofline": roofline if roofline is not None else ({"bound": "hbm", "kernel": gname,
                       "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                       "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
                       "algorithmic_bytes_per_launch": kbytes, "avg_launch_us": lm_ms * 1e3,
                       "tensor_frac": tflops / tpeak}
                      if achieved / peak >= tflops / tpeak else
-                     {"bound": "tensor", "kernel": "k_gemm_tc (LM head + W1_H, tcgen05/TMA)",
+                     {"bound": "tensor", "kernel": gname,
                       "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
                       "peak_source": f"{tpeak_kind} bf16_tflops (burst)", "traffic": traffic,
                       "algorithmic_flops_per_launch": gemm_flops(cfg), "avg_launch_us": lm_ms * 1e3,
@@ -593,7 +607,7 @@ def bench_gpu(args):
 def _kernel_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "common.cuh"):
+    for f in ("gemm_tc.cu", "common.cuh", "topm_fused.cuh"):
         with open(os.path.join(ROOT, "conditional_draft_tree_lm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

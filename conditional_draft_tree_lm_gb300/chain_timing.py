@@ -49,7 +49,7 @@ def main():
     from .build import LIB_DIR, build_library
     from workloads import get_config, make_round_inputs, make_weights
 
-    path = build_library(force=True, extra_flags=["-DDT_DCHAIN_TIMING", "-DDT_TOPM_TIMING"],
+    path = build_library(force=True, extra_flags=["-DDT_DCHAIN_TIMING", "-DDT_TOPM_TIMING", "-DDT_GEMM_TIMING"],
                          lib_path=os.path.join(LIB_DIR, "libdtree_timing.so"))
     dtree._lib = None
     lib = dtree.load_library(path)
@@ -60,6 +60,8 @@ def main():
     lib.dt_dchain_xstamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
     lib.dt_topm_stamps.restype = ctypes.c_int
     lib.dt_topm_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.dt_gemm_stamps.restype = ctypes.c_int
+    lib.dt_gemm_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
 
     torch.cuda.set_device(0)
     cfg = get_config(args.workload)
@@ -73,7 +75,8 @@ def main():
     buf = np.zeros(2 * SLOTS * NPH, dtype=np.uint64)
     xbuf = np.zeros(2 * SLOTS * XCTAS, dtype=np.uint64)
     tbuf = np.zeros(2 * 64 * 16, dtype=np.uint64)
-    acc, xacc, tacc = [], [], []
+    gbuf = np.zeros(17 * 8, dtype=np.uint64)
+    acc, xacc, tacc, gacc = [], [], [], []
     for s in range(args.rounds + 3):
         H, r = make_round_inputs(cfg, s)
         Hd = dtree.bf16_tensor(H)
@@ -87,10 +90,13 @@ def main():
             raise SystemExit("dt_dchain_xstamps failed")
         if lib.dt_topm_stamps(tbuf.ctypes.data, tbuf.size) != tbuf.size:
             raise SystemExit("dt_topm_stamps failed")
+        if lib.dt_gemm_stamps(gbuf.ctypes.data, gbuf.size) != gbuf.size:
+            raise SystemExit("dt_gemm_stamps failed")
         if s >= 3:
             acc.append(buf.reshape(2, SLOTS, NPH).astype(np.int64).copy())
             xacc.append(xbuf.reshape(2, SLOTS, XCTAS).astype(np.int64).copy())
             tacc.append(tbuf.reshape(2, 64, 16).astype(np.int64).copy())
+            gacc.append(gbuf.reshape(17, 8).astype(np.int64).copy())
     st = np.stack(acc)  # [rounds, cta, slot, phase]
     if args.save:
         np.save(args.save, st)
@@ -139,13 +145,35 @@ def main():
               f"X: staging {sub(0, 16):.0f}, poll {sub(16, 17):.0f}, barrier + copies {sub(17, 1):.0f}")
     exchange_report(np.stack(xacc), D, b.plan())
     topm_report(np.stack(tacc))
+    gemm_report(np.stack(gacc), 1.0 / mhz)
     b.close()
+
+
+def gemm_report(gs, us):
+    """CTA 0 of the LM-head GEMM, tile by tile (us from the MMA warp's first tile)."""
+    g = gs.mean(axis=0)
+    t0 = g[0, 0]
+    n = int((gs[0, :16, 1] > 0).sum())
+    print(f"\nLM-head GEMM, CTA 0 ({n} tiles; us from its first MMA, mean over rounds)")
+    print("tile   MMA start   MMA end   epilogue has it   appended    ranked   epilogue done")
+    for t in range(n):
+        print(f"{t:4d}  {(g[t, 0] - t0) * us:9.2f}  {(g[t, 1] - t0) * us:8.2f}  {(g[t, 2] - t0) * us:16.2f}  "
+              f"{(g[t, 4] - t0) * us:9.2f}  {(g[t, 5] - t0) * us:8.2f}  {(g[t, 3] - t0) * us:14.2f}")
+    print(f"final pass: sums reduced {(g[16, 3] - t0) * us:.2f}, epilogue end {(g[16, 0] - t0) * us:.2f}")
 
 
 def topm_report(ts):
     """Top-M of row 0 by the global timer: the chunk CTAs' phases and the merge."""
     part, mrg = ts[:, 0], ts[:, 1, 0]  # [rounds, split, k], [rounds, k]
     S = int((part[0, :, 1] > 0).sum())
+    m = lambda a, b: (mrg[:, b] - mrg[:, a]).mean()
+    if S == 0:
+        # the Top-M ran in the LM-head GEMM's epilogue: only the merge kernel
+        print("\nTop-M in the LM-head GEMM's epilogue; the merge kernel, row 0 (ns, mean over rounds): "
+              f"entries + range {m(0, 10):.0f}, histogram {m(10, 11):.0f}, bin {m(11, 12):.0f}, "
+              f"gather {m(12, 13):.0f}, rank {m(13, 14):.0f}, winners {m(1, 2):.0f}, their ranks {m(2, 3):.0f}, "
+              f"rest + writes {m(3, 4):.0f}; total {m(0, 4):.0f}")
+        return
     part = part[:, :S]
     t1 = part[:, :, 1].min(axis=1)  # the earliest chunk CTA past the wait
     d = lambda a, b: (part[:, :, b] - part[:, :, a]).mean()
@@ -156,7 +184,6 @@ def topm_report(ts):
     print(f"chunk CTAs past the wait: last {(part[:, :, 1] - t1[:, None]).max(axis=1).mean():.0f} ns after the first; "
           f"arrivals: first {(part[:, :, 6].min(axis=1) - t1).mean():.0f}, last "
           f"{(part[:, :, 6].max(axis=1) - t1).mean():.0f}")
-    m = lambda a, b: (mrg[:, b] - mrg[:, a]).mean()
     print(f"merge: starts {(mrg[:, 0] - t1).mean():.0f}; entries + range {m(0, 10):.0f}, histogram {m(10, 11):.0f}, "
           f"bin {m(11, 12):.0f}, gather {m(12, 13):.0f}, rank {m(13, 14):.0f}, winners {m(1, 2):.0f}, "
           f"their ranks {m(2, 3):.0f}, rest + writes {m(3, 4):.0f}; ends {(mrg[:, 4] - t1).mean():.0f}")

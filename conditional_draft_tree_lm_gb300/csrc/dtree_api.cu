@@ -38,7 +38,7 @@ bool make_tables(const dt_config& c, Tables& t) {
 
 dt_status check(const dt_config* c) {
   if (!c) return DT_ERR_INVALID_ARG;
-  if ((c->flags & ~(DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST)) != 0) return DT_ERR_INVALID_ARG;
+  if ((c->flags & ~(DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST | DT_FLAG_SEPARATE_TOPM)) != 0) return DT_ERR_INVALID_ARG;
   if ((c->flags & DT_FLAG_BEST_FIRST) && c->n_req != 1) return DT_ERR_SHAPE;
   if (c->d <= 0 || c->V <= 0 || c->g <= 0 || c->r <= 0 || c->M <= 0 || c->K <= 0 || c->W <= 0 ||
       c->B <= 0 || c->n_req <= 0 || c->block < 2)
@@ -63,6 +63,7 @@ dt_status check(const dt_config* c) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
+  size_t fpart_id, fpart_val, fpart_max, fpart_sum, fpart_cnt, fpart_tail;
   size_t logits, h1, part_id, part_val, part_max, part_sum, part_cnt, part_kth, cand_tok, cand_base, rest_lse,
       row_done, S, sfrag, zfrag,
       uW1, live, node_tok, node_parent, node_logp, node_score, sel, bar, status, H_dev, root_dev,
@@ -70,7 +71,9 @@ struct Layout {
   size_t xtab;
 };
 
-void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L) {
+// fs: the partial lists per row of the fused Top-M (the LM-head GEMM's grid),
+// or 0 when the rounds do not fuse it.
+void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L, int fs) {
   const size_t rows = static_cast<size_t>(c.n_req) * t.D;
   const size_t N1 = static_cast<size_t>(t.N) + 1;
   const size_t S1 = static_cast<size_t>(c.B) + 1;
@@ -116,6 +119,12 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   put(L.out_mask, c.n_req * S1 * S1);
   put(L.acc_key, c.n_req * S1 * 8);
   put(L.acc_done, static_cast<size_t>(c.n_req) * 8);
+  put(L.fpart_id, rows * fs * c.M * 4);
+  put(L.fpart_val, rows * fs * c.M * 4);
+  put(L.fpart_max, rows * fs * 4);
+  put(L.fpart_sum, rows * fs * 4);
+  put(L.fpart_cnt, rows * fs * 4);
+  put(L.fpart_tail, rows * fs * c.M * 4);
   L.total = o;
   L.xtab = static_cast<size_t>(c.V) * 3 * c.g * 4;
 }
@@ -144,6 +153,8 @@ struct dt_ctx {
   float* xtab = nullptr;
   CUtensorMap tm_lm, tm_w1h;
   TopmParams topm;
+  int fuse_topm = 0;  // rounds keep the Top-M in the LM-head GEMM's epilogue
+  TopmParams fmerge;  // the merge of the GEMM CTAs' lists
   AcceptParams acc;
   BestParams best;
   int best_first = 0;
@@ -151,7 +162,7 @@ struct dt_ctx {
   int use_dchain = 0;  // one request: the clustered depth chain (dchain.cu)
   int dchain_cs = 0;
   int dchain_jc = 0;
-  char plan[256] = "";  // which kernels a round runs (dt_plan_string)
+  char plan[384] = "";  // which kernels a round runs (dt_plan_string)
   const float* logits_src = nullptr;
   int next_depth = 1;
   cudaStream_t cap_stream = nullptr;
@@ -186,13 +197,9 @@ dt_status cuda_status(cudaError_t e, const char* what = "") {
     if (_e != cudaSuccess) return cuda_status(_e, #x); \
   } while (0)
 
-dt_status enqueue_base_logits(dt_ctx* c, const void* H, float* logits, cudaStream_t st) {
-  const dt_config& k = c->cfg;
+// The launch shape of the LM-head GEMM over one round's H rows (no pointers).
+GemmParams logits_gemm_params(const dt_config& k, const Tables& t) {
   const int BN = logits_bn(k);
-  CUtensorMap tm_h;
-  if (!make_tmap_bf16_2d(&tm_h, H, k.d, static_cast<uint64_t>(k.n_req) * k.block,
-                         static_cast<uint64_t>(k.d) * 2, BN > 256 ? 256 : BN))
-    return DT_ERR_INVALID_ARG;
   GemmParams p = {};
   p.mode = GEMM_LOGITS;
   p.K = k.d;
@@ -204,11 +211,37 @@ dt_status enqueue_base_logits(dt_ctx* c, const void* H, float* logits, cudaStrea
   p.rows_a = k.V;
   p.rows_a2 = k.r;
   p.block = k.block;
-  p.D = c->t.D;
-  p.logits = logits;
+  p.D = t.D;
+  gemm_plan(p, BN);
+  p.ft_P = t.D;
+  p.ft_M = k.M;
+  p.ft_invT = 1.0f / k.T;
+  return p;
+}
+
+// fused: the Top-M runs in the epilogue (dt_ctx::fuse_topm) and the logits
+// are not written (logits may be null).
+dt_status enqueue_base_logits(dt_ctx* c, const void* H, float* logits, cudaStream_t st, bool fused = false) {
+  const dt_config& k = c->cfg;
+  const int BN = logits_bn(k);
+  CUtensorMap tm_h;
+  if (!make_tmap_bf16_2d(&tm_h, H, k.d, static_cast<uint64_t>(k.n_req) * k.block,
+                         static_cast<uint64_t>(k.d) * 2, BN > 256 ? 256 : BN))
+    return DT_ERR_INVALID_ARG;
+  GemmParams p = logits_gemm_params(k, c->t);
+  p.logits = fused ? nullptr : logits;
   p.h1 = c->at<float>(c->lay.h1);
   p.status = c->at<int>(c->lay.status);
-  gemm_plan(p, BN);
+  if (fused) {
+    gemm_ft_plan(p);
+    p.part_id = c->fmerge.part_id;
+    p.part_val = c->fmerge.part_val;
+    p.part_max = c->fmerge.part_max;
+    p.part_sum = c->fmerge.part_sum;
+    p.part_cnt = c->fmerge.part_cnt;
+    p.part_kth = nullptr;
+    p.part_tail = c->fmerge.part_tail;
+  }
   DT_TRY(launch_gemm_tc(c->tm_lm, c->tm_w1h, tm_h, p, c->num_sms, st));
   return DT_OK;
 }
@@ -426,15 +459,32 @@ dt_status enqueue_build(dt_ctx* c, const int32_t* root, int32_t* tok, int32_t* p
   return DT_OK;
 }
 
-dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* tok, int32_t* parent,
-                        int32_t* depth, float* logp_cum, uint8_t* mask, cudaStream_t st) {
+// The LM-head GEMM and the Top-M of a round: the GEMM with the Top-M in its
+// epilogue and the merge of its CTAs' lists, or the GEMM and the Top-M kernel.
+// The second kernel launches as a programmatic dependent (it waits for the
+// GEMM's end before reading its results) and clears `clear` (the grid-barrier
+// chain's counter) when not null.
+dt_status enqueue_base_topm(dt_ctx* c, const void* H, cudaStream_t st, unsigned* clear) {
+  if (c->fuse_topm) {
+    dt_status s = enqueue_base_logits(c, H, nullptr, st, true);
+    if (s != DT_OK) return s;
+    TopmParams mp = c->fmerge;
+    mp.clear_word = clear;
+    mp.pdl = 1;
+    DT_TRY(launch_topm_merge(mp, st));
+    return DT_OK;
+  }
   float* logits = c->at<float>(c->lay.logits);
   dt_status s = enqueue_base_logits(c, H, logits, st);
   if (s != DT_OK) return s;
-  // Top-M and the chain launch as programmatic dependents (each waits for its
-  // predecessor's end before reading its results); Top-M also clears the
-  // chain's barrier counter, so the round needs no memset
-  s = enqueue_topm(c, logits, st, c->at<unsigned>(c->lay.bar), 1);
+  return enqueue_topm(c, logits, st, clear, 1);
+}
+
+dt_status enqueue_round(dt_ctx* c, const void* H, const int32_t* root, int32_t* tok, int32_t* parent,
+                        int32_t* depth, float* logp_cum, uint8_t* mask, cudaStream_t st) {
+  // the chain launches as a programmatic dependent of the Top-M stage, whose
+  // second kernel clears the chain's barrier counter: no memset in a round
+  dt_status s = enqueue_base_topm(c, H, st, c->at<unsigned>(c->lay.bar));
   if (s != DT_OK) return s;
   return enqueue_build(c, root, tok, parent, depth, logp_cum, mask, st, true);
 }
@@ -462,7 +512,7 @@ size_t dt_workspace_bytes(const dt_config* cfg) {
   tp.M = cfg->M;
   topm_plan(tp, 1 << 20);  // the most chunks any SM count can plan: an upper bound
   Layout L;
-  layout(*cfg, t, tp, L);
+  layout(*cfg, t, tp, L, cfg->n_req == 1 ? 1024 : 0);  // fused lists: up to 1024 GEMM CTAs
   return L.total + L.xtab;
 }
 
@@ -534,7 +584,19 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->acc.V = cfg->V;
   c->acc.D = c->t.D;
   accept_plan(c->acc, c->num_sms);
-  layout(*cfg, c->t, c->topm, c->lay);
+  // the Top-M in the LM-head GEMM's epilogue: one request, and the GEMM and
+  // the merge support the shape
+  int fs = 0;
+  if (cfg->n_req == 1 && !(cfg->flags & DT_FLAG_SEPARATE_TOPM)) {
+    const GemmParams gp = logits_gemm_params(*cfg, c->t);
+    if (gemm_ft_supported(gp, c->num_sms)) {
+      TopmParams mp = c->topm;
+      mp.S = gemm_grid(gp, c->num_sms);
+      if (!topm_merge_unsupported(mp)) fs = mp.S;
+    }
+  }
+  c->fuse_topm = fs > 0 ? 1 : 0;
+  layout(*cfg, c->t, c->topm, c->lay, fs);
   // host-side fault injection: DT_FAULT_INJECT_ALLOC set in the environment
   // makes the workspace allocation fail as an out-of-memory would
   e = getenv("DT_FAULT_INJECT_ALLOC") ? cudaErrorMemoryAllocation : cudaMalloc(&c->ws, c->lay.total);
@@ -556,6 +618,16 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   c->topm.rest_lse = c->at<float>(c->lay.rest_lse);
   c->topm.row_done = c->at<unsigned>(c->lay.row_done);
   c->topm.status = c->at<int>(c->lay.status);
+  c->fmerge = c->topm;
+  c->fmerge.S = fs;
+  c->fmerge.part_id = c->at<int>(c->lay.fpart_id);
+  c->fmerge.part_val = c->at<float>(c->lay.fpart_val);
+  c->fmerge.part_max = c->at<float>(c->lay.fpart_max);
+  c->fmerge.part_sum = c->at<float>(c->lay.fpart_sum);
+  c->fmerge.part_cnt = c->at<int>(c->lay.fpart_cnt);
+  c->fmerge.part_kth = nullptr;
+  c->fmerge.part_tail = c->at<float>(c->lay.fpart_tail);
+  c->fmerge.row_done = nullptr;
   c->logits_src = c->at<float>(c->lay.logits);
   c->acc.rowkey = c->at<uint64_t>(c->lay.acc_key);
   c->acc.req_done = c->at<uint64_t>(c->lay.acc_done);
@@ -613,12 +685,17 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   } else {
     snprintf(why, sizeof(why), "%s", cfg->n_req != 1 ? "several requests" : "marginal or best-first mode");
   }
-  if (c->best_first)
-    snprintf(c->plan, sizeof(c->plan), "best-first builder on %d CTAs", c->chain_grid);
-  else if (c->use_dchain)
-    snprintf(c->plan, sizeof(c->plan), "clustered depth chain on %d CTAs: %s", cfg->g / c->dchain_jc, why);
+  char tm[96];
+  if (c->fuse_topm)
+    snprintf(tm, sizeof(tm), "Top-M in the LM-head GEMM's epilogue (%d CTA lists merged); ", c->fmerge.S);
   else
-    snprintf(c->plan, sizeof(c->plan), "grid-barrier depth chain on %d CTAs (clustered chain not used: %s)",
+    snprintf(tm, sizeof(tm), "Top-M kernel on %d chunks per row; ", c->topm.S);
+  if (c->best_first)
+    snprintf(c->plan, sizeof(c->plan), "%sbest-first builder on %d CTAs", tm, c->chain_grid);
+  else if (c->use_dchain)
+    snprintf(c->plan, sizeof(c->plan), "%sclustered depth chain on %d CTAs: %s", tm, cfg->g / c->dchain_jc, why);
+  else
+    snprintf(c->plan, sizeof(c->plan), "%sgrid-barrier depth chain on %d CTAs (clustered chain not used: %s)", tm,
              c->chain_grid, why);
 
   // tensor maps of the weights
@@ -688,6 +765,21 @@ dt_status dt_topm(dt_ctx* c, const float* logits, int32_t* cand_tok, float* cand
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   dt_status s = enqueue_topm(c, logits ? logits : c->logits_src, st);
   if (s != DT_OK) return s;
+  return dt_last_candidates(c, cand_tok, cand_base, rest_lse, stream);
+}
+
+dt_status dt_base_topm(dt_ctx* c, const void* H, void* stream) {
+  if (!c || !H) return DT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(H) & 15u) != 0) return DT_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  dt_status s = enqueue_base_topm(c, H, st, nullptr);
+  if (s == DT_OK) c->last_stream = st;
+  return s;
+}
+
+dt_status dt_last_candidates(dt_ctx* c, int32_t* cand_tok, float* cand_base, float* rest_lse, void* stream) {
+  if (!c) return DT_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rows = static_cast<size_t>(c->cfg.n_req) * c->t.D;
   if (cand_tok)
     DT_TRY(cudaMemcpyAsync(cand_tok, c->topm.cand_tok, rows * c->cfg.M * 4, cudaMemcpyDeviceToDevice, st));
@@ -887,6 +979,7 @@ dt_status dt_get_device_status(dt_ctx* c) {
 int dt_round_kernel_count(const dt_ctx* c) {
   if (!c) return -1;
   if (c->best_first) return 3;  // LM head GEMM, Top-M, best-first builder (tree and mask in its tail)
+  // (the merge of the GEMM's Top-M lists takes the Top-M kernel's place when it is fused)
   if (c->use_dchain) return 3;  // LM head GEMM, Top-M, clustered chain (Top-B and tree/mask in its tail)
   // LM head GEMM, Top-M, depth chain (+ Top-B, tree/mask unless the chain's tail does them)
   ChainParams cp = chain_params(const_cast<dt_ctx*>(c), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);

@@ -9,6 +9,9 @@
 //    M dimension is 128 vocabulary rows and its N dimension the few H rows; the
 //    kernel is bound by streaming A from HBM.  The epilogue scatters columns of
 //    block position i >= 1 to logits[q, i-1, v] (or h1[q, i-1, j]).
+//    With ft set (one request), the epilogue also keeps each CTA's exact
+//    Top-M of the logit rows as they stream by (topm_fused.cuh) and the
+//    logits need not be written at all.
 //  * the GRU input table (create time): A = E [V, d], B = W_ih [3g, d],
 //    D + b_ih -> X [V, 3g] fp32.
 //
@@ -25,18 +28,54 @@
 #include "kernels.h"
 
 namespace dt {
+// Tile stamps (built with -DDT_GEMM_TIMING only): clock64() of CTA 0 for its
+// first 16 tiles: [tile][0] the MMA warp starts the tile, [1] it commits the
+// tile, [2] the epilogue (warp 2, lane 0) has the accumulator, [3] the
+// epilogue is done with the tile, [4] / [5] inside the fused Top-M update;
+// [16][0] the epilogue's end, [16][3] the fused Top-M's sums reduced.
+#ifdef DT_GEMM_TIMING
+__device__ unsigned long long g_gemm_stamps[17][8];
+#define GEMM_STAMP(t, k)                                                                   \
+  do {                                                                                     \
+    if (blockIdx.x == 0 && (t) < 17) g_gemm_stamps[t][k] = static_cast<unsigned long long>(clock64()); \
+  } while (0)
+#else
+#define GEMM_STAMP(t, k) \
+  do {                   \
+  } while (0)
+#endif
+// (the fused Top-M's inner stamps, by warp 2 lane 0)
+#ifdef DT_GEMM_TIMING
+#define FT_STAMP(t, k)                    \
+  do {                                    \
+    if (threadIdx.x == 64) GEMM_STAMP(t, k); \
+  } while (0)
+#endif
+}  // namespace dt
+
+#include "topm_fused.cuh"
+
+namespace dt {
 
 namespace {
 
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = 128 * 128;  // 128 rows x 64 bf16
 
+
+// Byte offset of the fused Top-M area from the 1024-aligned shared base: after
+// the stages, the barriers and the tensor-memory slot.
+DT_HOST_DEVICE_INLINE size_t gemm_ft_offset(const GemmParams& p) {
+  return (static_cast<size_t>(p.stages) * p.stage_bytes + (2 * p.stages + 4) * 8 + 16 + 15) & ~static_cast<size_t>(15);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a2,
               const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // (offset from the shared array itself, so that accesses through smem stay
+  // shared-memory instructions rather than generic ones)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
   uint64_t* empty = full + p.stages;
   uint64_t* tfull = empty + p.stages;
@@ -101,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t use = p.acc_bufs == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
         if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, p.status)) break;
         tc_fence_after();
+        GEMM_STAMP(local, 0);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.status)) { ok = false; break; }
@@ -127,21 +167,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == static_cast<uint32_t>(p.stages)) { stage = 0; phase ^= 1u; }
         }
         if (ok) tc_commit(&tfull[acc]);
+        GEMM_STAMP(local, 1);
       }
     }
   } else {
     // epilogue: warps 2..5; TMEM lanes [32*(warp%4), +32)
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    const bool ft = p.ft != 0;
+    FtState fs;
+    FtSums fsum;
+    int ft_tiles = 0;
+    if (ft) {
+      fs = ft_state(smem + gemm_ft_offset(p), p.ft_P);
+      ft_init(fs, fsum, p.ft_P, row_in_tile);
+    }
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       const int acc = p.acc_bufs == 2 ? (local & 1) : 0;
       const uint32_t use = p.acc_bufs == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
-      if (!mbar_wait(&tfull[acc], use & 1u, p.status)) break;
+      const bool got = mbar_wait(&tfull[acc], use & 1u, p.status);
+      if (ft ? !ft_all(got) : !got) break;
       tc_fence_after();
+      if (warp == 2 && lane == 0) GEMM_STAMP(local, 2);
       const int mt = tile / p.n_tiles, nt = tile % p.n_tiles;
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * p.BN);
+      if (ft && mt < p.m_tiles_a) {
+        // one 16-column tile: read it, give the accumulator back at once, then
+        // the logits (if wanted) and the running Top-M
+        uint32_t v[16];
+        tmem_ld16(tbase, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        const int row = mt * 128 + row_in_tile;
+        const bool valid = row < p.rows_a;
+        if (p.logits && valid) {
+#pragma unroll
+          for (int j = 1; j < 16; ++j)
+            if (j < p.n_valid) p.logits[static_cast<size_t>(j - 1) * p.rows_a + row] = __uint_as_float(v[j]);
+        }
+        ft_tile(fs, fsum, v, p.ft_P, p.ft_M, p.ft_invT, row, valid, row_in_tile, ft_tiles);
+        ++ft_tiles;
+        if (warp == 2 && lane == 0) GEMM_STAMP(local, 3);
+        continue;
+      }
       if (p.mode == GEMM_LOGITS) {
         const bool second = mt >= p.m_tiles_a;
         const int row = (second ? mt - p.m_tiles_a : mt) * 128 + row_in_tile;
@@ -191,6 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
+    if (ft) {
+      ft_finish(fs, fsum, p.ft_P, p.ft_M, p.ft_invT, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                row_in_tile, p.part_id, p.part_val, p.part_max, p.part_sum, p.part_cnt, p.part_kth, p.part_tail);
+    }
+    if (warp == 2 && lane == 0) GEMM_STAMP(16, 0);
   }
 
   tc_fence_before();
@@ -250,7 +326,28 @@ void gemm_plan(GemmParams& p, int BN) {
 }
 
 size_t gemm_smem_bytes(const GemmParams& p) {
+  if (p.ft) return 1024 + gemm_ft_offset(p) + ft_layout(p.ft_P).total;
   return 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (2 * p.stages + 4) * 8 + 16;
+}
+
+int gemm_grid(const GemmParams& p, int num_sms) {
+  const int tiles = (p.m_tiles_a + p.m_tiles_a2) * p.n_tiles;
+  return tiles < num_sms ? tiles : num_sms;
+}
+
+bool gemm_ft_supported(const GemmParams& p, int num_sms) {
+  if (p.mode != GEMM_LOGITS || p.n_tiles != 1 || p.BN != 16 || p.n_valid > 16) return false;
+  if (p.ft_P < 1 || p.ft_P > kFtMaxRows || p.ft_P > p.n_valid - 1) return false;
+  if (p.ft_M < 1 || p.ft_M > kFtMaxM) return false;
+  GemmParams q = p;
+  q.ft = 1;
+  gemm_ft_plan(q);
+  return q.stages >= 4 && gemm_smem_bytes(q) <= 227 * 1024;
+}
+
+void gemm_ft_plan(GemmParams& p) {
+  p.ft = 1;
+  while (p.stages > 2 && gemm_smem_bytes(p) > 227 * 1024) --p.stages;
 }
 
 cudaError_t gemm_prepare() {
@@ -261,10 +358,19 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_a2, co
                            const GemmParams& p, int num_sms, cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  const int tiles = (p.m_tiles_a + p.m_tiles_a2) * p.n_tiles;
-  const int grid = tiles < num_sms ? tiles : num_sms;
+  if (p.ft && !gemm_ft_supported(p, num_sms)) return cudaErrorInvalidValue;
+  const int grid = gemm_grid(p, num_sms);
   k_gemm_tc<<<grid, kThreads, smem, stream>>>(tm_a, tm_a2, tm_b, p);
   return cudaGetLastError();
 }
 
 }  // namespace dt
+
+#ifdef DT_GEMM_TIMING
+// The GEMM tile stamps of the last launch (17 x 8 clock64 values, layout as
+// above).  Returns the number of values copied, or -1.
+extern "C" int dt_gemm_stamps(unsigned long long* out, int n) {
+  if (!out || n < 17 * 8) return -1;
+  return cudaMemcpyFromSymbol(out, dt::g_gemm_stamps, sizeof(dt::g_gemm_stamps)) == cudaSuccess ? 17 * 8 : -1;
+}
+#endif

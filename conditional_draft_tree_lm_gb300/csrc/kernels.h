@@ -36,12 +36,33 @@ struct GemmParams {
   int ldo;
   const uint16_t* bias;
   int* status;
+  // logits mode with the Top-M in the epilogue (topm_fused.cuh): each CTA
+  // reports the sorted M best of its vocabulary rows for the ft_P logit rows
+  // into the partial lists (S = the grid), and logits may be null
+  int ft;
+  int ft_P, ft_M;
+  float ft_invT;
+  int* part_id;     // [ft_P, S, M]
+  float* part_val;  // [ft_P, S, M]
+  float* part_max;  // [ft_P, S]
+  float* part_sum;  // [ft_P, S]
+  int* part_cnt;    // [ft_P, S]
+  float* part_kth;  // [ft_P, S] or null
+  float* part_tail; // [ft_P, S, M]: sum over the list's entries j.. of exp(logit/T - part_max)
 };
 
 bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_bytes, uint32_t box_rows);
 void gemm_plan(GemmParams& p, int BN);
 size_t gemm_smem_bytes(const GemmParams& p);
+// The grid of a launch (one persistent CTA per SM at most).
+int gemm_grid(const GemmParams& p, int num_sms);
+// Whether the Top-M can run in the epilogue of this logits launch (one N tile
+// of at most 16 columns, ft_P <= 16 rows, M <= 64, and the shared memory for
+// it next to at least four pipeline stages); gemm_plan has been applied.
+bool gemm_ft_supported(const GemmParams& p, int num_sms);
+// Switches the planned launch to the fused Top-M (fewer stages to make room).
+void gemm_ft_plan(GemmParams& p);
 cudaError_t gemm_prepare();
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_a2, const CUtensorMap& tm_b,
                            const GemmParams& p, int num_sms, cudaStream_t stream);
@@ -57,6 +78,9 @@ struct TopmParams {
   float* part_sum;  // [rows, S]   sum over the chunk's non-candidates of exp(logit/T - max)
   int* part_cnt;    // [rows, S]
   float* part_kth;  // [rows, S]   the chunk's M-th largest logit (-inf if it has <= M)
+  // [rows, S, M] or null: part_tail[j] = sum over the list's entries j, j+1,
+  // ... of exp(logit/T - part_max); with it a merge reads only the lists' heads
+  float* part_tail;
   int* cand_tok;    // [rows, M]
   float* cand_base; // [rows, M]
   float* rest_lse;  // [rows]
@@ -74,6 +98,12 @@ cudaError_t topm_prepare();
 // or a merge beyond the kernel's capacity), or null when it can.
 const char* topm_unsupported(const TopmParams& p);
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream);
+// The merge of partial lists written by another kernel (S lists of M per row,
+// part_* arrays as above), one CTA per row; launch_topm_merge returns
+// cudaErrorInvalidValue when topm_merge_unsupported says why not.
+size_t topm_merge_only_smem(const TopmParams& p);
+const char* topm_merge_unsupported(const TopmParams& p);
+cudaError_t launch_topm_merge(const TopmParams& p, cudaStream_t stream);
 
 // Text returned by dt_last_error() on the calling thread.
 void set_last_error(const char* msg);

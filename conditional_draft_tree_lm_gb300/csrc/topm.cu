@@ -26,6 +26,8 @@
 // histogram, the M best ranked among themselves, and
 //   rest_lse = log( sum_chunks part_sum e^{part_max} + sum_{losing entries} e^{logit/T} ),
 // so every non-candidate token enters the log-partition exactly once.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "select.cuh"
@@ -51,10 +53,13 @@ constexpr int kMergeCap = 2048;       // merge candidates ranked among themselve
 constexpr int kTopmStampSplits = 64;
 constexpr int kTopmStamps = 16;
 __device__ unsigned long long g_topm_stamps[2][kTopmStampSplits][kTopmStamps];
-#define TOPM_STAMP(which, k)                                                                        \
-  do {                                                                                             \
-    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.x < kTopmStampSplits)                      \
-      g_topm_stamps[which][(which) ? 0 : blockIdx.x][k] = dt_globaltimer();                         \
+// which 1 in the merge-only kernel (grid = rows): row 0 is CTA 0
+#define TOPM_STAMP(which, k)                                                                      \
+  do {                                                                                           \
+    if (threadIdx.x == 0 &&                                                                      \
+        ((which) ? (gridDim.y == 1 ? blockIdx.x == 0 : blockIdx.y == 0)                          \
+                 : (blockIdx.y == 0 && blockIdx.x < kTopmStampSplits)))                          \
+      g_topm_stamps[which][(which) ? 0 : blockIdx.x][k] = dt_globaltimer();                       \
   } while (0)
 #else
 #define TOPM_STAMP(which, k) \
@@ -233,6 +238,183 @@ DT_DEVINL uint64_t block_kth_key(const uint64_t* keys, int n, int m, uint32_t* h
   __syncthreads();
   TOPM_STAMP(kWhich, 14);
   return *s_key;
+}
+
+// Shared memory a row merge works in.
+struct MergeSmem {
+  uint32_t* hist;  // 256 words
+  int* scan;       // 4 ints
+  float* red;      // kWarps + 1 floats
+  float* red4;     // 2 kWarps floats
+  uint64_t* s_lb;  // one key
+  int* s_ncand;
+  uint64_t* big;   // S * M entries
+  uint64_t* cand;  // kMergeCap keys
+};
+
+DT_DEVINL float block_max(float v, float* red) {
+  v = warp_max(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float s = threadIdx.x < kWarps ? red[threadIdx.x] : -INFINITY;
+    s = warp_max(s);
+    if (threadIdx.x == 0) red[kWarps] = s;
+  }
+  __syncthreads();
+  return red[kWarps];
+}
+
+// The merge when every list carries its suffix sums (part_tail): only the
+// lists' heads are read.  The M-th largest of the first t entries of every
+// list (S t >= M) bounds the row's M-th from below, so the row's M best are
+// among each list's entries at or above it (a prefix of the sorted list);
+// those few are selected exactly, and the log-partition takes, per list, its
+// rest sum plus the suffix sum after its entries among the M best.  Returns
+// false, having written nothing, when more than kMergeCap entries reach the
+// bound (or fewer than M exist), for the full merge to run instead.
+DT_DEVINL bool merge_row_tails(const TopmParams& p, int row, const MergeSmem& m, float invT, bool arrivals) {
+  const int tid = threadIdx.x;
+  const size_t rb = static_cast<size_t>(row) * p.S;
+  const int S = p.S, M = p.M;
+  auto key_at = [&](int s2, int j) {
+    const size_t e = (rb + s2) * M + j;
+    return rank_key(p.part_val[e], static_cast<uint32_t>(p.part_id[e]));
+  };
+  float gmax = -INFINITY;
+  for (int s2 = tid; s2 < S; s2 += kThreads) gmax = fmaxf(gmax, p.part_max[rb + s2]);
+  gmax = block_max(gmax, m.red);
+  const int t = min(M, max(1, (M + S - 1) / S));
+  const int n1 = S * t;
+  for (int u = tid; u < n1; u += kThreads) {
+    const int s2 = u / t, j = u - s2 * t;
+    m.big[u] = j < p.part_cnt[rb + s2] ? key_at(s2, j) : 0ull;
+  }
+  if (tid == 0) *m.s_ncand = 0;
+  __syncthreads();
+  const uint64_t lb = block_kth_key<1>(m.big, n1, M, m.hist, m.scan, m.cand, m.red4, m.s_lb);
+  TOPM_STAMP(1, 1);
+  for (int s2 = tid; s2 < S; s2 += kThreads) {
+    const int cnt = p.part_cnt[rb + s2];
+    for (int j = 0; j < cnt; ++j) {
+      const uint64_t k = key_at(s2, j);
+      if (k < lb) break;
+      const int at = atomicAdd(m.s_ncand, 1);
+      if (at < kMergeCap) m.cand[at] = k;
+    }
+  }
+  __syncthreads();
+  const int nc = *m.s_ncand;
+  if (nc > kMergeCap || nc < M) return false;
+  TOPM_STAMP(1, 2);
+  // the row's M-th key among the candidates; the M best ranked among
+  // themselves (gathered into big, free again)
+  const uint64_t kth = block_kth_key<1>(m.cand, nc, M, m.hist, m.scan, m.big, m.red4, m.s_lb);
+  if (tid == 0) *m.s_ncand = 0;
+  __syncthreads();
+  for (int e = tid; e < nc; e += kThreads)
+    if (m.cand[e] >= kth) m.big[atomicAdd(m.s_ncand, 1)] = m.cand[e];
+  __syncthreads();
+  rank_all(m.big, *m.s_ncand, [&](int, uint64_t ke, int rk) {
+    if (rk < M) {
+      p.cand_tok[static_cast<size_t>(row) * M + rk] = static_cast<int>(rank_key_id(ke));
+      p.cand_base[static_cast<size_t>(row) * M + rk] = key_f32(static_cast<uint32_t>(ke >> 32));
+    }
+  });
+  TOPM_STAMP(1, 3);
+  // per list: its rest sum and the suffix after its entries among the M best
+  float rest = 0.0f;
+  for (int s2 = tid; s2 < S; s2 += kThreads) {
+    const int cnt = p.part_cnt[rb + s2];
+    int c = 0;
+    while (c < cnt && key_at(s2, c) >= kth) ++c;
+    const float tail = c < cnt ? p.part_tail[(rb + s2) * M + c] : 0.0f;
+    const float pm = p.part_max[rb + s2];
+    if (pm > -INFINITY) rest += (p.part_sum[rb + s2] + tail) * expf(pm - gmax);
+  }
+  rest = block_sum(rest, m.red);
+  if (tid == 0) {
+    p.rest_lse[row] = rest > 0.0f ? gmax + logf(rest) : -INFINITY;
+    if (arrivals) p.row_done[row] = 0u;  // ready for the next round
+  }
+  TOPM_STAMP(1, 4);
+  return true;
+}
+
+// The merge of row `row`'s S sorted partial lists: the M best (cand_tok,
+// cand_base, sorted) and rest_lse.  arrivals: the row's arrival counter is
+// reset for the next launch (the merge at the end of the Top-M kernel).
+DT_DEVINL void merge_row(const TopmParams& p, int row, const MergeSmem& m, float invT, bool arrivals) {
+  if (p.part_tail && merge_row_tails(p, row, m, invT, arrivals)) return;
+  const int tid = threadIdx.x;
+  const size_t rb = static_cast<size_t>(row) * p.S;
+  const int S = p.S, M = p.M;
+  const int total = S * M;
+  float gmax = -INFINITY;
+  for (int s2 = tid; s2 < S; s2 += kThreads) gmax = fmaxf(gmax, p.part_max[rb + s2]);
+  gmax = block_max(gmax, m.red);
+  // entries e = s*M + j; value, id and list length are read together, eight
+  // entries per thread at a time (their loads in flight at once); slots past
+  // a list's length hold stale data and get key 0
+  constexpr int kBatch = 8;
+  for (int eb = tid; eb < total; eb += kBatch * kThreads) {
+    float v[kBatch];
+    int id[kBatch], ok[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int e = min(eb + b * kThreads, total - 1);
+      const int s2 = e / M, j = e - s2 * M;
+      v[b] = p.part_val[rb * M + e];
+      id[b] = p.part_id[rb * M + e];
+      ok[b] = j < p.part_cnt[rb + s2];
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int e = eb + b * kThreads;
+      if (e < total) m.big[e] = ok[b] ? rank_key(v[b], static_cast<uint32_t>(id[b])) : 0ull;
+    }
+  }
+  if (tid == 0) *m.s_ncand = 0;
+  __syncthreads();
+  // the row's M-th largest entry; the best M are gathered and ranked among
+  // themselves, every other entry feeds the log-partition (each thread over
+  // its own fixed range of entries)
+  const uint64_t kth = block_kth_key<1>(m.big, total, M, m.hist, m.scan, m.cand, m.red4, m.s_lb);
+  TOPM_STAMP(1, 1);
+  float rest2 = 0.0f;
+  const int per = (total + kThreads - 1) / kThreads;
+  const int e0 = min(total, tid * per), e1 = min(total, e0 + per);
+  for (int e = e0; e < e1; ++e) {
+    const uint64_t k2 = m.big[e];
+    const bool lose = k2 != 0ull && k2 < kth;
+    rest2 += lose ? expf(key_f32(static_cast<uint32_t>(k2 >> 32)) * invT - gmax) : 0.0f;
+    if (k2 != 0ull && k2 >= kth) {
+      const int at = atomicAdd(m.s_ncand, 1);
+      if (at < kMergeCap) m.cand[at] = k2;
+    }
+  }
+  __syncthreads();
+  const int nc = *m.s_ncand;
+  TOPM_STAMP(1, 2);
+  rank_all(m.cand, min(nc, kMergeCap), [&](int, uint64_t ke, int rk) {
+    if (rk < M) {
+      p.cand_tok[static_cast<size_t>(row) * M + rk] = static_cast<int>(rank_key_id(ke));
+      p.cand_base[static_cast<size_t>(row) * M + rk] = key_f32(static_cast<uint32_t>(ke >> 32));
+    }
+  });
+  for (int s2 = tid; s2 < S; s2 += kThreads) {
+    const float ps = p.part_sum[rb + s2];
+    if (ps > 0.0f) rest2 += ps * expf(p.part_max[rb + s2] - gmax);
+  }
+  TOPM_STAMP(1, 3);
+  rest2 = block_sum(rest2, m.red);
+  if (tid == 0) {
+    if (nc < M) dt_report(p.status, DT_DEV_BOUNDS);
+    p.rest_lse[row] = rest2 > 0.0f ? gmax + logf(rest2) : -INFINITY;
+    if (arrivals) p.row_done[row] = 0u;  // ready for the next round
+  }
+  TOPM_STAMP(1, 4);
 }
 
 // kMinBlocks = 2 caps the registers so that two CTAs share an SM: for grids of
@@ -489,62 +671,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_topm(const TopmParams 
   if (!s_last) return;
   TOPM_STAMP(1, 0);
 
-  const size_t rb = static_cast<size_t>(row) * p.S;
-  const int S = p.S, M = p.M;
-  const int total = S * M;
-  // every thread reads the S chunk maxima itself (no block reduction)
-  float gmax = -INFINITY;
-  for (int s2 = 0; s2 < S; ++s2) gmax = fmaxf(gmax, p.part_max[rb + s2]);
-  // entries e = s*M + j; value, id and list length are read together (one
-  // round trip); slots past a list's length hold stale data and get key 0
-  for (int e = tid; e < total; e += kThreads) {
-    const int s2 = e / M, j = e - s2 * M;
-    const float v = p.part_val[rb * M + e];
-    const int id = p.part_id[rb * M + e];
-    const int cnt = p.part_cnt[rb + s2];
-    big[e] = j < cnt ? rank_key(v, static_cast<uint32_t>(id)) : 0ull;
-  }
-  if (tid == 0) s_ncand = 0;
-  __syncthreads();
-  // the row's M-th largest entry; the best M are gathered and ranked among
-  // themselves, every other entry feeds the log-partition (each thread over
-  // its own fixed range of entries)
-  const uint64_t kth = block_kth_key<1>(big, total, M, hist, scan, cand, &red4[0][0], &s_lb);
-  TOPM_STAMP(1, 1);
-  float rest2 = 0.0f;
-  const int per = (total + kThreads - 1) / kThreads;
-  const int e0 = min(total, tid * per), e1 = min(total, e0 + per);
-  for (int e = e0; e < e1; ++e) {
-    const uint64_t k2 = big[e];
-    if (k2 == 0ull) continue;
-    if (k2 >= kth) {
-      const int at = atomicAdd(&s_ncand, 1);
-      if (at < kMergeCap) cand[at] = k2;
-    } else {
-      rest2 += expf(key_f32(static_cast<uint32_t>(k2 >> 32)) * invT - gmax);
-    }
-  }
-  __syncthreads();
-  const int nc = s_ncand;
-  TOPM_STAMP(1, 2);
-  rank_all(cand, min(nc, kMergeCap), [&](int, uint64_t ke, int rk) {
-    if (rk < M) {
-      p.cand_tok[static_cast<size_t>(row) * M + rk] = static_cast<int>(rank_key_id(ke));
-      p.cand_base[static_cast<size_t>(row) * M + rk] = key_f32(static_cast<uint32_t>(ke >> 32));
-    }
-  });
-  for (int s2 = tid; s2 < S; s2 += kThreads) {
-    const float ps = p.part_sum[rb + s2];
-    if (ps > 0.0f) rest2 += ps * expf(p.part_max[rb + s2] - gmax);
-  }
-  TOPM_STAMP(1, 3);
-  rest2 = block_sum(rest2, red);
-  if (tid == 0) {
-    if (nc < M) dt_report(p.status, DT_DEV_BOUNDS);
-    p.rest_lse[row] = rest2 > 0.0f ? gmax + logf(rest2) : -INFINITY;
-    p.row_done[row] = 0u;  // ready for the next round
-  }
-  TOPM_STAMP(1, 4);
+  MergeSmem ms{hist, scan, red, &red4[0][0], &s_lb, &s_ncand, big, cand};
+  merge_row(p, row, ms, invT, true);
+}
+
+// The merge alone, one CTA per row, over partial lists another kernel wrote
+// (the LM-head GEMM's fused Top-M): dynamic shared memory holds S*M entries
+// and the candidate keys.
+__global__ void __launch_bounds__(kThreads, 1) k_topm_merge(const TopmParams p) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ uint32_t hist[256];
+  __shared__ int scan[40];
+  __shared__ float red[kWarps + 1];
+  __shared__ float red4[2 * kWarps];
+  __shared__ int s_ncand;
+  __shared__ uint64_t s_lb;
+  uint64_t* big = reinterpret_cast<uint64_t*>(dyn);
+  uint64_t* cand = big + max(static_cast<size_t>(p.S) * p.M, static_cast<size_t>(kMergeCap));
+  TOPM_STAMP(1, 0);
+  dt_grid_wait();  // the partial lists come from the previous kernel
+  dt_grid_release();
+  if (p.clear_word && blockIdx.x == 0 && threadIdx.x == 0) *p.clear_word = 0u;
+  MergeSmem ms{hist, scan, red, red4, &s_lb, &s_ncand, big, cand};
+  merge_row(p, static_cast<int>(blockIdx.x), ms, 1.0f / p.T, false);
 }
 
 }  // namespace
@@ -570,6 +719,7 @@ size_t topm_merge_smem(const TopmParams& p) { return topm_partial_smem(p); }
 cudaError_t topm_prepare() {
   cudaError_t e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm<1>));
   if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm<2>));
+  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm_merge));
   return e;
 }
 
@@ -579,6 +729,32 @@ const char* topm_unsupported(const TopmParams& p) {
   if (p.chunk > kMaxChunk) return "V too large for M: a chunk would exceed 16384 logits (V <= 8192 * 16384 / M)";
   if (p.S * p.M > kMaxMerge) return "chunks x M above the 8192 merged entries of a row";
   return nullptr;
+}
+
+size_t topm_merge_only_smem(const TopmParams& p) {
+  return (std::max(static_cast<size_t>(p.S) * p.M, static_cast<size_t>(kMergeCap)) + kMergeCap) * 8;
+}
+
+const char* topm_merge_unsupported(const TopmParams& p) {
+  if (p.rows < 1 || p.rows > 65535) return "rows must be 1..65535";
+  if (p.M < 1 || p.M > kMergeCap) return "M out of range";
+  if (topm_merge_only_smem(p) > 227 * 1024) return "too many partial lists to merge in shared memory";
+  return nullptr;
+}
+
+cudaError_t launch_topm_merge(const TopmParams& p, cudaStream_t stream) {
+  if (topm_merge_unsupported(p)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = topm_merge_only_smem(p);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_topm_merge, p);
 }
 
 cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {

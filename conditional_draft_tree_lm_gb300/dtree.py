@@ -39,6 +39,7 @@ class DtConfig(ctypes.Structure):
 WEIGHT_FIELDS = ("lm_head", "emb", "w_ih", "b_ih", "w_hh", "w1", "w2")
 FLAG_MARGINAL = 1  # DT_FLAG_MARGINAL: marginal scoring (no correction)
 FLAG_BEST_FIRST = 2  # DT_FLAG_BEST_FIRST: sequential conditional best-first builder
+FLAG_SEPARATE_TOPM = 4  # DT_FLAG_SEPARATE_TOPM: the Top-M as its own kernel in rounds
 
 
 class DtWeights(ctypes.Structure):
@@ -65,6 +66,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dt_destroy": (c_int, [vp]),
         "dt_base_logits": (c_int, [vp, vp, vp, vp]),
         "dt_topm": (c_int, [vp, vp, vp, vp, vp, vp]),
+        "dt_last_candidates": (c_int, [vp, vp, vp, vp, vp]),
+        "dt_base_topm": (c_int, [vp, vp, vp]),
         "dt_expand_depth": (c_int, [vp, c_int, i32p, vp, vp, vp, vp, vp, vp]),
         "dt_prune_topB": (c_int, [vp, vp, vp, vp]),
         "dt_tree_mask": (c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
@@ -93,10 +96,12 @@ def status_string(s: int) -> str:
 
 def make_config(cfg) -> DtConfig:
     """DtConfig from any object with the workload fields (d, V, block, g, r, M, K, W, B, n_req, beta, T,
-    and optionally marginal and builder)."""
+    and optionally marginal, builder and separate_topm)."""
     flags = FLAG_MARGINAL if getattr(cfg, "marginal", False) else 0
     if getattr(cfg, "builder", "dartree") == "best_first":
         flags |= FLAG_BEST_FIRST
+    if getattr(cfg, "separate_topm", False):
+        flags |= FLAG_SEPARATE_TOPM
     return DtConfig(cfg.d, cfg.V, cfg.block, cfg.g, cfg.r, cfg.M, cfg.K, cfg.W, cfg.B,
                     getattr(cfg, "n_req", 1), float(cfg.beta), float(cfg.T), flags)
 
@@ -199,6 +204,23 @@ class DraftTreeBuilder:
                                 _ptr(cand_tok, torch.int32, rows * cfg.M, "cand_tok"),
                                 _ptr(cand_base, torch.float32, rows * cfg.M, "cand_base"),
                                 _ptr(rest_lse, torch.float32, rows, "rest_lse"), _stream(stream)), "dt_topm")
+
+    def base_topm(self, H, stream=None):
+        """The LM-head GEMM and the Top-M of a round (dt_base_topm)."""
+        import torch
+        cfg = self.cfg
+        _check(self.lib.dt_base_topm(self.ctx, _ptr(H, torch.bfloat16, cfg.n_req * cfg.block * cfg.d, "H"),
+                                     _stream(stream)), "dt_base_topm")
+
+    def last_candidates(self, cand_tok=None, cand_base=None, rest_lse=None, stream=None):
+        """The Top-M restriction of the last round (or dt_topm) into these buffers (dt_last_candidates)."""
+        import torch
+        cfg = self.cfg
+        rows = cfg.n_req * (cfg.block - 1)
+        _check(self.lib.dt_last_candidates(self.ctx, _ptr(cand_tok, torch.int32, rows * cfg.M, "cand_tok"),
+                                           _ptr(cand_base, torch.float32, rows * cfg.M, "cand_base"),
+                                           _ptr(rest_lse, torch.float32, rows, "rest_lse"), _stream(stream)),
+               "dt_last_candidates")
 
     def expand_depth(self, depth, root_tok, node_tok, node_parent, node_logp, node_score, live=None,
                      stream=None):

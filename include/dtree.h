@@ -75,7 +75,7 @@ typedef struct dt_config {
   int n_req;  /* independent requests per round; n_req * block <= 512 */
   float beta; /* depth bonus of the Top-B key (score + beta * depth); <= 0 */
   float T;    /* temperature dividing the corrected logits; > 0 */
-  unsigned flags; /* DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST, or 0 */
+  unsigned flags; /* DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST | DT_FLAG_SEPARATE_TOPM, or 0 */
 } dt_config;
 
 /* Marginal scoring over the same super-tree: the correction Delta L is left
@@ -100,6 +100,17 @@ typedef struct dt_config {
  * frontier (1 + B*K nodes) must fit in shared memory, else dt_create returns
  * DT_ERR_SHAPE.  Combines with DT_FLAG_MARGINAL. */
 #define DT_FLAG_BEST_FIRST 2u
+
+/* The rounds of dt_build_round / dt_build_round_host run the Top-M as its own
+ * kernel over logits written by the LM-head GEMM.  Without the flag, a round
+ * of one request whose LM-head GEMM has a single 16-wide tile of H rows
+ * (block <= 16) and M <= 64 keeps each CTA's Top-M inside the GEMM's
+ * epilogue as the logits stream by, does not
+ * write the logits, and merges the CTAs' lists in a small kernel; the
+ * candidates, their order and the log-partition are the same up to the
+ * rounding of the partial sums.  dt_plan_string says which one runs.  The
+ * stand-alone dt_base_logits and dt_topm calls are not affected. */
+#define DT_FLAG_SEPARATE_TOPM 4u
 
 /* Frozen weights (device pointers, borrowed: they must outlive the context).
  * All bf16, row-major, torch.nn.Linear out-by-in layout.  GRU gate blocks are
@@ -184,6 +195,23 @@ dt_status dt_base_logits(dt_ctx* ctx, const void* H, float* logits, void* stream
  *              -inf when M == V. */
 dt_status dt_topm(dt_ctx* ctx, const float* logits, int32_t* cand_tok, float* cand_base,
                   float* rest_lse, void* stream);
+
+/* Steps 1 and 2 as a round runs them: the LM-head GEMM over H ([n_req,
+ * block, d] bf16, device, 16-byte aligned) and the Top-M restriction, either
+ * in the GEMM's epilogue with a merge of its CTAs' lists (the logits are not
+ * written) or as the Top-M kernel over the logits (DT_FLAG_SEPARATE_TOPM, or a
+ * shape the epilogue does not take).  The candidates are then read with
+ * dt_last_candidates, and dt_expand_prune builds the tree from them. */
+dt_status dt_base_topm(dt_ctx* ctx, const void* H, void* stream);
+
+/* The Top-M restriction the context holds now: that of the last round
+ * (dt_build_round, dt_build_round_host: with the Top-M in the LM-head GEMM's
+ * epilogue or as its own kernel, see DT_FLAG_SEPARATE_TOPM), of the last
+ * dt_base_topm or of the last dt_topm, copied on `stream` into the caller's
+ * device buffers (any may be NULL), in the layout of dt_topm's outputs.
+ * Before any of those the contents are zero. */
+dt_status dt_last_candidates(dt_ctx* ctx, int32_t* cand_tok, float* cand_base, float* rest_lse,
+                             void* stream);
 
 /* Step 3 — one depth of the batched expansion (DARTree page, Metodología 1;
  * Domino page, Cabeza de Domino).  For every live branch p of depth-1:

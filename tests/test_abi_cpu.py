@@ -87,12 +87,13 @@ def test_workspace_bytes(lib):
 
 
 def test_check_config_flags(lib):
-    """Unknown flag bits are rejected; the two defined flags combine."""
+    """Unknown flag bits are rejected; the three defined flags combine."""
     import ctypes
     from conditional_draft_tree_lm_gb300.dtree import load_library, make_config
-    cfg = make_config(get_config("tiny_bf16", builder="best_first", marginal=True))
-    assert cfg.flags == 3
+    cfg = make_config(get_config("tiny_bf16", builder="best_first", marginal=True, separate_topm=True))
+    assert cfg.flags == 7
     L = load_library()
     assert L.dt_check_config(ctypes.byref(cfg)) == 0
-    cfg.flags = 4
-    assert L.dt_check_config(ctypes.byref(cfg)) == 1
+    for bad in (8, 15, 1 << 31):
+        cfg.flags = bad
+        assert L.dt_check_config(ctypes.byref(cfg)) == 1

@@ -99,10 +99,17 @@ def test_tiny_stages(tiny, seed):
             want = list(t.live[i]) + [-1] * (cfg.W - len(t.live[i]))
             assert lives[i - 1] == want, f"live list after depth {i}"
         assert lives[D - 1] == [-1] * cfg.W
-    # the captured round reproduces the step-by-step results bit for bit
+    # the captured round reproduces the step-by-step results: bit for bit
+    # where both take the Top-M kernel; with the Top-M in the GEMM's epilogue
+    # the log-partition adds the same terms in another order, so the tree is
+    # the same and its log-probs agree to fp32 rounding
     whole = to_np(b.build_round(Hd, rd))
+    fused = "epilogue" in b.plan()
     for k in gt:
-        assert np.array_equal(whole[k], gt[k]), k
+        if fused and k == "logp_cum":
+            np.testing.assert_allclose(whole[k], gt[k], rtol=0, atol=1e-5)
+        else:
+            assert np.array_equal(whole[k], gt[k]), k
     assert b.device_status() == 0
 
 

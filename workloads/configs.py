@@ -34,6 +34,7 @@ class WorkloadConfig:
     weight_dtype: str = "bf16"  # "bf16" (rounded, RNE) or "fp32"
     marginal: bool = False      # marginal scoring: Delta L = 0 (path-independent children)
     builder: str = "dartree"    # "dartree" (depth-batched) or "best_first" (sequential heap)
+    separate_topm: bool = False  # run the Top-M as its own kernel, not in the LM-head GEMM
 
     @property
     def D(self) -> int:
