@@ -278,6 +278,7 @@ DT_DEVINL bool merge_row_tails(const TopmParams& p, int row, const MergeSmem& m,
   const int tid = threadIdx.x;
   const size_t rb = static_cast<size_t>(row) * p.S;
   const int S = p.S, M = p.M;
+  if (S > 256) return false;  // one thread per list, counts in the 256-word histogram
   auto key_at = [&](int s2, int j) {
     const size_t e = (rb + s2) * M + j;
     return rank_key(p.part_val[e], static_cast<uint32_t>(p.part_id[e]));
@@ -291,47 +292,57 @@ DT_DEVINL bool merge_row_tails(const TopmParams& p, int row, const MergeSmem& m,
     const int s2 = u / t, j = u - s2 * t;
     m.big[u] = j < p.part_cnt[rb + s2] ? key_at(s2, j) : 0ull;
   }
-  if (tid == 0) *m.s_ncand = 0;
   __syncthreads();
   const uint64_t lb = block_kth_key<1>(m.big, n1, M, m.hist, m.scan, m.cand, m.red4, m.s_lb);
   TOPM_STAMP(1, 1);
-  for (int s2 = tid; s2 < S; s2 += kThreads) {
-    const int cnt = p.part_cnt[rb + s2];
-    for (int j = 0; j < cnt; ++j) {
-      const uint64_t k = key_at(s2, j);
-      if (k < lb) break;
-      const int at = atomicAdd(m.s_ncand, 1);
-      if (at < kMergeCap) m.cand[at] = k;
+  // thread s: list s's entries at or above the bound (a prefix), read four at
+  // a time; their count, then their place in the candidate list (lists in
+  // order, so the list is the same every run)
+  int* ncs = reinterpret_cast<int*>(m.hist);  // [S] (the histogram is free again)
+  int cnt = 0, nmine = 0;
+  if (tid < S) {
+    cnt = p.part_cnt[rb + tid];
+    for (int j0 = 0; j0 < cnt; j0 += 4) {
+      uint64_t k4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) k4[i] = j0 + i < cnt ? key_at(tid, j0 + i) : 0ull;
+      int more = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) more += (j0 + i < cnt && k4[i] >= lb) ? 1 : 0;
+      nmine += more;
+      if (more < 4) break;
     }
   }
+  int total;
+  const int base = block_exclusive_scan(nmine, m.scan, &total);
+  if (total > kMergeCap || total < M) return false;  // (uniform: every thread has the total)
+  int* list_of = reinterpret_cast<int*>(m.big);  // [kMergeCap] list of candidate e (big is free again)
+  if (tid < S)
+    for (int j = 0; j < nmine; ++j) {
+      m.cand[base + j] = key_at(tid, j);
+      list_of[base + j] = tid;
+    }
+  if (tid < S) ncs[tid] = 0;
   __syncthreads();
-  const int nc = *m.s_ncand;
-  if (nc > kMergeCap || nc < M) return false;
   TOPM_STAMP(1, 2);
-  // the row's M-th key among the candidates; the M best ranked among
-  // themselves (gathered into big, free again)
-  const uint64_t kth = block_kth_key<1>(m.cand, nc, M, m.hist, m.scan, m.big, m.red4, m.s_lb);
-  if (tid == 0) *m.s_ncand = 0;
-  __syncthreads();
-  for (int e = tid; e < nc; e += kThreads)
-    if (m.cand[e] >= kth) m.big[atomicAdd(m.s_ncand, 1)] = m.cand[e];
-  __syncthreads();
-  rank_all(m.big, *m.s_ncand, [&](int, uint64_t ke, int rk) {
+  // ranks among the candidates: the M best are written in order, and each
+  // list counts its entries among them
+  rank_all(m.cand, total, [&](int e, uint64_t ke, int rk) {
     if (rk < M) {
       p.cand_tok[static_cast<size_t>(row) * M + rk] = static_cast<int>(rank_key_id(ke));
       p.cand_base[static_cast<size_t>(row) * M + rk] = key_f32(static_cast<uint32_t>(ke >> 32));
+      atomicAdd(&ncs[list_of[e]], 1);
     }
   });
+  __syncthreads();
   TOPM_STAMP(1, 3);
   // per list: its rest sum and the suffix after its entries among the M best
   float rest = 0.0f;
-  for (int s2 = tid; s2 < S; s2 += kThreads) {
-    const int cnt = p.part_cnt[rb + s2];
-    int c = 0;
-    while (c < cnt && key_at(s2, c) >= kth) ++c;
-    const float tail = c < cnt ? p.part_tail[(rb + s2) * M + c] : 0.0f;
-    const float pm = p.part_max[rb + s2];
-    if (pm > -INFINITY) rest += (p.part_sum[rb + s2] + tail) * expf(pm - gmax);
+  if (tid < S) {
+    const int c = ncs[tid];
+    const float tail = c < cnt ? p.part_tail[(rb + tid) * M + c] : 0.0f;
+    const float pm = p.part_max[rb + tid];
+    if (pm > -INFINITY) rest = (p.part_sum[rb + tid] + tail) * expf(pm - gmax);
   }
   rest = block_sum(rest, m.red);
   if (tid == 0) {
