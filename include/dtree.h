@@ -280,7 +280,8 @@ dt_status dt_accept_walk(dt_ctx* ctx, const float* target_logits, const int32_t*
 
 /* Steps 3-5 in as few launches as the shape allows (one for a single request):
  * every depth of the expansion, the global Top-B and the tree/mask, from the
- * Top-M results that the last dt_topm left in the workspace (or, with
+ * Top-M results that the last dt_topm, dt_base_topm or round left in the
+ * workspace (or, with
  * DT_FLAG_BEST_FIRST, the best-first builder).  Node arrays and the selection
  * stay in the workspace.
  *   root_tok: [n_req] int32; outputs as dt_tree_mask.
@@ -361,10 +362,11 @@ dt_status dt_check_bounded_waits(dt_ctx* ctx, int which, void* stream);
 /* Number of kernel launches one dt_build_round replay performs. */
 int dt_round_kernel_count(const dt_ctx* ctx);
 
-/* Which kernels the context's rounds run, chosen at dt_create from the shape
- * and the device (for one request: the clustered depth chain, with its cluster
- * size, or the grid-barrier chain and the reason).  Owned by the context;
- * "" for NULL. */
+/* Which kernels the context's rounds run, chosen at dt_create from the shape,
+ * the flags and the device: the Top-M in the LM-head GEMM's epilogue (with the
+ * number of CTA lists merged) or the Top-M kernel (with its chunks per row);
+ * then, for one request, the clustered depth chain with its cluster size, or
+ * the grid-barrier chain and the reason.  Owned by the context; "" for NULL. */
 const char* dt_plan_string(const dt_ctx* ctx);
 
 #ifdef __cplusplus
