@@ -1,15 +1,17 @@
 """Per-depth phase breakdown of the clustered depth chain (a profiling tool).
 
-Builds an instrumented copy of libdtree (``-DDT_DCHAIN_TIMING``: thread 0 of
-CTA 0 and of the last CTA record ``clock64()`` at every phase boundary of every
-depth) beside the normal library, replays whole rounds of a workload through
-it, and prints the mean cycles of each phase: X (waiting for and gathering the
-previous depth's states), A1 (W1_S projection and z), A2 (partial
-correction), A3 (W_hh projection), R (the cluster reduction of the
-correction), B (corrected log-probs and top-K: B.sel; the children: B.out; the
-block barrier: B.bar), top-W, C (GRU update, publication), and the kernel's prologue and tail.  Every CTA also records the
+Builds an instrumented copy of libdtree (``-DDT_DCHAIN_TIMING``,
+``-DDT_TOPM_TIMING``, ``-DDT_GEMM_TIMING``: thread 0 of CTA 0 and of the last
+CTA record ``clock64()`` at every phase boundary of every depth) beside the
+normal library, replays whole rounds of a workload through it, and prints the
+mean cycles of each phase: X (waiting for and gathering the previous depth's
+states), A1 (W1_S projection and z), A2 (partial correction), A3 (W_hh projection), R (the cluster
+reduction of the correction), B (corrected log-probs and top-K: B.sel; the
+children: B.out; the block barrier: B.bar), top-W, C (GRU update,
+publication), and the kernel's prologue and tail.  Every CTA also records the
 global timer when it has published a depth's states and when it holds all of
 them, which shows the spread of the publications and the exchange latency.
+It also prints the Top-M's phases (row 0) and the LM-head GEMM's tiles (CTA 0).
 The normal library is not touched; the instrumented one is only loaded by this
 process.
 
@@ -142,7 +144,7 @@ def main():
         print(f"  A1: loads + MMAs {sub(1, 11):.0f}, partial sums {sub(11, 12):.0f}, barrier {sub(12, 13):.0f}, "
               f"z {sub(13, 2):.0f};  B.sel: operands {sub(5, 15):.0f}, top-K rounds + log-partition {sub(15, 6):.0f};  "
               f"topW: rounds {sub(8, 14):.0f}, survivor order {sub(14, 9):.0f};  "
-              f"X: staging {sub(0, 16):.0f}, poll {sub(16, 17):.0f}, barrier + copies {sub(17, 1):.0f}")
+              f"X: loads issued {sub(0, 16):.0f}, poll {sub(16, 17):.0f}, barrier + copies {sub(17, 1):.0f}")
     exchange_report(np.stack(xacc), D, b.plan())
     topm_report(np.stack(tacc))
     gemm_report(np.stack(gacc), 1.0 / mhz)

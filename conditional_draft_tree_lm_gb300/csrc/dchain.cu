@@ -476,40 +476,40 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     }
   }
 
+  // the epoch: the previous launch of this kernel ended before this one started
+  const uint32_t E = ld_relaxed_u32(p.epoch) + 1u;
+  uint64_t* xch = reinterpret_cast<uint64_t*>(p.xch);
+  const int nwords = L.G * kWP;                      // every CTA's words
+  bool aborted = false;
+  // the peers' barriers are initialised before anyone pushes into them; the
+  // resident weights have landed
+  cluster_sync();
+  if (!mbar_wait(&s_mbar_w, 0, p.status)) {
+    st_relaxed_u32(p.abort_word, E);
+    aborted = true;
+  }
+
   // everything below reads the previous kernels' results
   DCH_STAMP(0, 4);
   dt_grid_wait();
   DCH_STAMP(0, 5);
-  const uint32_t E = ld_relaxed_u32(p.epoch) + 1u;
-
-  for (int idx = tid; idx < D * M; idx += kT) {
-    const int i = idx / M, c = idx - i * M;
-    int t = p.cand_tok[idx];
-    if (t < 0 || t >= p.V) {
-      dt_report(p.status, DT_DEV_BOUNDS);
-      t = 0;
-    }
-    tok_all[i * kMP + c] = t;
-  }
-  __syncthreads();
 
   // stage the candidate data of one depth with threads t0 .. t0 + nt - 1 (one
-  // cp.async group each, possibly empty)
-  auto stage_depth = [&](int i, int t0, int nt) {
+  // cp.async group each, possibly empty); tok(c) gives candidate c's token
+  auto stage_with = [&](int i, int t0, int nt, auto tok) {
     const int t = tid - t0;
     if (i <= p.depth_last) {
       const Stage b = stage(i);
-      const int* tk = tok_all + (i - 1) * kMP;
       const int r8 = RQ / 8;
       for (int idx = t; idx < M * r8; idx += nt) {
         const int c = idx / r8, k8 = idx - c * r8;
-        cp_async16(b.w2 + static_cast<size_t>(c) * RQP + 8 * k8, p.w2 + static_cast<size_t>(tk[c]) * r + r0 + 8 * k8);
+        cp_async16(b.w2 + static_cast<size_t>(c) * RQP + 8 * k8, p.w2 + static_cast<size_t>(tok(c)) * r + r0 + 8 * k8);
       }
       constexpr int kQ4 = JC / 4;  // 16-byte pieces of one gate's owned columns
       for (int idx = t; idx < M * 3 * kQ4; idx += nt) {
         const int c = idx / (3 * kQ4), rem = idx - c * 3 * kQ4, gate = rem / kQ4, h = rem - gate * kQ4;
         cp_async16(b.xs + c * 3 * JC + gate * JC + 4 * h,
-                   p.xtab + static_cast<size_t>(tk[c]) * 3 * g + gate * g + j0 + 4 * h);
+                   p.xtab + static_cast<size_t>(tok(c)) * 3 * g + gate * g + j0 + 4 * h);
       }
       for (int c = t; c < M; c += nt) cp_async4(b.cbs + c, p.cand_base + static_cast<size_t>(i - 1) * M + c);
       for (int k4 = t; k4 < RQ / 4; k4 += nt)
@@ -518,22 +518,57 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     }
     cp_async_commit();
   };
-  stage_depth(p.depth_first, 0, kT);
+  auto stage_depth = [&](int i, int t0, int nt) {
+    const int* tk = tok_all + (i - 1) * kMP;
+    stage_with(i, t0, nt, [&](int c) {
+      int t = tk[c];
+      if (t < 0 || t >= p.V) {
+        dt_report(p.status, DT_DEV_BOUNDS);
+        t = 0;
+      }
+      return t;
+    });
+  };
+  auto checked_tok = [&](int idx) {
+    int t = p.cand_tok[idx];
+    if (t < 0 || t >= p.V) {
+      dt_report(p.status, DT_DEV_BOUNDS);
+      t = 0;
+    }
+    return t;
+  };
+  // the first depth's candidate data straight from its tokens, one round trip
+  // sooner: thread c < M holds candidate c's token and copies its rows
+  {
+    const int tf = tid < M ? checked_tok((f0 - 1) * M + tid) : 0;
+    if (tid < M) {
+      const Stage b = stage(f0);
+      for (int k8 = 0; k8 < RQ / 8; ++k8)
+        cp_async16(b.w2 + static_cast<size_t>(tid) * RQP + 8 * k8, p.w2 + static_cast<size_t>(tf) * r + r0 + 8 * k8);
+#pragma unroll
+      for (int gate = 0; gate < 3; ++gate)
+#pragma unroll
+        for (int h = 0; h < JC / 4; ++h)
+          cp_async16(b.xs + tid * 3 * JC + gate * JC + 4 * h,
+                     p.xtab + static_cast<size_t>(tf) * 3 * g + gate * g + j0 + 4 * h);
+      cp_async4(b.cbs + tid, p.cand_base + static_cast<size_t>(f0 - 1) * M + tid);
+    } else if (tid - M < RQ / 4) {
+      const Stage b = stage(f0);
+      cp_async16(b.h1 + 4 * (tid - M), p.h1 + static_cast<size_t>(f0 - 1) * r + r0 + 4 * (tid - M));
+    } else if (tid == kT - 1) {
+      cp_async4(stage(f0).rest, p.rest_lse + (f0 - 1));
+    }
+    // every depth's tokens into shared memory for the later stagings, copied in
+    // the same group (the first depth waits for it; its barriers show the
+    // tokens to every thread; the stagings check them)
+    for (int idx = tid; idx < D * M; idx += kT) cp_async4(tok_all + (idx / M) * kMP + idx % M, p.cand_tok + idx);
+    cp_async_commit();
+  }
 
   const int nkw = (L.nk16 - warp + kNW - 1) / kNW;  // k16 steps of this warp (kt = warp + kNW m)
   // lambda = (base + dL) / T as a product with 1/T (exact at T = 1; within an
   // ulp of the quotient otherwise)
   const float invT = 1.0f / p.T;
-  uint64_t* xch = reinterpret_cast<uint64_t*>(p.xch);
-  const int nwords = L.G * kWP;                      // every CTA's words
-  bool aborted = false;
-
-  // the peers' barriers are initialised before anyone pushes into them
-  cluster_sync();
-  if (!mbar_wait(&s_mbar_w, 0, p.status)) {
-    st_relaxed_u32(p.abort_word, E);
-    aborted = true;
-  }
 
   for (int i = f0; i <= p.depth_last; ++i) {
     const int Lp = p.L[i - 1];  // live branches entering this depth
