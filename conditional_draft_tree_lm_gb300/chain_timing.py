@@ -51,7 +51,8 @@ def main():
     from .build import LIB_DIR, build_library
     from workloads import get_config, make_round_inputs, make_weights
 
-    path = build_library(force=True, extra_flags=["-DDT_DCHAIN_TIMING", "-DDT_TOPM_TIMING", "-DDT_GEMM_TIMING"],
+    path = build_library(force=True, extra_flags=["-DDT_DCHAIN_TIMING", "-DDT_TOPM_TIMING", "-DDT_GEMM_TIMING",
+                                                  "-DDT_CHAIN_TIMING"],
                          lib_path=os.path.join(LIB_DIR, "libdtree_timing.so"))
     dtree._lib = None
     lib = dtree.load_library(path)
@@ -71,8 +72,9 @@ def main():
     wd = {k: dtree.bf16_tensor(v) for k, v in w.items()}
     b = dtree.DraftTreeBuilder(cfg, wd)
     print("plan:", b.plan())
-    if "clustered" not in b.plan():
-        raise SystemExit("the workload does not run the clustered depth chain")
+    if "clustered depth chain on" not in b.plan():
+        grid_chain_report(lib, b, cfg, args)
+        return
     D = cfg.block - 1
     buf = np.zeros(2 * SLOTS * NPH, dtype=np.uint64)
     xbuf = np.zeros(2 * SLOTS * XCTAS, dtype=np.uint64)
@@ -149,6 +151,54 @@ def main():
     topm_report(np.stack(tacc))
     gemm_report(np.stack(gacc), 1.0 / mhz)
     b.close()
+
+
+GRID_PHASES = ["A", "bar1", "B", "bar2", "C", "bar3"]
+
+
+def grid_chain_report(lib, b, cfg, args):
+    """The grid-barrier chain (several requests, or many branches): per depth,
+    phase A (projections; its waits for state blocks shown apart), the
+    barrier after it, phase B (selections; with one request also phase C), the
+    barrier before the all-request phase C, phase C, and the depth's last
+    barrier, for CTA 0 and the last CTA."""
+    import torch
+
+    from . import dtree
+    from workloads import make_round_inputs
+    lib.dt_chain_stamps.restype = ctypes.c_int
+    lib.dt_chain_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    D = cfg.block - 1
+    buf = np.zeros(2 * SLOTS * 8, dtype=np.uint64)
+    acc = []
+    for s in range(args.rounds + 3):
+        H, r = make_round_inputs(cfg, s)
+        Hd = dtree.bf16_tensor(H)
+        rd = torch.from_numpy(np.asarray(r).astype(np.int32)).cuda()
+        b.build_round(Hd, rd)
+        torch.cuda.synchronize()
+        if lib.dt_chain_stamps(buf.ctypes.data, buf.size) != buf.size:
+            raise SystemExit("dt_chain_stamps failed")
+        if s >= 3:
+            acc.append(buf.reshape(2, SLOTS, 8).astype(np.int64).copy())
+    st = np.stack(acc)
+    us = 1.0 / (args.mhz or 2070.0)
+    print(f"{len(acc)} rounds of {cfg.name}; grid-barrier chain; cycles, mean over rounds")
+    for c, name in ((0, "CTA 0"), (1, "last CTA")):
+        k = st[:, c]
+        print(f"\n{name}")
+        print("depth " + " ".join(f"{p:>8s}" for p in GRID_PHASES) + "  blk-wait  total(us)")
+        tot = np.zeros(len(GRID_PHASES) + 1)
+        for i in range(1, D + 1):
+            t = k[:, i]
+            # stamp 4 exists only with several requests; stamp 6 not at the last depth
+            s4 = np.where(t[:, 4] > 0, t[:, 4], t[:, 3])
+            s6 = t[:, 6] if i < D else t[:, 5]
+            row = [(t[:, 1] - t[:, 0]).mean(), (t[:, 2] - t[:, 1]).mean(), (t[:, 3] - t[:, 2]).mean(),
+                   (s4 - t[:, 3]).mean(), (t[:, 5] - s4).mean(), (s6 - t[:, 5]).mean(), t[:, 7].mean()]
+            tot += np.array(row)
+            print(f"{i:5d} " + " ".join(f"{v:8.0f}" for v in row) + f"  {(s6 - t[:, 0]).mean() * us:8.2f}")
+        print("us    " + " ".join(f"{v / D * us:8.2f}" for v in tot))
 
 
 def gemm_report(gs, us):

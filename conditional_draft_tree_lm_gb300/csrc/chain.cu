@@ -67,6 +67,34 @@ constexpr int kZLoads = 16;      // z values per thread on the tensor-core path:
 constexpr int kFragMax = 8;      // fragment loads per lane in phase A: g <= 16 * kWarps * kFragMax
 constexpr int kZFragMax = 16;    // z fragment loads per lane in phase B: r <= 16 * kZFragMax
 
+// Phase stamps (built with -DDT_CHAIN_TIMING only): thread 0 of CTA 0 and of
+// the last CTA records clock64() at the phase boundaries of every depth;
+// dt_chain_stamps copies them out.  Slot layout [CTA 0 / last][depth][phase]:
+// 0 depth start, 1 phase A done, 2 past the barrier after A, 3 phase B done,
+// 4 past the barrier before C (several requests), 5 phase C done, 6 past the
+// depth's last barrier, 7 cycles spent waiting for state blocks in phase A.
+#ifdef DT_CHAIN_TIMING
+constexpr int kChainStamps = 8;
+__device__ unsigned long long g_chain_stamps[2][kMaxDepth + 2][kChainStamps];
+#define CH_STAMP(depth, k)                                                                       \
+  do {                                                                                           \
+    if (tid == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1))                            \
+      g_chain_stamps[blockIdx.x == 0 ? 0 : 1][depth][k] = static_cast<unsigned long long>(clock64()); \
+  } while (0)
+#define CH_STAMP_SET(depth, k, v)                                                                \
+  do {                                                                                           \
+    if (tid == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1))                            \
+      g_chain_stamps[blockIdx.x == 0 ? 0 : 1][depth][k] = (v);                                   \
+  } while (0)
+#else
+#define CH_STAMP(depth, k) \
+  do {                     \
+  } while (0)
+#define CH_STAMP_SET(depth, k, v) \
+  do {                            \
+  } while (0)
+#endif
+
 // Dimensions a launch runs with (see chain_plan).
 struct Shape {
   int g, r, M, K, W, n_req, D, jper, rper, cpad;
@@ -86,7 +114,15 @@ struct Shape {
   // one request, many branches, SIMT phase B: branches scored by different
   // CTAs; no GRU-input slices are staged (phase C reads the table)
   bool bdist;
+  // phase A on tcgen05 (states streamed as 128-row A-operand chunks into ns
+  // shared-memory slots, accumulators in tensor memory)
+  bool tc;
+  int ns;
 };
+
+// One streamed A-operand chunk of the tcgen05 phase A: 128 state rows x 64
+// bf16 (one part, high or low, of one K block), 128-byte swizzled.
+constexpr int kTcChunk = 16384;
 
 DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
   return n_req == 1 && W <= kPC && g % (16 * kWarps) == 0 && g / (16 * kWarps) <= kFragMax;
@@ -111,7 +147,7 @@ DT_HOST_DEVICE_INLINE Shape runtime_shape(const ChainParams& p) {
   return Shape{p.g, p.r, p.M, p.K, p.W, p.n_req, p.D, p.jper, p.rper, p.cpad, p.stage_w2 != 0, p.mma_b != 0,
                prefetch_tokens(p.D, p.M), p.dbuf != 0, fr,
                fr && p.mma_b != 0 && p.dbuf != 0 && p.r % 16 == 0 && p.r / 16 <= kZFragMax,
-               mfrag_ok(p), bdist_ok(p)};
+               mfrag_ok(p) && p.tc == 0, bdist_ok(p), p.tc != 0, p.tc_ns};
 }
 
 // Generic instantiation: every dimension from the launch parameters.
@@ -122,7 +158,7 @@ struct DimsRuntime {
 // CTAs): dimensions are literals, so the compiler folds the index arithmetic.
 struct DimsQ4B {
   static constexpr Shape kShape{1024, 256, 64, 8, 8, 1, 15, 8, 2, 32, true, true, true, true, true, true, false,
-                                false};
+                                false, false, 0};
   static DT_DEVINL Shape get(const ChainParams&) { return kShape; }
 };
 
@@ -164,6 +200,7 @@ struct Smem {
   uint64_t* lamkey; // [W][M] (lambda, token) keys (tensor-core phase B)
   uint4* mf0;       // fragment blocks of the states, two buffers (several requests)
   uint4* mf1;
+  uint8_t* ring;    // [ns][kTcChunk] streamed A-operand chunks (tcgen05 phase A)
   Stage st0, st1;   // stage buffers of even and odd depths (the same buffer without dbuf)
 };
 
@@ -212,11 +249,15 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
   const size_t gp = static_cast<size_t>(kstride(sh.g));
   const size_t shsl = gp * kPC * 2 * 2, zl = zrows_bytes(sh) + lamkey_bytes(sh);
   const size_t mblk = sh.mfrag ? static_cast<size_t>(32) * sh.g : 0;  // one 8-state fragment block
-  const size_t r1 = shsl > zl ? shsl : zl;
+  // the tcgen05 phase A needs neither the state chunk (region 1) nor the
+  // partial sums (region 2); without them the Top-B and tree/mask tail runs
+  // in its own launches (chain_can_fuse_tree reads these sizes)
+  const bool lean = sh.tc;
+  const size_t r1 = (shsl > zl && !lean) ? shsl : zl;
   const size_t sz[23] = {
       gp * sh.cpad * 2,
       r1 > mblk ? r1 : mblk,
-      static_cast<size_t>(kWarps) * kPC * sh.cpad * 4,
+      lean ? 0 : static_cast<size_t>(kWarps) * kPC * sh.cpad * 4,
       static_cast<size_t>(sh.n_req) * sh.W * 3 * sh.jper * 4,
       sh.mma_b ? 0 : static_cast<size_t>(kWarps) * sh.r * 4,
       stage_bytes(sh, 0),
@@ -235,17 +276,52 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
       static_cast<size_t>(sh.W) * 4,
       static_cast<size_t>(sh.W) * 4,
       sh.prefetch ? static_cast<size_t>(sh.D) * sh.M * 4 : 0,
-      mblk,  // the second fragment-block buffer (the first is region 1)
+      // the second fragment-block buffer (the first is region 1), or the
+      // tcgen05 phase A's chunk slots
+      sh.tc ? static_cast<size_t>(sh.ns) * kTcChunk : mblk,
       0,     // (z rows and (lambda, token) keys: in region 1)
   };
   SmemSizes s;
   size_t o = 0;
   for (int i = 0; i < 23; ++i) {
+    // tcgen05 operands (the weights, region 0, and the chunk slots, region
+    // 21) start on 1024-byte boundaries (the 128-byte swizzle's atoms)
+    if (i == 21 && sh.tc) o = (o + 1023) & ~static_cast<size_t>(1023);
     s.off[i] = o;
     o += al16(sz[i]);
   }
-  s.total = o;
+  // room to align the base of the dynamic shared memory to 1024 bytes
+  s.total = o + (sh.tc ? 1024 : 0);
   return s;
+}
+
+// Byte offset of state (row st, column k) in the tcgen05 A-operand chunks of
+// one parity: chunk (row tile st/128, K block k/64, part), inside it the
+// 128-byte swizzled K-major layout (8-row atoms of 1024 bytes, row st%8 of an
+// atom at 128 st%8, its 16-byte piece k%64/8 at piece (k%64/8) xor (st%8)).
+// The low part's chunk follows the high part's.
+DT_DEVINL size_t tc_off(int st, int k, int KB) {
+  const int mt = st >> 7, rr = st & 127, kb = k >> 6, ch = (k >> 3) & 7;
+  return static_cast<size_t>((mt * KB + kb) * 2) * kTcChunk + (rr >> 3) * 1024 + (rr & 7) * 128 +
+         ((ch ^ (rr & 7)) << 4) + (k & 7) * 2;
+}
+// One state value: its bf16 high part and the bf16 of the remainder.
+DT_DEVINL void store_tc1(uint8_t* base, int st, int k, int KB, float v) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+  uint8_t* a = base + tc_off(st, k, KB);
+  *reinterpret_cast<uint16_t*>(a) = __bfloat16_as_ushort(hi);
+  *reinterpret_cast<uint16_t*>(a + kTcChunk) = __bfloat16_as_ushort(lo);
+}
+// Eight consecutive values (columns k..k+7, k a multiple of 8): one 16-byte
+// piece of each part.
+DT_DEVINL void store_tc8(uint8_t* base, int st, int k, int KB, const float (&v)[8]) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) hi[e] = split_hi_lo(v[2 * e], v[2 * e + 1], lo[e]);
+  uint8_t* a = base + tc_off(st, k, KB);
+  *reinterpret_cast<uint4*>(a) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(a + kTcChunk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
 // Read the candidate tokens of one (request, depth) row into shared memory.
@@ -336,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   __shared__ uint32_t s_state[4];
   __shared__ float s_tred[64];  // Top-B min/max partials of the tail
   __shared__ int s_tscan[40];   // Top-B fallback scans
+  // tcgen05 phase A: chunk slots full [0..3] / free [4..7], products done [8]
+  __shared__ __align__(8) uint64_t s_tcbar[9];
+  __shared__ uint32_t s_tmem;
 
   const Shape sh = Dm::get(p);
   // candidate keys carry their candidate index (M <= 64, token ids < 2^26)
@@ -352,6 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   Smem s;
   {
     const SmemSizes L = smem_sizes(sh);
+    // (the tcgen05 operands want 1024-byte aligned regions)
+    uint8_t* const smem_raw_ = smem_raw;
+    uint8_t* const smem_raw =
+        sh.tc ? smem_raw_ + ((1024u - (smem_u32(smem_raw_) & 1023u)) & 1023u) : smem_raw_;
     s.w = reinterpret_cast<uint16_t*>(smem_raw + L.off[0]);
     s.sh = reinterpret_cast<uint16_t*>(smem_raw + L.off[1]);
     s.sl = s.sh + static_cast<size_t>(kPC) * kstride(g);
@@ -391,19 +474,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     s.lamkey = reinterpret_cast<uint64_t*>(smem_raw + L.off[1] + zrows_bytes(sh));
     s.mf0 = reinterpret_cast<uint4*>(smem_raw + L.off[1]);
     s.mf1 = reinterpret_cast<uint4*>(smem_raw + L.off[21]);
+    s.ring = smem_raw + L.off[21];
   }
 
   if (tid == 0) {
     s_abort = 0;
     mbar_init(&s_mbar[0], 1);
     mbar_init(&s_mbar[1], 1);
+    if (sh.tc)
+      for (int b = 0; b < 9; ++b) mbar_init(&s_tcbar[b], 1);
     fence_mbar_init();
   }
   uint32_t mf_phase = 0;  // completed-phase parity of the two block buffers
+  // tcgen05 phase A: tensor-memory columns (one 128-lane tile of cpad fp32
+  // columns per 128 state rows), chunks streamed so far, products-done parity
+  const int tc_nmt = (n_req * W + 127) / 128;
+  uint32_t tc_cols = 32;
+  while (sh.tc && tc_cols < static_cast<uint32_t>(tc_nmt * cpad)) tc_cols <<= 1;
+  uint32_t tc_seq = 0, tc_done_ph = 0;
+  if (sh.tc && warp == 0) tmem_alloc(&s_tmem, tc_cols);
 
   // ---- the owned weight columns, K-major: s.w[c][k] (zero padded) ----
   const int gp = kstride(g);
-  if (!p.marginal) {
+  if (sh.tc) {
+    // tcgen05 B operand: K blocks of 64 (cpad rows x 128 bytes each), the
+    // rows 128-byte swizzled in 8-row atoms
+    const int g8 = g / 8;
+    uint8_t* wb = reinterpret_cast<uint8_t*>(s.w);
+    for (int idx = tid; idx < cpad * g8; idx += kThreads) {
+      const int c = idx / g8, k8 = idx - c * g8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (c < 3 * nj) {
+        const int gate = c / nj, jj = c - gate * nj;
+        v = *reinterpret_cast<const uint4*>(p.w_hh + static_cast<size_t>(gate * g + j0 + jj) * g + 8 * k8);
+      } else if (c < ncol) {
+        const int rr = r0 + (c - 3 * nj);
+        v = *reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(rr) * p.ldw1 + p.d + 8 * k8);
+      }
+      const int kb = k8 >> 3, ch = k8 & 7;
+      *reinterpret_cast<uint4*>(wb + static_cast<size_t>(kb) * cpad * 128 + (c >> 3) * 1024 + (c & 7) * 128 +
+                                ((ch ^ (c & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();  // read by tcgen05.mma
+    tc_fence_before();
+  } else if (!p.marginal) {
     const int g8 = gp / 8;  // 16-byte chunks per padded row
     for (int idx = tid; idx < cpad * g8; idx += kThreads) {
       const int c = idx / g8, k8 = idx - c * g8;
@@ -424,6 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   // the resident weights are loaded; everything below reads the previous
   // kernels' results (and the barrier counter Top-M cleared)
   dt_grid_wait();
+  uint32_t tmem_base = 0;
+  if (sh.tc) {
+    __syncthreads();
+    tc_fence_after();
+    tmem_base = s_tmem;
+  }
 
   // ---- candidate tokens of every depth of request 0, read once ----
   if (sh.prefetch) {
@@ -452,7 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   // step and phase A)
   auto buf = [&](int depth) -> Stage { return (depth & 1) ? s.st1 : s.st0; };
   // on a barrier timeout: let the CTA's own copies land before it returns
-  auto drain = [&]() { cp_async_wait_all(); };
+  // (and give back the tensor memory)
+  auto drain = [&]() {
+    cp_async_wait_all();
+    if (sh.tc) {
+      tc_fence_before();
+      __syncthreads();
+      if (warp == 0) tmem_dealloc(tmem_base, tc_cols);
+    }
+  };
   if (qfirst < n_req) {
     select_row_tokens(p, sh, s, qfirst, p.depth_first);
     __syncthreads();
@@ -477,8 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       const float s0 = (1.0f - zg) * ng;
       p.S[static_cast<size_t>(q * W) * g + jj] = s0;
       if (sh.frag || sh.mfrag) store_frag(p.sfrag, q * W, jj, g / 16, s0);  // parity 0 = depth 0
+      if (sh.tc) store_tc1(reinterpret_cast<uint8_t*>(p.sfrag), q * W, jj, g / 64, s0);
     }
-    if (sh.mfrag) fence_proxy_async_global();
+    if (sh.mfrag || sh.tc) fence_proxy_async_global();
     if (blockIdx.x == 0) {
       for (int q = tid; q < n_req; q += kThreads) {
         const size_t b = static_cast<size_t>(q) * p.N1;
@@ -504,6 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     float* Snext = p.S + static_cast<size_t>(i & 1) * n_req * W * g;
     const int* live_prev = p.live + static_cast<size_t>((i - 1) & 1) * n_req * W;
     int* live_next = p.live + static_cast<size_t>(i & 1) * n_req * W;
+    CH_STAMP(i, 0);
+#ifdef DT_CHAIN_TIMING
+    unsigned long long blk_wait = 0;
+#endif
     // one request: the next depth's candidate data is staged now, into the
     // other buffer (its last reader, depth i-1, finished before the barrier);
     // it lands during this depth
@@ -589,6 +722,105 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
     }
+    if (sh.tc) {
+      // the states on tcgen05: u[row][c] = sum_k S[row][k] W[c][k] for every
+      // state row (128-row tiles) and owned weight row c (N = cpad), the
+      // high and the low parts of the states accumulated into the same fp32
+      // accumulator.  Warp 1 streams the A chunks (128 rows x 64 K of one
+      // part) from L2 into ns slots with bulk copies; one thread of warp 0
+      // issues four K=16 MMAs per chunk against the resident weights and
+      // frees the slot through the MMAs' commit.
+      if (sh.dbuf && i < p.depth_last)
+        stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
+                  i + 1 != D);
+      const int KB = g / 64;
+      const int nch = tc_nmt * KB * 2;
+      const int ns = sh.ns;
+      const uint8_t* abase = reinterpret_cast<const uint8_t*>(p.sfrag) +
+                             static_cast<size_t>((i - 1) & 1) * tc_nmt * KB * 2 * kTcChunk;
+      // every CTA starts at a different K block, so that the CTAs do not all
+      // read the same lines at the same time
+      const int rot = static_cast<int>(blockIdx.x) % KB;
+      if (warp == 1) {
+        if (lane == 0) {
+          fence_proxy_async_global();  // the states were written by generic stores
+          for (int c = 0; c < nch; ++c) {
+            const uint32_t n = tc_seq + static_cast<uint32_t>(c), slot = n % ns, use = n / ns;
+            if (use > 0 && !mbar_wait(&s_tcbar[4 + slot], (use - 1) & 1u, p.status)) {
+              s_abort = 1;
+              break;
+            }
+            const int mt = c / (2 * KB), rem = c - mt * 2 * KB, kk = rem >> 1, part = rem & 1;
+            const int kb = kk + rot < KB ? kk + rot : kk + rot - KB;
+            mbar_arrive_expect_tx(&s_tcbar[slot], kTcChunk);
+            bulk_g2s(s.ring + static_cast<size_t>(slot) * kTcChunk,
+                     abase + static_cast<size_t>((mt * KB + kb) * 2 + part) * kTcChunk, kTcChunk, &s_tcbar[slot]);
+          }
+        }
+        __syncwarp();
+      } else if (warp == 0) {
+        if (lane == 0) {
+          const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(cpad));
+          const uint32_t wbase = smem_u32(s.w);
+          for (int c = 0; c < nch; ++c) {
+            const uint32_t n = tc_seq + static_cast<uint32_t>(c), slot = n % ns, use = n / ns;
+            if (!mbar_wait(&s_tcbar[slot], use & 1u, p.status)) {
+              s_abort = 1;
+              break;
+            }
+            tc_fence_after();
+            const int mt = c / (2 * KB), rem = c - mt * 2 * KB, kk = rem >> 1;
+            const int kb = kk + rot < KB ? kk + rot : kk + rot - KB;
+            const uint32_t a0 = smem_u32(s.ring + static_cast<size_t>(slot) * kTcChunk);
+            const uint32_t b0 = wbase + static_cast<uint32_t>(kb * cpad * 128);
+            const uint32_t d = tmem_base + static_cast<uint32_t>(mt * cpad);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_bf16(d, sdesc_k_sw128(a0 + ks * 32), sdesc_k_sw128(b0 + ks * 32), idesc,
+                          (rem == 0 && ks == 0) ? 0u : 1u);
+            tc_commit(&s_tcbar[4 + slot]);  // the slot is free once these MMAs are done
+          }
+          tc_commit(&s_tcbar[8]);  // every product of the depth is done
+        }
+        __syncwarp();
+      }
+      tc_seq += static_cast<uint32_t>(nch);
+      if (!mbar_wait(&s_tcbar[8], tc_done_ph, p.status)) s_abort = 1;
+      tc_done_ph ^= 1u;
+      __syncwarp();
+      tc_fence_after();
+      // warp w reads lane quarter w%4 (rows 32(w%4)..+31) of the row tiles
+      // w/4, w/4 + 2, ...: the gate rows go to shared memory (phase C), the
+      // W1_S rows to u_W1 (phase B)
+      const int q4 = warp & 3;
+      for (int mt = warp >> 2; mt < tc_nmt; mt += kWarps / 4) {
+        const int st = mt * 128 + q4 * 32 + lane;
+        const int q = st / W, b = st - q * W;
+        const bool ok = st < n_req * W && b < Lp;
+        const uint32_t ta = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(mt * cpad);
+        for (int c0 = 0; c0 < ncol; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(ta + static_cast<uint32_t>(c0), v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c0 + e;
+            if (ok && c < ncol) {
+              const float u = __uint_as_float(v[e]);
+              if (c < 3 * nj) s.uu[static_cast<size_t>(q * Lp + b) * 3 * sh.jper + c] = u;
+              else p.uW1[static_cast<size_t>(q * W + b) * r + r0 + (c - 3 * nj)] = u;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncthreads();
+      if (s_abort) {
+        // a copy or a product that never completed: stop here (every CTA
+        // times out at its next grid barrier)
+        drain();
+        return;
+      }
+    }
     if (sh.mfrag) {
       // several requests: the states as ready-made fragments, block by block
       // (8 states: rows 0-7 of the tile carry the high parts, rows 8-15 the
@@ -620,7 +852,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       if (nblk > 1) load_blk(1);
       for (int rb = 0; rb < nblk; ++rb) {
         const int sb = rb & 1;
+#ifdef DT_CHAIN_TIMING
+        const unsigned long long tw0 = clock64();
+#endif
         if (!mbar_wait(&s_mbar[sb], (mf_phase >> sb) & 1u, p.status)) s_abort = 1;
+#ifdef DT_CHAIN_TIMING
+        blk_wait += clock64() - tw0;
+#endif
         mf_phase ^= 1u << sb;
         __syncthreads();
         if (s_abort) {
@@ -681,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
     }
-    for (int p0 = 0; p0 < (sh.frag || sh.mfrag || p.marginal ? 0 : P); p0 += kPC) {
+    for (int p0 = 0; p0 < (sh.frag || sh.mfrag || sh.tc || p.marginal ? 0 : P); p0 += kPC) {
       const int pc = min(kPC, P - p0);
       __syncthreads();
       // state rows -> bf16 high + low parts (S = hi + lo to ~16 mantissa bits)
@@ -775,10 +1013,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
       }
     }
+    CH_STAMP(i, 1);
+#ifdef DT_CHAIN_TIMING
+    CH_STAMP_SET(i, 7, blk_wait);
+#endif
     if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
       drain();
       return;
     }
+    CH_STAMP(i, 2);
 
     // ================= phase B: corrected log-probs and selections ==========
     const int row_off = p.off[i];
@@ -1335,11 +1578,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           Snext[static_cast<size_t>(q * W + jv) * g + j0 + jj] = hn;
           if (sh.frag || sh.mfrag)
             store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
+          if (sh.tc)
+            store_tc1(reinterpret_cast<uint8_t*>(p.sfrag) + static_cast<size_t>(i & 1) * tc_nmt * (g / 64) * 2 * kTcChunk,
+                      q * W + jv, j0 + jj, g / 64, hn);
         }
       } else if ((dist || blockIdx.x == 0) && p.live_out) {
         for (int j = tid; j < W; j += kThreads) p.live_out[static_cast<size_t>(q) * W + j] = -1;
       }
     }
+    CH_STAMP(i, 3);
     if (dist && !last) {
       // ================= phase C (all requests): GRU of the survivors =====
       // the survivors (node indices) and their tokens come from the
@@ -1348,7 +1595,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         drain();
         return;
       }
-      for (int idx = tid; idx < n_req * Li * nj; idx += kThreads) {
+      CH_STAMP(i, 4);
+      if (sh.tc) {
+        // one survivor row per thread, eight columns at a time: the loads of
+        // a group are issued together, and its high and low parts go out as
+        // one 16-byte piece each
+        uint8_t* sb = reinterpret_cast<uint8_t*>(p.sfrag) + static_cast<size_t>(i & 1) * tc_nmt * (g / 64) * 2 * kTcChunk;
+        for (int qv = tid; qv < n_req * Li; qv += kThreads) {
+          const int q = qv / Li, jv = qv - q * Li;
+          const int node = __ldcg(live_next + static_cast<size_t>(q) * W + jv);
+          const int e = node - row_off;
+          const int tok = (e >= 0 && e < Lp * K) ? __ldcg(p.node_tok + static_cast<size_t>(q) * p.N1 + node) : -1;
+          if (tok < 0 || tok >= p.V) {
+            dt_report(p.status, DT_DEV_BOUNDS);
+            continue;
+          }
+          const int b = e / K;
+          const float* x = p.xtab + static_cast<size_t>(tok) * 3 * g + j0;
+          const float* uu = s.uu + static_cast<size_t>(q * Lp + b) * 3 * sh.jper;
+          const float* hp = Sprev + static_cast<size_t>(q * W + b) * g + j0;
+          float* ho = Snext + static_cast<size_t>(q * W + jv) * g + j0;
+          for (int j8 = 0; j8 < nj; j8 += 8) {
+            float xr[8], xz[8], xn[8], h[8], hn[8];
+#pragma unroll
+            for (int e4 = 0; e4 < 2; ++e4) {
+              *reinterpret_cast<float4*>(xr + 4 * e4) = *reinterpret_cast<const float4*>(x + j8 + 4 * e4);
+              *reinterpret_cast<float4*>(xz + 4 * e4) = *reinterpret_cast<const float4*>(x + g + j8 + 4 * e4);
+              *reinterpret_cast<float4*>(xn + 4 * e4) = *reinterpret_cast<const float4*>(x + 2 * g + j8 + 4 * e4);
+              *reinterpret_cast<float4*>(h + 4 * e4) = *reinterpret_cast<const float4*>(hp + j8 + 4 * e4);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float rg = sigmoidf_(xr[jj] + uu[j8 + jj]);
+              const float zg = sigmoidf_(xz[jj] + uu[nj + j8 + jj]);
+              const float ng = tanhf_(xn[jj] + rg * uu[2 * nj + j8 + jj]);
+              hn[jj] = (1.0f - zg) * ng + zg * h[jj];
+            }
+#pragma unroll
+            for (int e4 = 0; e4 < 2; ++e4)
+              *reinterpret_cast<float4*>(ho + j8 + 4 * e4) = *reinterpret_cast<const float4*>(hn + 4 * e4);
+            store_tc8(sb, q * W + jv, j0 + j8, g / 64, hn);
+          }
+        }
+      }
+      for (int idx = tid; idx < (sh.tc ? 0 : n_req * Li * nj); idx += kThreads) {
         const int qv = idx / nj, jj = idx - qv * nj;
         const int q = qv / Li, jv = qv - q * Li;
         const int node = __ldcg(live_next + static_cast<size_t>(q) * W + jv);
@@ -1371,7 +1661,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
       }
     }
-    if (sh.mfrag && !last) fence_proxy_async_global();  // the next depth bulk-copies these fragments
+    if ((sh.mfrag || sh.tc) && !last) fence_proxy_async_global();  // the next depth bulk-copies these fragments
+    CH_STAMP(i, 5);
     if (i < p.depth_last) {
       if (!sh.dbuf && qfirst < n_req) {
         // stage the next depth's first request of this CTA now: the copies
@@ -1387,6 +1678,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         return;
       }
     }
+    CH_STAMP(i, 6);
   }
 
   // ---- tail: global Top-B and tree/mask of the single request (CTA 0) ----
@@ -1409,6 +1701,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
                 reinterpret_cast<uint32_t*>(s.red), kWarps * 256, s_state, s_tred, s_tscan, p.sel);
     tree_and_mask(p.sel, p.N1, p.B, D, offs, p.node_tok, p.node_parent, p.node_score, nullptr, nodes, par, dep, anc,
                   p.tok, p.parent, p.depth, p.logp_cum, p.mask, p.status);
+  }
+  if (sh.tc) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem_base, tc_cols);
   }
 }
 
@@ -1435,7 +1732,7 @@ bool is_q4b(const ChainParams& p, int grid) {
   return grid == 128 && a.g == b.g && a.r == b.r && a.M == b.M && a.K == b.K && a.W == b.W &&
          a.n_req == b.n_req && a.D == b.D && a.jper == b.jper && a.rper == b.rper && a.cpad == b.cpad &&
          a.stage_w2 == b.stage_w2 && a.mma_b == b.mma_b && a.prefetch == b.prefetch && a.dbuf == b.dbuf &&
-         a.frag == b.frag && a.zf == b.zf;
+         a.frag == b.frag && a.zf == b.zf && a.tc == b.tc;
 }
 
 }  // namespace
@@ -1478,14 +1775,32 @@ void chain_plan(ChainParams& p, int grid) {
   if (p.dbuf && chain_smem_bytes(p) > kBudget) p.dbuf = 0;
   if (p.mma_b && chain_smem_bytes(p) > kBudget) p.mma_b = 0;
   if (!p.mma_b && chain_smem_bytes(p) > kBudget) p.stage_w2 = 0;
+  // tcgen05 phase A: more state rows than one A fragment holds, whole K
+  // blocks of 64, every CTA owning the same whole groups of 8 state columns,
+  // one tile of cpad columns per 128 rows within the 512 tensor-memory
+  // columns, and 2 to 4 chunk slots within the budget
+  p.tc = 0;
+  p.tc_ns = 0;
+  const int nmt = (p.n_req * p.W + 127) / 128;
+  if (!frag_ok(p.n_req, p.W, p.g) && p.g % 64 == 0 && p.jper % 8 == 0 && p.g % p.jper == 0 &&
+      p.g / p.jper == grid && p.cpad % 16 == 0 && p.cpad <= 256 && nmt * p.cpad <= 512) {
+    for (int ns = 4; ns >= 2 && !p.tc; --ns) {
+      p.tc = 1;
+      p.tc_ns = ns;
+      if (chain_smem_bytes(p) > kBudget) {
+        p.tc = 0;
+        p.tc_ns = 0;
+      }
+    }
+  }
 }
 
 bool chain_can_fuse_tree(const ChainParams& p) {
   if (p.n_req != 1) return false;
-  const size_t gp = static_cast<size_t>(kstride(p.g));
-  const size_t weight_bytes = gp * p.cpad * 2;                          // holds the Top-B keys + candidates
-  const size_t red_words = static_cast<size_t>(kWarps) * kPC * p.cpad;  // holds the histograms
-  const size_t state_bytes = gp * kPC * 2 * 2;                          // holds offsets, slots, ancestor rows
+  const SmemSizes L = smem_sizes(runtime_shape(p));
+  const size_t weight_bytes = L.off[1] - L.off[0];     // holds the Top-B keys + candidates
+  const size_t red_words = (L.off[3] - L.off[2]) / 4;  // holds the histograms
+  const size_t state_bytes = L.off[2] - L.off[1];      // holds offsets, slots, ancestor rows
   const size_t S = static_cast<size_t>(p.B) + 1;
   return static_cast<size_t>(p.N1 - 1) * 12 <= weight_bytes && red_words >= static_cast<size_t>(kWarps) * 256 &&
          (static_cast<size_t>(kMaxDepth + 2) + 3 * S + S * anc_words(static_cast<int>(S))) * 4 <= state_bytes;
@@ -1515,3 +1830,14 @@ cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream) {
 }
 
 }  // namespace dt
+
+#ifdef DT_CHAIN_TIMING
+// The phase stamps of the last grid-barrier chain launch: 2 x 66 x 8 values
+// ([CTA 0 / last CTA][depth][stamp], clock64(); the stamps are listed where
+// g_chain_stamps is defined).  Returns the number of values copied, or -1.
+extern "C" int dt_chain_stamps(unsigned long long* out, int n) {
+  const int total = 2 * (dt::kMaxDepth + 2) * dt::kChainStamps;
+  if (!out || n < total) return -1;
+  return cudaMemcpyFromSymbol(out, dt::g_chain_stamps, sizeof(dt::g_chain_stamps)) == cudaSuccess ? total : -1;
+}
+#endif

@@ -95,7 +95,9 @@ void layout(const dt_config& c, const Tables& t, const TopmParams& tp, Layout& L
   put(L.rest_lse, rows * 4);
   put(L.row_done, rows * 4);
   put(L.S, 2ull * c.n_req * c.W * c.g * 4);
-  put(L.sfrag, 2ull * c.n_req * c.W * c.g * 4);
+  // two parities of the states' hi/lo copy; rows padded to whole tiles of 128
+  // for the tcgen05 operand layout
+  put(L.sfrag, 2ull * ((static_cast<size_t>(c.n_req) * c.W + 127) / 128 * 128) * c.g * 4);
   put(L.zfrag, static_cast<size_t>(c.n_req) * c.W * c.r * 4);
   put(L.uW1, static_cast<size_t>(c.n_req) * c.W * c.r * 4);
   put(L.live, 2ull * c.n_req * c.W * 4);
@@ -695,8 +697,8 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   else if (c->use_dchain)
     snprintf(c->plan, sizeof(c->plan), "%sclustered depth chain on %d CTAs: %s", tm, cfg->g / c->dchain_jc, why);
   else
-    snprintf(c->plan, sizeof(c->plan), "%sgrid-barrier depth chain on %d CTAs (clustered chain not used: %s)", tm,
-             c->chain_grid, why);
+    snprintf(c->plan, sizeof(c->plan), "%sgrid-barrier depth chain on %d CTAs%s (clustered chain not used: %s)", tm,
+             c->chain_grid, probe.tc ? ", tcgen05 projection of the states" : "", why);
 
   // tensor maps of the weights
   const dt_config& k = *cfg;

@@ -125,7 +125,9 @@ struct ChainParams {
   float* S;      // [2, n_req*W, g]
   // the same states split into bf16 high + low parts, laid out as mma.sync
   // A fragments: [2][n_req*W][g/16][4 lane groups][hi pair 0, hi pair 1,
-  // lo pair 0, lo pair 1] (used when one request's W rows fit one fragment)
+  // lo pair 0, lo pair 1] (used when one request's W rows fit one fragment);
+  // with tc, as tcgen05 A-operand chunks: [2][row tile of 128][g/64][hi, lo]
+  // chunks of 16 KB (128 rows x 64 bf16, 128-byte swizzled)
   uint32_t* sfrag;
   // z = SiLU(h1_i + u_W1) of the live branches in the same fragment order
   // ([n_req*W][r/16][4][4]), written by the CTAs that own bottleneck rows
@@ -147,6 +149,10 @@ struct ChainParams {
   int stage_w2;       // 1: stage the candidates' W2 rows in shared memory
   int dbuf;           // 1: stage the next depth's candidate data a depth ahead (one request)
   int mma_b;          // 1: corrected logits of all branches as one tensor-core product
+  // 1: phase A on tcgen05 (states as the 128-row A operand, streamed from
+  // sfrag in the 128-byte swizzled K-major layout, accumulators in tensor
+  // memory); tc_ns shared-memory slots of 16 KB for the streamed chunks
+  int tc, tc_ns;
   // tail of a whole-round launch of one request: CTA 0 (which wrote every node
   // array itself) runs the global Top-B and the tree/mask, no extra launch
   int fuse_tree;
