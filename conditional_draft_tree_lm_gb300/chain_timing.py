@@ -161,7 +161,8 @@ def grid_chain_report(lib, b, cfg, args):
     phase A (projections; its waits for state blocks shown apart), the
     barrier after it, phase B (selections; with one request also phase C), the
     barrier before the all-request phase C, phase C, and the depth's last
-    barrier, for CTA 0 and the last CTA."""
+    barrier, for CTA 0 and the last CTA; phase B is split further (scoring,
+    the top-W)."""
     import torch
 
     from . import dtree
@@ -169,8 +170,11 @@ def grid_chain_report(lib, b, cfg, args):
     lib.dt_chain_stamps.restype = ctypes.c_int
     lib.dt_chain_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
     D = cfg.block - 1
-    buf = np.zeros(2 * SLOTS * 8, dtype=np.uint64)
-    acc = []
+    buf = np.zeros(2 * SLOTS * 20, dtype=np.uint64)
+    lib.dt_chain_tcstamps.restype = ctypes.c_int
+    lib.dt_chain_tcstamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    tcb = np.zeros(3 * 128, dtype=np.uint64)
+    acc, tacc = [], []
     for s in range(args.rounds + 3):
         H, r = make_round_inputs(cfg, s)
         Hd = dtree.bf16_tensor(H)
@@ -180,7 +184,9 @@ def grid_chain_report(lib, b, cfg, args):
         if lib.dt_chain_stamps(buf.ctypes.data, buf.size) != buf.size:
             raise SystemExit("dt_chain_stamps failed")
         if s >= 3:
-            acc.append(buf.reshape(2, SLOTS, 8).astype(np.int64).copy())
+            acc.append(buf.reshape(2, SLOTS, 20).astype(np.int64).copy())
+            lib.dt_chain_tcstamps(tcb.ctypes.data, tcb.size)
+            tacc.append(tcb.reshape(3, 128).astype(np.int64).copy())
     st = np.stack(acc)
     us = 1.0 / (args.mhz or 2070.0)
     print(f"{len(acc)} rounds of {cfg.name}; grid-barrier chain; cycles, mean over rounds")
@@ -199,6 +205,26 @@ def grid_chain_report(lib, b, cfg, args):
             tot += np.array(row)
             print(f"{i:5d} " + " ".join(f"{v:8.0f}" for v in row) + f"  {(s6 - t[:, 0]).mean() * us:8.2f}")
         print("us    " + " ".join(f"{v / D * us:8.2f}" for v in tot))
+        if c == 0 and D >= 2:
+            t = np.stack(tacc).mean(axis=0)
+            n = int((t[1] > 0).sum())
+            if n:
+                t0 = t[0, 0]
+                lat = t[1, :n] - t[0, :n]
+                print(f"  tcgen05 phase A, depth 2 ({n} chunks; cycles from the first copy): copy latency "
+                      f"mean {lat.mean():.0f} (min {lat.min():.0f}, max {lat.max():.0f}); data landed at "
+                      + ", ".join(f"{v - t0:.0f}" for v in t[1, :min(n, 12)]) + f" ...; last {t[1, n - 1] - t0:.0f}; "
+                      f"products issued {t[2, 0] - t0:.0f}")
+        mid = k[:, 2:D]
+        if (mid[:, :, 8] > 0).all():
+            sub = lambda a, b: (mid[:, :, b] - mid[:, :, a]).mean() * us
+            print(f"  B (branches spread): scoring {sub(2, 8):.2f} [to the branch {sub(2, 12):.2f}, z {sub(12, 13):.2f}, "
+                  f"logits {sub(13, 14):.2f}, log-partition + keys {sub(14, 15):.2f}, K best {sub(15, 16):.2f}, "
+                  f"children {sub(16, 18):.2f} + {sub(18, 8):.2f}], barrier {sub(8, 9):.2f}, children read back "
+                  f"{sub(9, 10):.2f}, top-W {sub(10, 11):.2f} [threshold {sub(10, 17):.2f}], the rest {sub(11, 3):.2f} us")
+        elif (mid[:, :, 10] > 0).all():
+            sub = lambda a, b: (mid[:, :, b] - mid[:, :, a]).mean() * us
+            print(f"  B: selections {sub(2, 10):.2f}, top-W {sub(10, 11):.2f}, the rest {sub(11, 3):.2f} us")
 
 
 def gemm_report(gs, us):

@@ -72,14 +72,25 @@ constexpr int kZFragMax = 16;    // z fragment loads per lane in phase B: r <= 1
 // dt_chain_stamps copies them out.  Slot layout [CTA 0 / last][depth][phase]:
 // 0 depth start, 1 phase A done, 2 past the barrier after A, 3 phase B done,
 // 4 past the barrier before C (several requests), 5 phase C done, 6 past the
-// depth's last barrier, 7 cycles spent waiting for state blocks in phase A.
+// depth's last barrier, 7 cycles spent waiting for state blocks in phase A;
+// branches scored by different CTAs: 8 scoring done, 9 past the barrier after
+// it; 10 children ready for the top-W, 11 top-W done; inside the scoring of
+// the CTA's first branch: 12 start, 13 z, 14 corrected logits, 15 keys, 16
+// the K best; 17 the top-W's threshold key.  g_chain_tcst: the tcgen05 phase
+// A of depth 2 in CTA 0, per chunk: copy issued, data landed, slot freed.
 #ifdef DT_CHAIN_TIMING
-constexpr int kChainStamps = 8;
+constexpr int kChainStamps = 20;
 __device__ unsigned long long g_chain_stamps[2][kMaxDepth + 2][kChainStamps];
 #define CH_STAMP(depth, k)                                                                       \
   do {                                                                                           \
     if (tid == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1))                            \
       g_chain_stamps[blockIdx.x == 0 ? 0 : 1][depth][k] = static_cast<unsigned long long>(clock64()); \
+  } while (0)
+__device__ unsigned long long g_chain_tcst[3][128];
+#define CH_TCST(which, c, depth)                                                                  \
+  do {                                                                                           \
+    if (blockIdx.x == 0 && (depth) == 2 && (c) < 128)                                            \
+      g_chain_tcst[which][c] = static_cast<unsigned long long>(clock64());                        \
   } while (0)
 #define CH_STAMP_SET(depth, k, v)                                                                \
   do {                                                                                           \
@@ -92,6 +103,9 @@ __device__ unsigned long long g_chain_stamps[2][kMaxDepth + 2][kChainStamps];
   } while (0)
 #define CH_STAMP_SET(depth, k, v) \
   do {                            \
+  } while (0)
+#define CH_TCST(which, c, depth) \
+  do {                           \
   } while (0)
 #endif
 
@@ -120,9 +134,13 @@ struct Shape {
   int ns;
 };
 
-// One streamed A-operand chunk of the tcgen05 phase A: 128 state rows x 64
-// bf16 (one part, high or low, of one K block), 128-byte swizzled.
+// One shared-memory slot of the tcgen05 phase A: a streamed A-operand chunk
+// of 128 (or 64) state rows x 64 bf16 (one part, high or low, of one K
+// block), 128-byte swizzled.
 constexpr int kTcChunk = 16384;
+// Row tile of the tcgen05 phase A: 64 rows when every state row fits one
+// (M = 64 products, half the bytes streamed), else 128.
+DT_HOST_DEVICE_INLINE int tc_tile_shift(int rows) { return rows <= 64 ? 6 : 7; }
 
 DT_HOST_DEVICE_INLINE bool frag_ok(int n_req, int W, int g) {
   return n_req == 1 && W <= kPC && g % (16 * kWarps) == 0 && g / (16 * kWarps) <= kFragMax;
@@ -296,32 +314,43 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
 }
 
 // Byte offset of state (row st, column k) in the tcgen05 A-operand chunks of
-// one parity: chunk (row tile st/128, K block k/64, part), inside it the
-// 128-byte swizzled K-major layout (8-row atoms of 1024 bytes, row st%8 of an
-// atom at 128 st%8, its 16-byte piece k%64/8 at piece (k%64/8) xor (st%8)).
-// The low part's chunk follows the high part's.
-DT_DEVINL size_t tc_off(int st, int k, int KB) {
-  const int mt = st >> 7, rr = st & 127, kb = k >> 6, ch = (k >> 3) & 7;
-  return static_cast<size_t>((mt * KB + kb) * 2) * kTcChunk + (rr >> 3) * 1024 + (rr & 7) * 128 +
+// one parity (row tiles of 2^ts rows, chunks of 2^ts x 128 bytes): chunk (row
+// tile, K block k/64, part), inside it the 128-byte swizzled K-major layout
+// (8-row atoms of 1024 bytes, row rr%8 of an atom at 128 rr%8, its 16-byte
+// piece k%64/8 at piece (k%64/8) xor (rr%8)).  The low part's chunk follows
+// the high part's.
+DT_DEVINL size_t tc_off(int st, int k, int KB, int ts) {
+  const int mt = st >> ts, rr = st & ((1 << ts) - 1), kb = k >> 6, ch = (k >> 3) & 7;
+  return (static_cast<size_t>((mt * KB + kb) * 2) << (ts + 7)) + (rr >> 3) * 1024 + (rr & 7) * 128 +
          ((ch ^ (rr & 7)) << 4) + (k & 7) * 2;
 }
 // One state value: its bf16 high part and the bf16 of the remainder.
-DT_DEVINL void store_tc1(uint8_t* base, int st, int k, int KB, float v) {
+DT_DEVINL void store_tc1(uint8_t* base, int st, int k, int KB, int ts, float v) {
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
   const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-  uint8_t* a = base + tc_off(st, k, KB);
+  uint8_t* a = base + tc_off(st, k, KB, ts);
   *reinterpret_cast<uint16_t*>(a) = __bfloat16_as_ushort(hi);
-  *reinterpret_cast<uint16_t*>(a + kTcChunk) = __bfloat16_as_ushort(lo);
+  *reinterpret_cast<uint16_t*>(a + (1 << (ts + 7))) = __bfloat16_as_ushort(lo);
 }
 // Eight consecutive values (columns k..k+7, k a multiple of 8): one 16-byte
 // piece of each part.
-DT_DEVINL void store_tc8(uint8_t* base, int st, int k, int KB, const float (&v)[8]) {
+DT_DEVINL void store_tc8(uint8_t* base, int st, int k, int KB, int ts, const float (&v)[8]) {
   uint32_t hi[4], lo[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) hi[e] = split_hi_lo(v[2 * e], v[2 * e + 1], lo[e]);
-  uint8_t* a = base + tc_off(st, k, KB);
+  uint8_t* a = base + tc_off(st, k, KB, ts);
   *reinterpret_cast<uint4*>(a) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-  *reinterpret_cast<uint4*>(a + kTcChunk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  *reinterpret_cast<uint4*>(a + (1 << (ts + 7))) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Bring the W2 rows of one depth's candidates (tokens tok[0, M)) into L2,
+// candidate c by CTA c mod G, ahead of the scoring that reads them from L2.
+DT_DEVINL void prefetch_w2_rows(const ChainParams& p, const Shape& sh, const int* tok) {
+  const int G = static_cast<int>(gridDim.x);
+  for (int c = static_cast<int>(blockIdx.x) + G * static_cast<int>(threadIdx.x); c < sh.M; c += G * kThreads)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.w2 + static_cast<size_t>(tok[c]) * sh.r),
+                 "r"(static_cast<uint32_t>(sh.r * 2))
+                 : "memory");
 }
 
 // Read the candidate tokens of one (request, depth) row into shared memory.
@@ -411,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   __shared__ int s_wcnt[kWarps];
   __shared__ uint32_t s_state[4];
   __shared__ float s_tred[64];  // Top-B min/max partials of the tail
-  __shared__ int s_tscan[40];   // Top-B fallback scans
+  __shared__ int s_tscan[40];   // Top-B fallback scans; top-W bin search and scan
+  __shared__ uint64_t s_kth;    // top-W: the Li-th best key
   // tcgen05 phase A: chunk slots full [0..3] / free [4..7], products done [8]
   __shared__ __align__(8) uint64_t s_tcbar[9];
   __shared__ uint32_t s_tmem;
@@ -488,7 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   uint32_t mf_phase = 0;  // completed-phase parity of the two block buffers
   // tcgen05 phase A: tensor-memory columns (one 128-lane tile of cpad fp32
   // columns per 128 state rows), chunks streamed so far, products-done parity
-  const int tc_nmt = (n_req * W + 127) / 128;
+  const int tc_ts = tc_tile_shift(n_req * W), tc_tm = 1 << tc_ts;
+  const int tc_nmt = (n_req * W + tc_tm - 1) / tc_tm;
+  const uint32_t tc_chunk = static_cast<uint32_t>(tc_tm) * 128u;  // bytes of one streamed chunk
   uint32_t tc_cols = 32;
   while (sh.tc && tc_cols < static_cast<uint32_t>(tc_nmt * cpad)) tc_cols <<= 1;
   uint32_t tc_seq = 0, tc_done_ph = 0;
@@ -557,6 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     }
   }
   __syncthreads();
+  // W2 rows read from L2 by the scoring (not staged): the first depth's now,
+  // every later depth's one depth ahead
+  const bool w2_ahead = !p.marginal && !sh.stage_w2 && sh.prefetch && (sh.r * 2) % 16 == 0;
+  if (w2_ahead) prefetch_w2_rows(p, sh, s.tok_all + static_cast<size_t>(p.depth_first - 1) * M);
   // Several requests: CTA c selects for requests c, c + G, ... (G CTAs) and
   // every CTA then updates its state columns of all requests after one more
   // grid barrier.  One request: every CTA selects for it (identically) and
@@ -605,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       const float s0 = (1.0f - zg) * ng;
       p.S[static_cast<size_t>(q * W) * g + jj] = s0;
       if (sh.frag || sh.mfrag) store_frag(p.sfrag, q * W, jj, g / 16, s0);  // parity 0 = depth 0
-      if (sh.tc) store_tc1(reinterpret_cast<uint8_t*>(p.sfrag), q * W, jj, g / 64, s0);
+      if (sh.tc) store_tc1(reinterpret_cast<uint8_t*>(p.sfrag), q * W, jj, g / 64, tc_ts, s0);
     }
     if (sh.mfrag || sh.tc) fence_proxy_async_global();
     if (blockIdx.x == 0) {
@@ -637,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
 #ifdef DT_CHAIN_TIMING
     unsigned long long blk_wait = 0;
 #endif
+    if (w2_ahead && i < p.depth_last) prefetch_w2_rows(p, sh, s.tok_all + static_cast<size_t>(i) * M);
     // one request: the next depth's candidate data is staged now, into the
     // other buffer (its last reader, depth i-1, finished before the barrier);
     // it lands during this depth
@@ -737,50 +774,74 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       const int nch = tc_nmt * KB * 2;
       const int ns = sh.ns;
       const uint8_t* abase = reinterpret_cast<const uint8_t*>(p.sfrag) +
-                             static_cast<size_t>((i - 1) & 1) * tc_nmt * KB * 2 * kTcChunk;
+                             static_cast<size_t>((i - 1) & 1) * tc_nmt * KB * 2 * tc_chunk;
       // every CTA starts at a different K block, so that the CTAs do not all
       // read the same lines at the same time
       const int rot = static_cast<int>(blockIdx.x) % KB;
+      // (a single thread runs each loop: slots, phases and descriptors are
+      // stepped, not recomputed, to keep its dependent instructions few)
       if (warp == 1) {
         if (lane == 0) {
           fence_proxy_async_global();  // the states were written by generic stores
-          for (int c = 0; c < nch; ++c) {
-            const uint32_t n = tc_seq + static_cast<uint32_t>(c), slot = n % ns, use = n / ns;
-            if (use > 0 && !mbar_wait(&s_tcbar[4 + slot], (use - 1) & 1u, p.status)) {
-              s_abort = 1;
-              break;
+          uint32_t slot = tc_seq % static_cast<uint32_t>(ns), use = tc_seq / static_cast<uint32_t>(ns);
+          int c = 0;
+          for (int mt = 0; mt < tc_nmt && !s_abort; ++mt) {
+            for (int kk = 0, kb = rot; kk < KB; ++kk, kb = (kb + 1 == KB ? 0 : kb + 1)) {
+              const uint8_t* src = abase + static_cast<size_t>((mt * KB + kb) * 2) * tc_chunk;
+              for (int part = 0; part < 2; ++part, ++c) {
+                if (use > 0 && !mbar_wait(&s_tcbar[4 + slot], (use - 1) & 1u, p.status)) {
+                  s_abort = 1;
+                  break;
+                }
+                CH_TCST(0, c, i);
+                mbar_arrive_expect_tx(&s_tcbar[slot], tc_chunk);
+                bulk_g2s(s.ring + static_cast<size_t>(slot) * kTcChunk, src + part * tc_chunk, tc_chunk,
+                         &s_tcbar[slot]);
+                if (++slot == static_cast<uint32_t>(ns)) {
+                  slot = 0;
+                  ++use;
+                }
+              }
+              if (s_abort) break;
             }
-            const int mt = c / (2 * KB), rem = c - mt * 2 * KB, kk = rem >> 1, part = rem & 1;
-            const int kb = kk + rot < KB ? kk + rot : kk + rot - KB;
-            mbar_arrive_expect_tx(&s_tcbar[slot], kTcChunk);
-            bulk_g2s(s.ring + static_cast<size_t>(slot) * kTcChunk,
-                     abase + static_cast<size_t>((mt * KB + kb) * 2 + part) * kTcChunk, kTcChunk, &s_tcbar[slot]);
           }
         }
         __syncwarp();
       } else if (warp == 0) {
         if (lane == 0) {
-          const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(cpad));
-          const uint32_t wbase = smem_u32(s.w);
-          for (int c = 0; c < nch; ++c) {
-            const uint32_t n = tc_seq + static_cast<uint32_t>(c), slot = n % ns, use = n / ns;
-            if (!mbar_wait(&s_tcbar[slot], use & 1u, p.status)) {
-              s_abort = 1;
-              break;
-            }
-            tc_fence_after();
-            const int mt = c / (2 * KB), rem = c - mt * 2 * KB, kk = rem >> 1;
-            const int kb = kk + rot < KB ? kk + rot : kk + rot - KB;
-            const uint32_t a0 = smem_u32(s.ring + static_cast<size_t>(slot) * kTcChunk);
-            const uint32_t b0 = wbase + static_cast<uint32_t>(kb * cpad * 128);
+          const uint32_t idesc = idesc_bf16_f32(static_cast<uint32_t>(tc_tm), static_cast<uint32_t>(cpad));
+          // descriptors of slot 0 and of K block 0; a slot is kTcChunk / 16
+          // units further, a K block cpad * 128 / 16, a K step 32 / 16
+          const uint64_t ad0 = sdesc_k_sw128(smem_u32(s.ring)), bd0 = sdesc_k_sw128(smem_u32(s.w));
+          uint32_t slot = tc_seq % static_cast<uint32_t>(ns), use = tc_seq / static_cast<uint32_t>(ns);
+          int c = 0;
+          for (int mt = 0; mt < tc_nmt && !s_abort; ++mt) {
             const uint32_t d = tmem_base + static_cast<uint32_t>(mt * cpad);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc_mma_bf16(d, sdesc_k_sw128(a0 + ks * 32), sdesc_k_sw128(b0 + ks * 32), idesc,
-                          (rem == 0 && ks == 0) ? 0u : 1u);
-            tc_commit(&s_tcbar[4 + slot]);  // the slot is free once these MMAs are done
+            for (int kk = 0, kb = rot; kk < KB; ++kk, kb = (kb + 1 == KB ? 0 : kb + 1)) {
+              const uint64_t bd = bd0 + static_cast<uint64_t>(kb * cpad * 8);
+              for (int part = 0; part < 2; ++part, ++c) {
+                if (!mbar_wait(&s_tcbar[slot], use & 1u, p.status)) {
+                  s_abort = 1;
+                  break;
+                }
+                CH_TCST(1, c, i);
+                tc_fence_after();
+                const uint64_t ad = ad0 + static_cast<uint64_t>(slot * (kTcChunk / 16));
+                tc_mma_bf16(d, ad, bd, idesc, (kk | part) != 0 ? 1u : 0u);
+                tc_mma_bf16(d, ad + 2, bd + 2, idesc, 1u);
+                tc_mma_bf16(d, ad + 4, bd + 4, idesc, 1u);
+                tc_mma_bf16(d, ad + 6, bd + 6, idesc, 1u);
+                tc_commit(&s_tcbar[4 + slot]);  // the slot is free once these MMAs are done
+                if (++slot == static_cast<uint32_t>(ns)) {
+                  slot = 0;
+                  ++use;
+                }
+              }
+              if (s_abort) break;
+            }
           }
           tc_commit(&s_tcbar[8]);  // every product of the depth is done
+          CH_TCST(2, 0, i);
         }
         __syncwarp();
       }
@@ -789,14 +850,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       tc_done_ph ^= 1u;
       __syncwarp();
       tc_fence_after();
-      // warp w reads lane quarter w%4 (rows 32(w%4)..+31) of the row tiles
-      // w/4, w/4 + 2, ...: the gate rows go to shared memory (phase C), the
-      // W1_S rows to u_W1 (phase B)
+      // warp w reads lane quarter w%4 of the row tiles w/4, w/4 + 2, ...: of
+      // a 128-row tile, rows 32(w%4)..+31 in its 32 lanes; of a 64-row tile,
+      // rows 16(w%4)..+15 in its first 16 lanes.  The gate rows go to shared
+      // memory (phase C), the W1_S rows to u_W1 (phase B).
       const int q4 = warp & 3;
       for (int mt = warp >> 2; mt < tc_nmt; mt += kWarps / 4) {
-        const int st = mt * 128 + q4 * 32 + lane;
+        const int st = mt * tc_tm + (tc_tm == 128 ? q4 * 32 + lane : q4 * 16 + lane);
         const int q = st / W, b = st - q * W;
-        const bool ok = st < n_req * W && b < Lp;
+        const bool ok = (tc_tm == 128 || lane < 16) && st < n_req * W && b < Lp;
         const uint32_t ta = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(mt * cpad);
         for (int c0 = 0; c0 < ncol; c0 += 16) {
           uint32_t v[16];
@@ -1281,8 +1343,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         int* win = s.crank;        // [K]
         for (int b = blockIdx.x; b < Lp; b += gridDim.x) {
           const float* u = p.uW1 + static_cast<size_t>(b) * r;
+          CH_STAMP(i, 12);
           for (int k = tid; k < r; k += kThreads) zv[k] = siluf_(s.h1s[k] + __ldcg(u + k));
           __syncthreads();
+          CH_STAMP(i, 13);
           // one candidate per thread: its W2 row from L2, z from shared memory
           float lmax_t = -INFINITY;
           for (int c = tid; c < M; c += kThreads) {
@@ -1301,6 +1365,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           lmax_t = warp_max(lmax_t);
           if (lane == 0) s_tred[warp] = lmax_t;
           __syncthreads();
+          CH_STAMP(i, 14);
           float lmax = rest;
           for (int w8 = 0; w8 < kWarps; ++w8) lmax = fmaxf(lmax, s_tred[w8]);
           float se_t = 0.0f;
@@ -1317,11 +1382,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
             keys[c] = rank_key(lp, static_cast<uint32_t>(s.ctk[c]));
           }
           __syncthreads();
+          CH_STAMP(i, 15);
           // the K best (ties to the lower token id), then in token order
           block_rank_all(keys, M, [&](int e, uint64_t, int rk) {
             if (rk < K) win[rk] = e;
           });
           __syncthreads();
+          CH_STAMP(i, 16);
           if (warp == 0) {
             int c = lane < K ? win[lane] : 0;
             if (c < 0 || c >= M) {
@@ -1340,12 +1407,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               p.node_score[nidx] = s.pscore[b] + lp;
             }
           }
+          CH_STAMP(i, 18);
           __syncthreads();  // z, lambda, keys are free for the next branch
         }
+        CH_STAMP(i, 8);
         if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
           drain();
           return;
         }
+        CH_STAMP(i, 9);
         // every child of the depth, from the node arrays
         for (int e = tid; e < nchild; e += kThreads) {
           const size_t nidx = static_cast<size_t>(row_off) + e;
@@ -1478,6 +1548,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           p.node_score[nb + e] = s.cscore[e];
         }
       }
+      CH_STAMP(i, 10);
       if (!last) {
         // top-W of the depth by (score desc, node index asc); survivors ascending
         if (nchild <= 64) {
@@ -1522,6 +1593,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
             for (int w2 = 0; w2 < warp; ++w2) pos += s_wcnt[w2];
             s.surv[q * W + pos] = tid;
           }
+        } else if ((nchild + kThreads - 1) / kThreads <= 32) {
+          // many children: the Li-th best (score, node index) key by a value
+          // histogram (block_kth_rank_key); the survivors, the keys at or
+          // above it, are placed in slot order by a block scan over
+          // consecutive children per thread
+          const int npad = pow2_at_least(nchild);
+          uint32_t* hist = reinterpret_cast<uint32_t*>(s.wkey);  // 256 words, then the bin's keys
+          uint64_t* bnd = s.wkey + 128;
+          const uint64_t kth =
+              block_kth_rank_key(s.cscore, nchild, Li, hist, bnd, npad - 128, s_tred, s_tscan, &s_kth);
+          CH_STAMP(i, 17);
+          const int per = (nchild + kThreads - 1) / kThreads, e0 = tid * per;
+          int nsv = 0;
+          uint32_t msk = 0u;
+          for (int j = 0; j < per; ++j) {
+            const int e = e0 + j;
+            if (e < nchild && rank_key(s.cscore[e], static_cast<uint32_t>(e)) >= kth) {
+              msk |= 1u << j;
+              ++nsv;
+            }
+          }
+          int tot;
+          int pos = block_exclusive_scan(nsv, s_tscan, &tot);
+          for (int j = 0; j < per; ++j)
+            if ((msk >> j) & 1u) s.surv[q * W + pos++] = e0 + j;
         } else {
           const int npad = pow2_at_least(nchild);
           for (int e = tid; e < npad; e += kThreads)
@@ -1552,6 +1648,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           }
         }
         __syncthreads();
+        CH_STAMP(i, 11);
         if (dist || blockIdx.x == 0) {
           for (int j = tid; j < W; j += kThreads) {
             const int node = j < Li ? row_off + s.surv[q * W + j] : -1;
@@ -1579,8 +1676,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           if (sh.frag || sh.mfrag)
             store_frag(p.sfrag + static_cast<size_t>(i & 1) * n_req * W * g, q * W + jv, j0 + jj, g / 16, hn);
           if (sh.tc)
-            store_tc1(reinterpret_cast<uint8_t*>(p.sfrag) + static_cast<size_t>(i & 1) * tc_nmt * (g / 64) * 2 * kTcChunk,
-                      q * W + jv, j0 + jj, g / 64, hn);
+            store_tc1(reinterpret_cast<uint8_t*>(p.sfrag) + static_cast<size_t>(i & 1) * tc_nmt * (g / 64) * 2 * tc_chunk,
+                      q * W + jv, j0 + jj, g / 64, tc_ts, hn);
         }
       } else if ((dist || blockIdx.x == 0) && p.live_out) {
         for (int j = tid; j < W; j += kThreads) p.live_out[static_cast<size_t>(q) * W + j] = -1;
@@ -1600,7 +1697,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         // one survivor row per thread, eight columns at a time: the loads of
         // a group are issued together, and its high and low parts go out as
         // one 16-byte piece each
-        uint8_t* sb = reinterpret_cast<uint8_t*>(p.sfrag) + static_cast<size_t>(i & 1) * tc_nmt * (g / 64) * 2 * kTcChunk;
+        uint8_t* sb = reinterpret_cast<uint8_t*>(p.sfrag) + static_cast<size_t>(i & 1) * tc_nmt * (g / 64) * 2 * tc_chunk;
         for (int qv = tid; qv < n_req * Li; qv += kThreads) {
           const int q = qv / Li, jv = qv - q * Li;
           const int node = __ldcg(live_next + static_cast<size_t>(q) * W + jv);
@@ -1634,7 +1731,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
 #pragma unroll
             for (int e4 = 0; e4 < 2; ++e4)
               *reinterpret_cast<float4*>(ho + j8 + 4 * e4) = *reinterpret_cast<const float4*>(hn + 4 * e4);
-            store_tc8(sb, q * W + jv, j0 + j8, g / 64, hn);
+            store_tc8(sb, q * W + jv, j0 + j8, g / 64, tc_ts, hn);
           }
         }
       }
@@ -1839,5 +1936,11 @@ extern "C" int dt_chain_stamps(unsigned long long* out, int n) {
   const int total = 2 * (dt::kMaxDepth + 2) * dt::kChainStamps;
   if (!out || n < total) return -1;
   return cudaMemcpyFromSymbol(out, dt::g_chain_stamps, sizeof(dt::g_chain_stamps)) == cudaSuccess ? total : -1;
+}
+// The tcgen05 phase A of depth 2 in CTA 0: [copy issued / data landed /
+// (slot 0) products of the depth issued][chunk], clock64().
+extern "C" int dt_chain_tcstamps(unsigned long long* out, int n) {
+  if (!out || n < 3 * 128) return -1;
+  return cudaMemcpyFromSymbol(out, dt::g_chain_tcst, sizeof(dt::g_chain_tcst)) == cudaSuccess ? 3 * 128 : -1;
 }
 #endif

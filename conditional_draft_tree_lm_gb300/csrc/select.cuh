@@ -135,4 +135,99 @@ DT_DEVINL void block_rank_all(const uint64_t* keys, int c, Fn fn) {
   }
 }
 
+// The m-th largest of the n keys rank_key(v[e], e) (values v in shared
+// memory; 1 <= m <= n; the keys are distinct, a tie in value going to the
+// lower index).  A 256-bin histogram over the value range [lo, hi] (bin 0
+// holds the largest values) locates the bin that holds it; that bin's keys
+// are gathered (at most bnd_cap; beyond that every key of the bin is ranked
+// against the whole bin instead) and ranked exactly.  `hist` holds 256
+// words, `red` 2 x (warps) floats, `sc` 3 ints, `s_key` one key.  Every thread
+// of the block calls it and receives the key.
+DT_DEVINL uint64_t block_kth_rank_key(const float* v, int n, int m, uint32_t* hist, uint64_t* bnd, int bnd_cap,
+                                      float* red, int* sc, uint64_t* s_key) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x, nw = nt >> 5;
+  float lo = INFINITY, hi = -INFINITY;
+  for (int e = tid; e < n; e += nt) {
+    lo = fminf(lo, v[e]);
+    hi = fmaxf(hi, v[e]);
+  }
+  lo = -warp_max(-lo);
+  hi = warp_max(hi);
+  if (lane == 0) {
+    red[warp] = lo;
+    red[nw + warp] = hi;
+  }
+  for (int b = tid; b < 256; b += nt) hist[b] = 0u;
+  if (tid == 0) {
+    sc[0] = 0;
+    sc[1] = 0;
+    sc[2] = 0;
+  }
+  __syncthreads();
+  lo = INFINITY;
+  hi = -INFINITY;
+  for (int w = 0; w < nw; ++w) {
+    lo = fminf(lo, red[w]);
+    hi = fmaxf(hi, red[nw + w]);
+  }
+  const float scale = hi > lo ? 256.0f / (hi - lo) : 0.0f;
+  auto bin_of = [&](float x) { return min(255, max(0, __float2int_rz((hi - x) * scale))); };
+  for (int e = tid; e < n; e += nt) atomicAdd(&hist[bin_of(v[e])], 1u);
+  __syncthreads();
+  if (warp == 0) {
+    // lane l totals bins 8l .. 8l+7; the first bin where the running count
+    // reaches m holds the m-th key
+    uint32_t c8[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c8[j] = hist[8 * lane + j];
+      sum += c8[j];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(m));
+    if (hit && lane == __ffs(hit) - 1) {
+      uint32_t cum = incl - sum;
+      for (int j = 0; j < 8; ++j) {
+        if (cum + c8[j] >= static_cast<uint32_t>(m)) {
+          sc[0] = 8 * lane + j;
+          sc[1] = static_cast<int>(cum);
+          break;
+        }
+        cum += c8[j];
+      }
+    }
+  }
+  __syncthreads();
+  const int bt = sc[0];
+  const int need = m - sc[1];  // the need-th largest key of bin bt
+  for (int e = tid; e < n; e += nt) {
+    if (bin_of(v[e]) == bt) {
+      const int at = atomicAdd(&sc[2], 1);
+      if (at < bnd_cap) bnd[at] = rank_key(v[e], static_cast<uint32_t>(e));
+    }
+  }
+  __syncthreads();
+  const int nb = sc[2];
+  if (nb <= bnd_cap) {
+    block_rank_all(bnd, nb, [&](int, uint64_t ke, int rk) {
+      if (rk == need - 1) *s_key = ke;
+    });
+  } else {
+    for (int e = tid; e < n; e += nt) {
+      if (bin_of(v[e]) != bt) continue;
+      const uint64_t k = rank_key(v[e], static_cast<uint32_t>(e));
+      int rk = 0;
+      for (int f = 0; f < n; ++f) rk += (bin_of(v[f]) == bt && rank_key(v[f], static_cast<uint32_t>(f)) > k) ? 1 : 0;
+      if (rk == need - 1) *s_key = k;
+    }
+  }
+  __syncthreads();
+  return *s_key;
+}
+
 }  // namespace dt
