@@ -690,6 +690,8 @@ dt_status dt_create(const dt_config* cfg, const dt_weights* w, void* stream, dt_
   char tm[96];
   if (c->fuse_topm)
     snprintf(tm, sizeof(tm), "Top-M in the LM-head GEMM's epilogue (%d CTA lists merged); ", c->fmerge.S);
+  else if (c->topm.rowwise)
+    snprintf(tm, sizeof(tm), "Top-M kernel streaming each row in one CTA; ");
   else
     snprintf(tm, sizeof(tm), "Top-M kernel on %d chunks per row; ", c->topm.S);
   if (c->best_first)

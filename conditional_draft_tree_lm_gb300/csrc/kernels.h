@@ -89,6 +89,8 @@ struct TopmParams {
   unsigned* clear_word;  // or null: a word the kernel sets to zero (the next chain's barrier counter)
   int pdl;               // 1: launched as a programmatic dependent of the previous kernel
   int occ2;              // 1: the two-CTAs-per-SM build (grids of several waves)
+  int rowwise;           // 1: one CTA per SM streams whole rows (many rows); no partial lists
+  int num_sms;           // the SM count topm_plan planned for
 };
 void topm_plan(TopmParams& p, int num_sms);
 size_t topm_partial_smem(const TopmParams& p);

@@ -707,6 +707,218 @@ __global__ void __launch_bounds__(kThreads, 1) k_topm_merge(const TopmParams p) 
   merge_row(p, static_cast<int>(blockIdx.x), ms, 1.0f / p.T, false);
 }
 
+// Many rows (at least one per SM): two CTAs per SM stream whole rows (rows
+// blockIdx.x, + gridDim.x, ...) through kRowStages shared-memory slots filled
+// by bulk copies of kRowSub tiles each, tile by tile.  A logit whose
+// (value, lowest token) key exceeds the row's running bound tau is appended
+// to a candidate buffer; every other one is a loser and feeds the thread's
+// running log-partition sum.  When the buffer could overflow with the next
+// tile (and after the row's last), it is cut to its M best (block_kth_key):
+// the cut entries feed a second running sum and tau becomes the M-th key, so
+// later logits enter only when they beat it.  The M kept are ranked among
+// themselves; the two sums of every thread give rest_lse.  No partial lists
+// and no merge.
+constexpr int kRowVals = 8;                         // logits per thread and tile
+constexpr int kRowTile = kThreads * kRowVals;       // 4096 logits, 16 KB
+constexpr int kRowSub = 1;                          // tiles per copy
+constexpr int kRowStages = 3;
+constexpr int kRowCap = kRowTile + 2 * kCandCap;    // candidate buffer (keys)
+
+DT_DEVINL void row_bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_topm_rows(const TopmParams p) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ uint32_t hist[256];
+  __shared__ int sc[4];
+  __shared__ float red[kWarps + 1];
+  __shared__ float red4[2 * kWarps];
+  __shared__ int s_cnt, s_keep, s_abort;
+  __shared__ uint64_t s_key;
+  __shared__ __align__(8) uint64_t s_full[kRowStages];
+  float* ring = reinterpret_cast<float*>(dyn);  // [kRowStages][kRowSub kRowTile]
+  uint64_t* buf = reinterpret_cast<uint64_t*>(ring + kRowStages * kRowSub * kRowTile);  // [kRowCap] candidates
+  uint64_t* bnd = buf + kRowCap;  // [kMergeCap] block_kth_key's bin, then the kept keys
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int V = p.V, M = p.M, G = static_cast<int>(gridDim.x);
+  const float invT = 1.0f / p.T;
+  const int nt = (V + kRowTile - 1) / kRowTile;  // tiles per row
+  const int ncp = (nt + kRowSub - 1) / kRowSub;  // copies per row
+  const int my_rows = (p.rows - static_cast<int>(blockIdx.x) + G - 1) / G;
+  const int total = my_rows * nt;                // tiles of this CTA, row after row
+  const int ncopies = my_rows * ncp;
+  if (tid == 0) {
+    for (int b = 0; b < kRowStages; ++b) mbar_init(&s_full[b], 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  TOPM_STAMP(0, 0);
+  dt_grid_wait();  // the logits come from the previous kernel
+  dt_grid_release();
+  TOPM_STAMP(0, 1);
+  if (p.clear_word && blockIdx.x == 0 && tid == 0) *p.clear_word = 0u;
+  __syncthreads();
+  // copy c of this CTA: row blockIdx.x + (c / ncp) G, its tiles from
+  // kRowSub (c % ncp) on, into slot c % kRowStages
+  auto issue = [&](int c) {
+    const int row = static_cast<int>(blockIdx.x) + (c / ncp) * G, t0 = (c - (c / ncp) * ncp) * kRowSub;
+    const int n = min(kRowSub * kRowTile, V - t0 * kRowTile);
+    row_bulk_load(ring + (c % kRowStages) * kRowSub * kRowTile, p.logits + static_cast<size_t>(row) * V + t0 * kRowTile,
+                  static_cast<uint32_t>(n) * 4u, &s_full[c % kRowStages]);
+  };
+  // slot b's copies are issued by lane 0 of warp b
+  if (lane == 0 && (tid >> 5) < min(ncopies, kRowStages)) issue(tid >> 5);
+  float mt = 0.0f, st = 0.0f, me = 0.0f, se = 0.0f, tauv = 0.0f;
+  uint64_t tau = 0ull;
+  // the buffer down to its M best: the rest feed (me, se); tau = the M-th key
+  auto cut = [&]() {
+    const int n = s_cnt;
+    const uint64_t kth = block_kth_key<0>(buf, n, M, hist, sc, bnd, red4, &s_key);
+    if (kth == 0ull) return;  // at most M candidates: nothing to cut
+    if (tid == 0) s_keep = 0;
+    __syncthreads();
+    for (int e = tid; e < n; e += kThreads) {
+      const uint64_t k = buf[e];
+      if (k >= kth) {
+        bnd[atomicAdd(&s_keep, 1)] = k;
+      } else {
+        const float l = key_f32(static_cast<uint32_t>(k >> 32)) * invT;
+        if (l > me) {
+          se = (me > -INFINITY ? se * expf(me - l) : 0.0f) + 1.0f;
+          me = l;
+        } else {
+          se += expf(l - me);
+        }
+      }
+    }
+    __syncthreads();
+    const int nk = s_keep;
+    for (int e = tid; e < nk; e += kThreads) buf[e] = bnd[e];
+    if (tid == 0) s_cnt = nk;
+    tau = kth;
+    tauv = key_f32(static_cast<uint32_t>(kth >> 32));
+    __syncthreads();
+  };
+  for (int q = 0, rn = 0, t = 0; q < total; ++q, t = (t + 1 == nt ? 0 : t + 1), rn += (t == 0 ? 1 : 0)) {
+    const int row = static_cast<int>(blockIdx.x) + rn * G;  // the CTA's rn-th row, its tile t
+    if (t == 0) {
+      // a new row: losers' and cut entries' sums, the bound, the buffer
+      mt = -INFINITY;
+      st = 0.0f;
+      me = -INFINITY;
+      se = 0.0f;
+      tau = 0ull;
+      tauv = -INFINITY;
+      if (tid == 0) s_cnt = 0;
+    }
+    const int c = rn * ncp + t / kRowSub, sub = t % kRowSub;  // the tile's copy, its place in it
+    const int slot = c % kRowStages;
+    // one thread waits for the copy; the barrier releases the others
+#ifdef DT_TOPM_TIMING
+    if (tid == 0 && blockIdx.x == 0 && q < kTopmStampSplits) g_topm_stamps[1][q][0] = dt_globaltimer();
+#endif
+    if (sub == 0 && tid == 0 && !mbar_wait(&s_full[slot], static_cast<uint32_t>(c / kRowStages) & 1u, p.status))
+      s_abort = 1;
+#ifdef DT_TOPM_TIMING
+    if (tid == 0 && blockIdx.x == 0 && q < kTopmStampSplits) g_topm_stamps[1][q][1] = dt_globaltimer();
+#endif
+    __syncthreads();
+    if (s_abort) return;  // a copy that never landed (reported): nothing more is issued or read
+    // logits e = t kRowTile + 4 (h kThreads + tid) + {0..3}, h = 0, 1; -inf
+    // past the row's end (the slot's bytes there are stale)
+    float v[kRowVals];
+#pragma unroll
+    for (int h = 0; h < kRowVals / 4; ++h) {
+      const int j = 4 * (h * kThreads + tid);
+      const float4 f = *reinterpret_cast<const float4*>(ring + (slot * kRowSub + sub) * kRowTile + j);
+      const int e = t * kRowTile + j;
+      v[4 * h] = e < V ? f.x : -INFINITY;
+      v[4 * h + 1] = e + 1 < V ? f.y : -INFINITY;
+      v[4 * h + 2] = e + 2 < V ? f.z : -INFINITY;
+      v[4 * h + 3] = e + 3 < V ? f.w : -INFINITY;
+    }
+    float tm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kRowVals; ++u) tm = fmaxf(tm, v[u]);
+    tm *= invT;
+    if (tm > mt) {
+      st = mt > -INFINITY ? st * __expf(mt - tm) : 0.0f;
+      mt = tm;
+    }
+    // the losers' exponentials in four independent sums; a logit at or
+    // above tau's value (rare once the bound has risen) is checked by its
+    // exact key, and the warp's appends take one atomic (a prefix sum of the
+    // lanes' counts)
+    float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const float mref = mt > -INFINITY ? mt : 0.0f;  // (past the row's end: -inf, adds 0)
+    uint32_t fl = 0u;
+#pragma unroll
+    for (int u = 0; u < kRowVals; ++u) {
+      const int e = t * kRowTile + 4 * ((u >> 2) * kThreads + tid) + (u & 3);
+      if (v[u] >= tauv && e < V && rank_key(v[u], static_cast<uint32_t>(e)) > tau)
+        fl |= 1u << u;
+      else
+        s4[u & 3] += __expf(v[u] * invT - mref);
+    }
+    if (__any_sync(0xFFFFFFFFu, fl != 0u)) {
+      const int cnt = __popc(fl);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&s_cnt, wtot);
+      base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+      for (int u = 0; u < kRowVals; ++u)
+        if ((fl >> u) & 1u) {
+          const int e = t * kRowTile + 4 * ((u >> 2) * kThreads + tid) + (u & 3);
+          buf[base++] = rank_key(v[u], static_cast<uint32_t>(e));
+        }
+    }
+    st += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    __syncthreads();  // the copy's last tile is read: refill its slot
+    if ((sub == kRowSub - 1 || t + 1 == nt) && tid == 32 * slot && c + kRowStages < ncopies) issue(c + kRowStages);
+    if (q == 0) TOPM_STAMP(0, 2);
+#ifdef DT_TOPM_TIMING
+    if (tid == 0 && blockIdx.x == 0 && q < kTopmStampSplits) g_topm_stamps[1][q][2] = dt_globaltimer();
+#endif
+    if (s_cnt + kRowTile > kRowCap || t + 1 == nt) cut();
+    if (q == 0) TOPM_STAMP(0, 3);
+#ifdef DT_TOPM_TIMING
+    if (tid == 0 && blockIdx.x == 0 && q < kTopmStampSplits) g_topm_stamps[1][q][3] = dt_globaltimer();
+#endif
+    if (t + 1 < nt) continue;
+    if (q + 1 == nt) TOPM_STAMP(0, 4);
+    // the row's M kept, in rank order (value desc, lower token first)
+    const int nk = s_cnt;
+    rank_all(buf, nk, [&](int, uint64_t ke, int rk) {
+      if (rk < M) {
+        p.cand_tok[static_cast<size_t>(row) * M + rk] = static_cast<int>(rank_key_id(ke));
+        p.cand_base[static_cast<size_t>(row) * M + rk] = key_f32(static_cast<uint32_t>(ke >> 32));
+      }
+    });
+    // log-partition of everything but the M best: the two sums of every thread
+    const float gmax = block_max(fmaxf(mt, me), red);
+    float rest = (mt > -INFINITY ? st * expf(mt - gmax) : 0.0f) + (me > -INFINITY ? se * expf(me - gmax) : 0.0f);
+    rest = block_sum(rest, red);
+    if (tid == 0) {
+      if (nk < M) dt_report(p.status, DT_DEV_BOUNDS);
+      p.rest_lse[row] = rest > 0.0f ? gmax + logf(rest) : -INFINITY;
+    }
+    if (q + 1 == nt) TOPM_STAMP(0, 5);
+    __syncthreads();  // the buffer is reset by the next row
+  }
+}
+
 }  // namespace
 
 void topm_plan(TopmParams& p, int num_sms) {
@@ -719,6 +931,9 @@ void topm_plan(TopmParams& p, int num_sms) {
   p.S = S;
   p.chunk = (p.V + S - 1) / S;
   p.occ2 = S * p.rows > num_sms ? 1 : 0;  // more than one wave at one CTA per SM
+  // at least one row per SM: one CTA per SM streams whole rows instead
+  p.rowwise = (p.rows >= num_sms && p.M <= kCandCap && p.V >= 2 * p.M && p.V % 4 == 0) ? 1 : 0;
+  p.num_sms = num_sms;
 }
 
 size_t topm_partial_smem(const TopmParams&) {
@@ -727,8 +942,13 @@ size_t topm_partial_smem(const TopmParams&) {
 
 size_t topm_merge_smem(const TopmParams& p) { return topm_partial_smem(p); }
 
+size_t topm_rows_smem() {
+  return static_cast<size_t>(kRowStages) * kRowSub * kRowTile * 4 + static_cast<size_t>(kRowCap + kMergeCap) * 8;
+}
+
 cudaError_t topm_prepare() {
   cudaError_t e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm<1>));
+  if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm_rows));
   if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm<2>));
   if (e == cudaSuccess) e = dt_allow_max_dynamic_smem(reinterpret_cast<const void*>(k_topm_merge));
   return e;
@@ -768,18 +988,22 @@ cudaError_t launch_topm_merge(const TopmParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, k_topm_merge, p);
 }
 
-cudaError_t launch_topm(const TopmParams& p, cudaStream_t stream) {
-  if (topm_unsupported(p)) return cudaErrorInvalidValue;
+cudaError_t launch_topm(const TopmParams& p_in, cudaStream_t stream) {
+  if (topm_unsupported(p_in)) return cudaErrorInvalidValue;
+  TopmParams p = p_in;
+  // the row-streaming kernel bulk-copies whole rows: 16-byte aligned logits
+  if (p.rowwise && (reinterpret_cast<uintptr_t>(p.logits) & 15u) != 0) p.rowwise = 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.S, p.rows);
+  cfg.gridDim = p.rowwise ? dim3(std::min(p.rows, 2 * p.num_sms)) : dim3(p.S, p.rows);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = topm_partial_smem(p);
+  cfg.dynamicSmemBytes = p.rowwise ? topm_rows_smem() : topm_partial_smem(p);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
+  if (p.rowwise) return cudaLaunchKernelEx(&cfg, k_topm_rows, p);
   return p.occ2 ? cudaLaunchKernelEx(&cfg, k_topm<2>, p) : cudaLaunchKernelEx(&cfg, k_topm<1>, p);
 }
 
