@@ -771,38 +771,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
                   i + 1 != D);
       const int KB = g / 64;
-      const int nch = tc_nmt * KB * 2;
       const int ns = sh.ns;
       const uint8_t* abase = reinterpret_cast<const uint8_t*>(p.sfrag) +
                              static_cast<size_t>((i - 1) & 1) * tc_nmt * KB * 2 * tc_chunk;
       // every CTA starts at a different K block, so that the CTAs do not all
       // read the same lines at the same time
       const int rot = static_cast<int>(blockIdx.x) % KB;
-      // (a single thread runs each loop: slots, phases and descriptors are
-      // stepped, not recomputed, to keep its dependent instructions few)
+      // A slot holds both parts of one K block (one copy, eight MMAs, one
+      // wait and one commit); a single thread runs each loop, with slots,
+      // phases and descriptors stepped, not recomputed, to keep its
+      // dependent instructions few.
+      const uint32_t pair = 2u * tc_chunk;
+      const uint32_t nsl = min(4u, max(1u, static_cast<uint32_t>(ns) * kTcChunk / pair));
       if (warp == 1) {
         if (lane == 0) {
           fence_proxy_async_global();  // the states were written by generic stores
-          uint32_t slot = tc_seq % static_cast<uint32_t>(ns), use = tc_seq / static_cast<uint32_t>(ns);
+          uint32_t slot = tc_seq % nsl, use = tc_seq / nsl;
           int c = 0;
           for (int mt = 0; mt < tc_nmt && !s_abort; ++mt) {
-            for (int kk = 0, kb = rot; kk < KB; ++kk, kb = (kb + 1 == KB ? 0 : kb + 1)) {
-              const uint8_t* src = abase + static_cast<size_t>((mt * KB + kb) * 2) * tc_chunk;
-              for (int part = 0; part < 2; ++part, ++c) {
-                if (use > 0 && !mbar_wait(&s_tcbar[4 + slot], (use - 1) & 1u, p.status)) {
-                  s_abort = 1;
-                  break;
-                }
-                CH_TCST(0, c, i);
-                mbar_arrive_expect_tx(&s_tcbar[slot], tc_chunk);
-                bulk_g2s(s.ring + static_cast<size_t>(slot) * kTcChunk, src + part * tc_chunk, tc_chunk,
-                         &s_tcbar[slot]);
-                if (++slot == static_cast<uint32_t>(ns)) {
-                  slot = 0;
-                  ++use;
-                }
+            for (int kk = 0, kb = rot; kk < KB; ++kk, kb = (kb + 1 == KB ? 0 : kb + 1), ++c) {
+              if (use > 0 && !mbar_wait(&s_tcbar[4 + slot], (use - 1) & 1u, p.status)) {
+                s_abort = 1;
+                break;
               }
-              if (s_abort) break;
+              CH_TCST(0, c, i);
+              mbar_arrive_expect_tx(&s_tcbar[slot], pair);
+              bulk_g2s(s.ring + static_cast<size_t>(slot) * pair, abase + static_cast<size_t>((mt * KB + kb) * 2) * tc_chunk,
+                       pair, &s_tcbar[slot]);
+              if (++slot == nsl) {
+                slot = 0;
+                ++use;
+              }
             }
           }
         }
@@ -810,34 +809,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       } else if (warp == 0) {
         if (lane == 0) {
           const uint32_t idesc = idesc_bf16_f32(static_cast<uint32_t>(tc_tm), static_cast<uint32_t>(cpad));
-          // descriptors of slot 0 and of K block 0; a slot is kTcChunk / 16
-          // units further, a K block cpad * 128 / 16, a K step 32 / 16
+          // descriptors of slot 0 and of K block 0 (16-byte units): a slot is
+          // pair / 16 further, the low part tc_chunk / 16, a K block
+          // cpad * 128 / 16, a K step 32 / 16
           const uint64_t ad0 = sdesc_k_sw128(smem_u32(s.ring)), bd0 = sdesc_k_sw128(smem_u32(s.w));
-          uint32_t slot = tc_seq % static_cast<uint32_t>(ns), use = tc_seq / static_cast<uint32_t>(ns);
+          const uint64_t lo_off = tc_chunk / 16;
+          uint32_t slot = tc_seq % nsl, use = tc_seq / nsl;
           int c = 0;
           for (int mt = 0; mt < tc_nmt && !s_abort; ++mt) {
             const uint32_t d = tmem_base + static_cast<uint32_t>(mt * cpad);
-            for (int kk = 0, kb = rot; kk < KB; ++kk, kb = (kb + 1 == KB ? 0 : kb + 1)) {
-              const uint64_t bd = bd0 + static_cast<uint64_t>(kb * cpad * 8);
-              for (int part = 0; part < 2; ++part, ++c) {
-                if (!mbar_wait(&s_tcbar[slot], use & 1u, p.status)) {
-                  s_abort = 1;
-                  break;
-                }
-                CH_TCST(1, c, i);
-                tc_fence_after();
-                const uint64_t ad = ad0 + static_cast<uint64_t>(slot * (kTcChunk / 16));
-                tc_mma_bf16(d, ad, bd, idesc, (kk | part) != 0 ? 1u : 0u);
-                tc_mma_bf16(d, ad + 2, bd + 2, idesc, 1u);
-                tc_mma_bf16(d, ad + 4, bd + 4, idesc, 1u);
-                tc_mma_bf16(d, ad + 6, bd + 6, idesc, 1u);
-                tc_commit(&s_tcbar[4 + slot]);  // the slot is free once these MMAs are done
-                if (++slot == static_cast<uint32_t>(ns)) {
-                  slot = 0;
-                  ++use;
-                }
+            for (int kk = 0, kb = rot; kk < KB; ++kk, kb = (kb + 1 == KB ? 0 : kb + 1), ++c) {
+              if (!mbar_wait(&s_tcbar[slot], use & 1u, p.status)) {
+                s_abort = 1;
+                break;
               }
-              if (s_abort) break;
+              CH_TCST(1, c, i);
+              tc_fence_after();
+              const uint64_t bd = bd0 + static_cast<uint64_t>(kb * cpad * 8);
+              const uint64_t ad = ad0 + static_cast<uint64_t>(slot * (pair / 16));
+              tc_mma_bf16(d, ad, bd, idesc, kk != 0 ? 1u : 0u);
+              tc_mma_bf16(d, ad + 2, bd + 2, idesc, 1u);
+              tc_mma_bf16(d, ad + 4, bd + 4, idesc, 1u);
+              tc_mma_bf16(d, ad + 6, bd + 6, idesc, 1u);
+              tc_mma_bf16(d, ad + lo_off, bd, idesc, 1u);
+              tc_mma_bf16(d, ad + lo_off + 2, bd + 2, idesc, 1u);
+              tc_mma_bf16(d, ad + lo_off + 4, bd + 4, idesc, 1u);
+              tc_mma_bf16(d, ad + lo_off + 6, bd + 6, idesc, 1u);
+              tc_commit(&s_tcbar[4 + slot]);  // the slot is free once these MMAs are done
+              if (++slot == nsl) {
+                slot = 0;
+                ++use;
+              }
             }
           }
           tc_commit(&s_tcbar[8]);  // every product of the depth is done
@@ -845,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
         __syncwarp();
       }
-      tc_seq += static_cast<uint32_t>(nch);
+      tc_seq += static_cast<uint32_t>(tc_nmt * KB);
       if (!mbar_wait(&s_tcbar[8], tc_done_ph, p.status)) s_abort = 1;
       tc_done_ph ^= 1u;
       __syncwarp();
