@@ -38,12 +38,14 @@ bool make_tables(const dt_config& c, Tables& t) {
 
 dt_status check(const dt_config* c) {
   if (!c) return DT_ERR_INVALID_ARG;
-  if ((c->flags & ~(DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST | DT_FLAG_SEPARATE_TOPM)) != 0) return DT_ERR_INVALID_ARG;
+  if ((c->flags & ~(DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST | DT_FLAG_SEPARATE_TOPM | DT_FLAG_POSITIVE_BETA)) != 0)
+    return DT_ERR_INVALID_ARG;
   if ((c->flags & DT_FLAG_BEST_FIRST) && c->n_req != 1) return DT_ERR_SHAPE;
   if (c->d <= 0 || c->V <= 0 || c->g <= 0 || c->r <= 0 || c->M <= 0 || c->K <= 0 || c->W <= 0 ||
       c->B <= 0 || c->n_req <= 0 || c->block < 2)
     return DT_ERR_INVALID_ARG;
-  if (!(c->T > 0.0f) || !(c->beta <= 0.0f)) return DT_ERR_INVALID_ARG;
+  if (!(c->T > 0.0f) || !(c->beta <= 0.0f || ((c->flags & DT_FLAG_POSITIVE_BETA) && c->beta < INFINITY)))
+    return DT_ERR_INVALID_ARG;
   if (c->K > c->M || c->M > c->V) return DT_ERR_INVALID_ARG;
   if (c->block > kMaxDepth) return DT_ERR_SHAPE;  // depths 1..63: off[D+1] stays inside the tables
   if (c->M > 512 || c->K > 32 || c->W > 64) return DT_ERR_SHAPE;

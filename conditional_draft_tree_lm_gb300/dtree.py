@@ -40,6 +40,7 @@ WEIGHT_FIELDS = ("lm_head", "emb", "w_ih", "b_ih", "w_hh", "w1", "w2")
 FLAG_MARGINAL = 1  # DT_FLAG_MARGINAL: marginal scoring (no correction)
 FLAG_BEST_FIRST = 2  # DT_FLAG_BEST_FIRST: sequential conditional best-first builder
 FLAG_SEPARATE_TOPM = 4  # DT_FLAG_SEPARATE_TOPM: the Top-M as its own kernel in rounds
+FLAG_POSITIVE_BETA = 8  # DT_FLAG_POSITIVE_BETA: beta > 0 accepted (Lemma 1 not guaranteed)
 
 
 class DtWeights(ctypes.Structure):
@@ -96,12 +97,14 @@ def status_string(s: int) -> str:
 
 def make_config(cfg) -> DtConfig:
     """DtConfig from any object with the workload fields (d, V, block, g, r, M, K, W, B, n_req, beta, T,
-    and optionally marginal, builder and separate_topm)."""
+    and optionally marginal, builder, separate_topm and positive_beta)."""
     flags = FLAG_MARGINAL if getattr(cfg, "marginal", False) else 0
     if getattr(cfg, "builder", "dartree") == "best_first":
         flags |= FLAG_BEST_FIRST
     if getattr(cfg, "separate_topm", False):
         flags |= FLAG_SEPARATE_TOPM
+    if getattr(cfg, "positive_beta", False):
+        flags |= FLAG_POSITIVE_BETA
     return DtConfig(cfg.d, cfg.V, cfg.block, cfg.g, cfg.r, cfg.M, cfg.K, cfg.W, cfg.B,
                     getattr(cfg, "n_req", 1), float(cfg.beta), float(cfg.T), flags)
 

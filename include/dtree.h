@@ -75,7 +75,7 @@ typedef struct dt_config {
   int n_req;  /* independent requests per round; n_req * block <= 512 */
   float beta; /* depth bonus of the Top-B key (score + beta * depth); <= 0 */
   float T;    /* temperature dividing the corrected logits; > 0 */
-  unsigned flags; /* DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST | DT_FLAG_SEPARATE_TOPM, or 0 */
+  unsigned flags; /* DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST | DT_FLAG_SEPARATE_TOPM | DT_FLAG_POSITIVE_BETA, or 0 */
 } dt_config;
 
 /* Marginal scoring over the same super-tree: the correction Delta L is left
@@ -112,6 +112,17 @@ typedef struct dt_config {
  * stand-alone dt_base_logits and dt_topm calls are not affected. */
 #define DT_FLAG_SEPARATE_TOPM 4u
 
+/* Accept beta > 0 (a bonus for depth instead of a penalty).  The pages state
+ * the equivalence of the global Top-B with sequential best-first (DARTree,
+ * Metodología, 2. Poda Diferida, Equivalencia Teórica, Lemma 1) for
+ * beta <= 0 only; with beta > 0 it does not hold: the global Top-B of the
+ * depth-batched builder may select a node without its parent (the tree/mask
+ * step then reports DT_DEV_TREE and the selection, dt_prune_topB's output,
+ * is still the B largest keys), while the best-first builder
+ * (DT_FLAG_BEST_FIRST), whose heap only reaches a node through its parent,
+ * always emits a tree.  Without the flag, beta > 0 is DT_ERR_INVALID_ARG. */
+#define DT_FLAG_POSITIVE_BETA 8u
+
 /* Frozen weights (device pointers, borrowed: they must outlive the context).
  * All bf16, row-major, torch.nn.Linear out-by-in layout.  GRU gate blocks are
  * ordered (r, z, n); the GRU has one input-side bias and no hidden bias. */
@@ -133,9 +144,10 @@ typedef struct dt_ctx dt_ctx;
 
 /* Validate a configuration: K <= M <= V, M <= 512, 1 <= K <= 32,
  * 1 <= W <= 64, 2 <= block <= 64, d % 8 == 0, g % 8 == 0, r % 8 == 0,
- * r <= 1024, g <= 4096, n_req * block <= 512, 1 <= B <= N, T > 0, beta <= 0,
- * flags within DT_FLAG_MARGINAL | DT_FLAG_BEST_FIRST.  Returns DT_OK,
- * DT_ERR_INVALID_ARG or DT_ERR_SHAPE. */
+ * r <= 1024, g <= 4096, n_req * block <= 512, 1 <= B <= N, T > 0, beta <= 0
+ * (or finite with DT_FLAG_POSITIVE_BETA), flags within DT_FLAG_MARGINAL |
+ * DT_FLAG_BEST_FIRST | DT_FLAG_SEPARATE_TOPM | DT_FLAG_POSITIVE_BETA.
+ * Returns DT_OK, DT_ERR_INVALID_ARG or DT_ERR_SHAPE. */
 dt_status dt_check_config(const dt_config* cfg);
 
 /* N: super-tree nodes of one request without the root (n_1 = K,

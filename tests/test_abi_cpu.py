@@ -53,7 +53,8 @@ def test_check_config_accepts_named_workloads(lib):
 
 @pytest.mark.parametrize("bad,code", [
     (dict(K=20, M=16), 1),          # K > M
-    (dict(beta=0.5), 1),            # positive depth bonus
+    (dict(beta=0.5), 1),            # positive depth bonus without DT_FLAG_POSITIVE_BETA
+    (dict(beta=float("inf"), positive_beta=True), 1),  # with the flag, still finite
     (dict(T=0.0), 1),               # temperature must be positive
     (dict(B=10 ** 6), 1),           # budget above the super-tree size
     (dict(M=2000), 1),              # M > V
@@ -87,13 +88,17 @@ def test_workspace_bytes(lib):
 
 
 def test_check_config_flags(lib):
-    """Unknown flag bits are rejected; the three defined flags combine."""
+    """Unknown flag bits are rejected; the four defined flags combine; beta > 0
+    passes only with DT_FLAG_POSITIVE_BETA."""
     import ctypes
     from conditional_draft_tree_lm_gb300.dtree import load_library, make_config
-    cfg = make_config(get_config("tiny_bf16", builder="best_first", marginal=True, separate_topm=True))
-    assert cfg.flags == 7
+    cfg = make_config(get_config("tiny_bf16", builder="best_first", marginal=True, separate_topm=True,
+                                 positive_beta=True, beta=5.0))
+    assert cfg.flags == 15
     L = load_library()
     assert L.dt_check_config(ctypes.byref(cfg)) == 0
-    for bad in (8, 15, 1 << 31):
+    cfg.flags = 7  # the same beta = 5 without the flag
+    assert L.dt_check_config(ctypes.byref(cfg)) == 1
+    for bad in (16, 31, 1 << 31):
         cfg.flags = bad
         assert L.dt_check_config(ctypes.byref(cfg)) == 1

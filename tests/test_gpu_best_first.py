@@ -56,6 +56,16 @@ def test_tiny_best_first(beta):
     assert status == 0
 
 
+def test_tiny_best_first_positive_beta():
+    """beta = +5 behind DT_FLAG_POSITIVE_BETA: the heap still emits a tree (a
+    node is only reached through its parent), the same as the oracle's."""
+    cfg = get_config("tiny_bf16", builder="best_first", beta=5.0, positive_beta=True)
+    counts, details, status = _rounds(cfg, range(6))
+    assert counts["MISMATCH"] == 0, details
+    assert counts["match"] >= 5, (counts, details)
+    assert status == 0
+
+
 def test_tiny_best_first_marginal():
     cfg = get_config("tiny_bf16", builder="best_first", marginal=True)
     counts, details, status = _rounds(cfg, range(6))

@@ -27,7 +27,7 @@ class WorkloadConfig:
     W: int          # live branches kept per depth
     B: int          # node budget of the emitted tree (root excluded)
     n_req: int = 1  # independent requests per round
-    beta: float = 0.0   # depth bonus, <= 0
+    beta: float = 0.0   # depth bonus, <= 0 (> 0 only with positive_beta)
     T: float = 1.0      # temperature dividing the corrected logits
     root: str = "uniform"   # "zero": root token id 0; "uniform": uniform over V
     h_scale: str = "unit"   # "unit": H ~ N(0,1); "heavy": per-position scale ~ U[0.5, 4]
@@ -35,6 +35,7 @@ class WorkloadConfig:
     marginal: bool = False      # marginal scoring: Delta L = 0 (path-independent children)
     builder: str = "dartree"    # "dartree" (depth-batched) or "best_first" (sequential heap)
     separate_topm: bool = False  # run the Top-M as its own kernel, not in the LM-head GEMM
+    positive_beta: bool = False  # accept beta > 0 (DT_FLAG_POSITIVE_BETA; Lemma 1 not guaranteed)
 
     @property
     def D(self) -> int:
