@@ -15,13 +15,15 @@
 //  * the GRU input table (create time): A = E [V, d], B = W_ih [3g, d],
 //    D + b_ih -> X [V, 3g] fp32.
 //
-// Structure: one persistent CTA per SM, 6 warps.  Warp 0 issues TMA loads of
+// Structure: one persistent CTA per SM, 10 warps.  Warp 0 issues TMA loads of
 // A/B k-blocks (64 bf16 = one 128-byte swizzle row) into a ring of shared-memory
 // stages; warp 1 owns the tensor memory and issues tcgen05.mma (M=128, N<=256,
 // K=16) from one thread, committing each stage back to the producer and each
 // finished tile to the epilogue; warps 2..5 drain the accumulator with
 // tcgen05.ld (one TMEM lane quarter each) while the next tile accumulates into
-// the other half of tensor memory.
+// the other half of tensor memory.  With the fused Top-M, warps 6..9 join
+// them (the same lane quarters, the other half of the 16 columns), halving
+// each warp's share of the Top-M work; otherwise they have nothing to do.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -59,7 +61,7 @@ namespace dt {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kABytes = 128 * 128;  // 128 rows x 64 bf16
 
 
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], p.ft ? 8 : 4);  // one arrival per epilogue warp
     }
     fence_mbar_init();
   }
@@ -170,17 +172,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         GEMM_STAMP(local, 1);
       }
     }
-  } else {
-    // epilogue: warps 2..5; TMEM lanes [32*(warp%4), +32)
+  } else if (warp < 6 || p.ft) {
+    // epilogue: warps 2..5 (and 6..9 with the fused Top-M); TMEM lanes
+    // [32*(warp%4), +32)
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // fused Top-M: columns 8 half .. 8 half + 7
     const int row_in_tile = quarter * 32 + lane;
+    const int et = (warp - 2) * 32 + lane;
     const bool ft = p.ft != 0;
     FtState fs;
     FtSums fsum;
     int ft_tiles = 0;
     if (ft) {
       fs = ft_state(smem + gemm_ft_offset(p), p.ft_P);
-      ft_init(fs, fsum, p.ft_P, row_in_tile);
+      ft_init(fs, fsum, p.ft_P, et);
     }
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
@@ -194,10 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * p.BN);
       if (ft && mt < p.m_tiles_a) {
-        // one 16-column tile: read it, give the accumulator back at once, then
-        // the logits (if wanted) and the running Top-M
-        uint32_t v[16];
-        tmem_ld16(tbase, v);
+        // one 16-column tile, half of it per warp: read it, give the
+        // accumulator back at once, then the logits (if wanted) and the
+        // running Top-M
+        uint32_t v[kFtCols];
+        tmem_ld8(tbase + static_cast<uint32_t>(kFtCols * half), v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -205,10 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = row < p.rows_a;
         if (p.logits && valid) {
 #pragma unroll
-          for (int j = 1; j < 16; ++j)
-            if (j < p.n_valid) p.logits[static_cast<size_t>(j - 1) * p.rows_a + row] = __uint_as_float(v[j]);
+          for (int j = 0; j < kFtCols; ++j) {
+            const int c = kFtCols * half + j;  // column c: logit row c - 1
+            if (c >= 1 && c < p.n_valid) p.logits[static_cast<size_t>(c - 1) * p.rows_a + row] = __uint_as_float(v[j]);
+          }
         }
-        ft_tile(fs, fsum, v, p.ft_P, p.ft_M, p.ft_invT, row, valid, row_in_tile, ft_tiles);
+        ft_tile(fs, fsum, v, p.ft_P, p.ft_M, p.ft_invT, row, valid, quarter, half, warp - 2, ft_tiles);
         ++ft_tiles;
         if (warp == 2 && lane == 0) GEMM_STAMP(local, 3);
         continue;
@@ -263,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
     if (ft) {
-      ft_finish(fs, fsum, p.ft_P, p.ft_M, p.ft_invT, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
-                row_in_tile, p.part_id, p.part_val, p.part_max, p.part_sum, p.part_cnt, p.part_kth, p.part_tail);
+      ft_finish(fs, fsum, p.ft_P, p.ft_M, p.ft_invT, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), et,
+                quarter, half, p.part_id, p.part_val, p.part_max, p.part_sum, p.part_cnt, p.part_kth, p.part_tail);
     }
     if (warp == 2 && lane == 0) GEMM_STAMP(16, 0);
   }

@@ -7,12 +7,15 @@
 // logit/T, the sum of exp(logit/T - max) over the rest), which a small merge
 // kernel then reduces over the CTAs.
 //
-// Per tile (128 vocabulary rows, one per epilogue thread), with the four
-// epilogue warps only (named barrier 1, 128 threads):
-//   1. each thread's logit of every row becomes a key; the keys above the
-//      row's held M-th key are appended to the row's new-key list, warp by
-//      warp in lane order (no atomics: the order is the same every run);
-//   2. warp w updates rows w, w + 4, ...: while nothing is held, a bitonic
+// Per tile (128 vocabulary rows), with the eight epilogue warps only (named
+// barrier 1, 256 threads): warp e (0..7) reads TMEM lane quarter e % 4 (its
+// vocabulary rows) and columns 8 h .. 8 h + 7, h = e / 4 (half of the logit
+// rows: column c holds row c - 1):
+//   1. each thread's logit of each of its rows becomes a key; the keys above
+//      the row's held M-th key are appended to the row's new-key list, warp
+//      by warp (lane quarter order) in lane order (no atomics: the order is
+//      the same every run);
+//   2. warp e updates rows e, e + 8: while nothing is held, a bitonic
 //      sort of the (at most 128) new keys; otherwise the held list (sorted)
 //      and the new keys are ranked against each other (a held key moves down
 //      by the new keys above it, a new key counts the held keys above it by
@@ -39,6 +42,8 @@ namespace dt {
 
 constexpr int kFtMaxRows = 16;   // logit rows P (one request, block <= 17)
 constexpr int kFtMaxM = 64;
+constexpr int kFtWarps = 8;      // epilogue warps: two per TMEM lane quarter
+constexpr int kFtCols = 8;       // accumulator columns (block positions) per epilogue thread
 
 // Shared-memory area of the fused Top-M (byte offsets from a 16-byte aligned base).
 struct FtLayout {
@@ -52,7 +57,7 @@ DT_HOST_DEVICE_INLINE FtLayout ft_layout(int P) {
   L.ent = o;
   o += static_cast<size_t>(P) * 128 * 8;          // [row][128] new keys of a tile
   L.misc = o;
-  // thr (u64); hn, par, wcnt[4] (ints); ev_sum, ev_ref, red[4] (floats)
+  // thr (u64); hn, par, wcnt[4 quarters] (ints); ev_sum, ev_ref, red[4 quarters] (floats)
   o += 8 * kFtMaxRows + 4 * 6 * kFtMaxRows + 4 * 6 * kFtMaxRows;
   L.total = (o + 15) & ~static_cast<size_t>(15);
   return L;
@@ -64,7 +69,7 @@ struct FtState {
   uint64_t* thr;    // [P] the held list's M-th key (0 while it holds fewer)
   int* hn;          // [P] keys held
   int* par;         // [P] which copy of the held list is current
-  int* wcnt;        // [4][16] new keys of the tile per warp and row
+  int* wcnt;        // [4][16] new keys of the tile per lane quarter and row
   float* ev_sum;    // [P] sum of exp(logit/T - ev_ref) over the evicted keys
   float* ev_ref;    // [P] the row's max of logit/T
   float* red;       // [4][16]
@@ -85,7 +90,7 @@ DT_DEVINL FtState ft_state(uint8_t* base, int P) {
   return s;
 }
 
-DT_DEVINL void ft_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+DT_DEVINL void ft_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The epilogue warps' common verdict (all true), so that they leave the tile
 // loop together and no named barrier waits for a warp that has left.
 DT_DEVINL bool ft_all(bool v) {
@@ -93,7 +98,7 @@ DT_DEVINL bool ft_all(bool v) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(static_cast<uint32_t>(v))
@@ -101,14 +106,14 @@ DT_DEVINL bool ft_all(bool v) {
   return r != 0;
 }
 
-// The running sums of one epilogue thread (registers): per row, the sum of
-// exp(logit/T - ref) over its logits that never entered, and ref.
+// The running sums of one epilogue thread (registers): per row of its half,
+// the sum of exp(logit/T - ref) over its logits that never entered, and ref.
 struct FtSums {
-  float rest[kFtMaxRows];
-  float ref[kFtMaxRows];
+  float rest[kFtCols];
+  float ref[kFtCols];
 };
 
-// et: epilogue thread 0..127 (its vocabulary row in a tile).
+// et: epilogue thread 0..255.
 DT_DEVINL void ft_init(FtState& s, FtSums& u, int P, int et) {
   if (et < P) {
     s.thr[et] = 0ull;
@@ -118,9 +123,9 @@ DT_DEVINL void ft_init(FtState& s, FtSums& u, int P, int et) {
     s.ev_ref[et] = -INFINITY;
   }
 #pragma unroll
-  for (int p = 0; p < kFtMaxRows; ++p) {
-    u.rest[p] = 0.0f;
-    u.ref[p] = -INFINITY;
+  for (int j = 0; j < kFtCols; ++j) {
+    u.rest[j] = 0.0f;
+    u.ref[j] = -INFINITY;
   }
   ft_bar();
 }
@@ -151,33 +156,38 @@ DT_DEVINL void ft_sort128(uint64_t (&a)[4], int lane) {
   }
 }
 
-// One logits tile: v[1 + p] is the logit of row p at vocabulary id `id`
-// (valid: id < V).
-DT_DEVINL void ft_tile(FtState& s, FtSums& u, const uint32_t (&v)[16], int P, int M, float invT, int id, bool valid,
-                       int et, int lt) {
-  const int lane = et & 31, w = et >> 5;
+// One logits tile: v[j] is the logit of row 8 h + j - 1 (column 8 h + j;
+// rows 0 .. P-1) at vocabulary id `id` (valid: id < V); q: the thread's lane
+// quarter, e: its epilogue warp 0..7.
+DT_DEVINL void ft_tile(FtState& s, FtSums& u, const uint32_t (&v)[kFtCols], int P, int M, float invT, int id,
+                       bool valid, int q, int h, int e, int lt) {
+  const int lane = threadIdx.x & 31;
   const unsigned below = (1u << lane) - 1u;
-  uint64_t key[kFtMaxRows];
-  unsigned bal[kFtMaxRows];
+  uint64_t key[kFtCols];
+  unsigned bal[kFtCols];
 #pragma unroll
-  for (int p = 0; p < kFtMaxRows; ++p) {
-    key[p] = valid ? rank_key(__uint_as_float(v[1 + p]), static_cast<uint32_t>(id)) : 0ull;
-    bal[p] = __ballot_sync(0xFFFFFFFFu, p < P && key[p] > s.thr[min(p, P - 1)]);
-    if (lane == 0) s.wcnt[w * kFtMaxRows + p] = __popc(bal[p]);
+  for (int j = 0; j < kFtCols; ++j) {
+    const int p = kFtCols * h + j - 1;
+    const bool row = p >= 0 && p < P;
+    key[j] = valid && row ? rank_key(__uint_as_float(v[j]), static_cast<uint32_t>(id)) : 0ull;
+    bal[j] = __ballot_sync(0xFFFFFFFFu, row && key[j] > s.thr[row ? p : 0]);
+    if (lane == 0 && row) s.wcnt[q * kFtMaxRows + p] = __popc(bal[j]);
   }
   ft_bar();
 #pragma unroll
-  for (int p = 0; p < kFtMaxRows; ++p) {
-    if ((bal[p] >> lane) & 1u) {
+  for (int j = 0; j < kFtCols; ++j) {
+    if ((bal[j] >> lane) & 1u) {
+      const int p = kFtCols * h + j - 1;
       int base = 0;
-      for (int w2 = 0; w2 < w; ++w2) base += s.wcnt[w2 * kFtMaxRows + p];
-      s.ent[p * 128 + base + __popc(bal[p] & below)] = key[p];
+      for (int q2 = 0; q2 < q; ++q2) base += s.wcnt[q2 * kFtMaxRows + p];
+      s.ent[p * 128 + base + __popc(bal[j] & below)] = key[j];
     }
   }
   ft_bar();
   FT_STAMP(lt, 4);
-  // the rows' updates, warp w taking rows w, w + 4, ...
-  for (int p = w; p < P; p += 4) {
+  const int w = e;
+  // the rows' updates, warp e taking rows e, e + 8
+  for (int p = w; p < P; p += kFtWarps) {
     const int en = s.wcnt[p] + s.wcnt[kFtMaxRows + p] + s.wcnt[2 * kFtMaxRows + p] + s.wcnt[3 * kFtMaxRows + p];
     if (en == 0) continue;
     const int hn = s.hn[p];
@@ -262,35 +272,38 @@ DT_DEVINL void ft_tile(FtState& s, FtSums& u, const uint32_t (&v)[16], int P, in
   FT_STAMP(lt, 5);
   // this thread's logits that did not enter, against the rows' new max
 #pragma unroll
-  for (int p = 0; p < kFtMaxRows; ++p) {
-    if (p < P) {
+  for (int j = 0; j < kFtCols; ++j) {
+    const int p = kFtCols * h + j - 1;
+    if (p >= 0 && p < P) {
       const float mx = s.ev_ref[p];
-      u.rest[p] = ft_rescale(u.rest[p], u.ref[p], mx);
-      u.ref[p] = fmaxf(u.ref[p], mx);
-      const bool skip = valid && !((bal[p] >> lane) & 1u);
-      u.rest[p] += skip ? __expf(__uint_as_float(v[1 + p]) * invT - u.ref[p]) : 0.0f;
+      u.rest[j] = ft_rescale(u.rest[j], u.ref[j], mx);
+      u.ref[j] = fmaxf(u.ref[j], mx);
+      const bool skip = valid && !((bal[j] >> lane) & 1u);
+      u.rest[j] += skip ? __expf(__uint_as_float(v[j]) * invT - u.ref[j]) : 0.0f;
     }
   }
 }
 
-// After the CTA's last tile: the partial lists of CTA `cta` (of S) for the P rows.
-DT_DEVINL void ft_finish(FtState& s, FtSums& u, int P, int M, float invT, int cta, int S, int et, int* part_id,
-                         float* part_val, float* part_max, float* part_sum, int* part_cnt, float* part_kth,
-                         float* part_tail) {
+// After the CTA's last tile: the partial lists of CTA `cta` (of S) for the P
+// rows.  et: epilogue thread 0..255 (warp e = et / 32); q, h as in ft_tile.
+DT_DEVINL void ft_finish(FtState& s, FtSums& u, int P, int M, float invT, int cta, int S, int et, int q, int h,
+                         int* part_id, float* part_val, float* part_max, float* part_sum, int* part_cnt,
+                         float* part_kth, float* part_tail) {
   const int lane = et & 31, w = et >> 5;
 #pragma unroll
-  for (int p = 0; p < kFtMaxRows; ++p) {
-    if (p < P) {
-      const float r = warp_sum(u.rest[p]);
-      if (lane == 0) s.red[w * kFtMaxRows + p] = r;
+  for (int j = 0; j < kFtCols; ++j) {
+    const int p = kFtCols * h + j - 1;
+    if (p >= 0 && p < P) {
+      const float r = warp_sum(u.rest[j]);
+      if (lane == 0) s.red[q * kFtMaxRows + p] = r;
     }
   }
   ft_bar();
   FT_STAMP(16, 3);
-  // the lists' suffix sums of exp(logit/T - max), warp w taking rows w, w + 4,
-  // ...: lane l sums entries 2l, 2l+1, then a suffix scan over the lanes
+  // the lists' suffix sums of exp(logit/T - max), warp e taking rows e, e + 8:
+  // lane l sums entries 2l, 2l+1, then a suffix scan over the lanes
   if (part_tail) {
-    for (int p = w; p < P; p += 4) {
+    for (int p = w; p < P; p += kFtWarps) {
       const int hn = s.hn[p];
       const uint64_t* h = s.held + (s.par[p] * P + p) * kFtMaxM;
       const float mx = s.ev_ref[p];
@@ -309,7 +322,7 @@ DT_DEVINL void ft_finish(FtState& s, FtSums& u, int P, int M, float invT, int ct
       if (2 * lane + 1 < hn) part_tail[q * M + 2 * lane + 1] = t1 + next;
     }
   }
-  for (int idx = et; idx < P * M; idx += 128) {
+  for (int idx = et; idx < P * M; idx += 32 * kFtWarps) {
     const int p = idx / M, j = idx - p * M;
     const int hn = s.hn[p];
     const size_t q = static_cast<size_t>(p) * S + cta;
