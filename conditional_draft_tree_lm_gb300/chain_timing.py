@@ -80,7 +80,10 @@ def main():
     xbuf = np.zeros(2 * SLOTS * XCTAS, dtype=np.uint64)
     tbuf = np.zeros(2 * 64 * 16, dtype=np.uint64)
     gbuf = np.zeros(17 * 8, dtype=np.uint64)
-    acc, xacc, tacc, gacc = [], [], [], []
+    acc, xacc, tacc, gacc, tbacc = [], [], [], [], []
+    lib.dt_dchain_topb_stamps.restype = ctypes.c_int
+    lib.dt_dchain_topb_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    tbb = np.zeros(8, dtype=np.uint64)
     for s in range(args.rounds + 3):
         H, r = make_round_inputs(cfg, s)
         Hd = dtree.bf16_tensor(H)
@@ -101,6 +104,8 @@ def main():
             xacc.append(xbuf.reshape(2, SLOTS, XCTAS).astype(np.int64).copy())
             tacc.append(tbuf.reshape(2, 64, 16).astype(np.int64).copy())
             gacc.append(gbuf.reshape(17, 8).astype(np.int64).copy())
+            lib.dt_dchain_topb_stamps(tbb.ctypes.data, tbb.size)
+            tbacc.append(tbb.astype(np.int64).copy())
     st = np.stack(acc)  # [rounds, cta, slot, phase]
     if args.save:
         np.save(args.save, st)
@@ -147,6 +152,12 @@ def main():
               f"z {sub(13, 2):.0f};  B.sel: operands {sub(5, 15):.0f}, top-K rounds + log-partition {sub(15, 6):.0f};  "
               f"topW: rounds {sub(8, 14):.0f}, survivor order {sub(14, 9):.0f};  "
               f"X: loads issued {sub(0, 16):.0f}, poll {sub(16, 17):.0f}, barrier + copies {sub(17, 1):.0f}")
+    tb = np.stack(tbacc).mean(axis=0)
+    t6 = st[:, 0, 0, 6].mean()  # before Top-B
+    print("  tail (cycles from the Top-B's start): keys %.0f, histogram %.0f, bound %.0f, candidates %.0f, ranks + "
+          "order %.0f | tree slots %.0f, parents %.0f, ancestors %.0f, mask to the end %.0f" % (
+              tb[0] - t6, tb[1] - tb[0], tb[2] - tb[1], tb[3] - tb[2], tb[4] - tb[3], tb[5] - tb[4], tb[6] - tb[5],
+              tb[7] - tb[6], st[:, 0, 0, 2].mean() - tb[7]))
     exchange_report(np.stack(xacc), D, b.plan())
     topm_report(np.stack(tacc))
     gemm_report(np.stack(gacc), 1.0 / mhz)

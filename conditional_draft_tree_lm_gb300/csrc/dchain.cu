@@ -66,6 +66,16 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "chainlib.cuh"
+#ifdef DT_DCHAIN_TIMING
+// the Top-B / tree tail's inner phases: slot 0, phases 8.. of CTA 0's stamps
+namespace dt {
+__device__ unsigned long long g_topb_stamps[8];
+}
+#define TOPB_STAMP(k)                                                                          \
+  do {                                                                                         \
+    if (threadIdx.x == 0 && blockIdx.x == 0) dt::g_topb_stamps[k] = static_cast<unsigned long long>(clock64()); \
+  } while (0)
+#endif
 #include "prune.cuh"
 
 namespace dt {
@@ -271,8 +281,12 @@ DT_HOST_DEVICE_INLINE Lay make_lay(int jc, int g, int r, int K, int D, int cs) {
 DT_HOST_DEVICE_INLINE size_t tail_bytes(int N1, int B) {
   const size_t S = static_cast<size_t>(B) + 1;
   return a16((static_cast<size_t>(kMaxDepth) + 2 + 3 * S + S * anc_words(static_cast<int>(S))) * 4) +
-         a16(static_cast<size_t>(N1 - 1) * 8) + a16(static_cast<size_t>(N1 - 1) * 4) + kNW * 256 * 4;
+         a16(static_cast<size_t>(N1 - 1) * 8) + a16(static_cast<size_t>(N1 - 1) * 4) + kNW * 256 * 4 +
+         3 * a16(static_cast<size_t>(N1) * 4) + a16(static_cast<size_t>(B) * 4);  // node scores, parents and
+                                                                                   // tokens; the selection
 }
+// Node scores a tail thread loads into registers before the cluster barrier.
+constexpr int kTailScores = 8;
 
 struct Stage {
   uint16_t* w2;  // [kMP][RQP]
@@ -1031,6 +1045,22 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
   DCH_STAMP(0, 1);
   // the node arrays of depth D (which ends after its selections)
   if (cta == 0 && !aborted && p.depth_last == D) write_nodes(D);
+  // the tail's node scores: loads issued now, their latency hidden by the
+  // cluster barrier (the block barrier makes depth D's writes visible)
+  const bool tail = p.fuse_tree && cta == 0 && !aborted;
+  const bool tail_pre = tail && p.N1 <= kTailScores * kT;
+  float scv[kTailScores];
+  int pav[kTailScores], tov[kTailScores];
+  if (tail_pre) {
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kTailScores; ++k) {
+      const int v = tid + k * kT;
+      scv[k] = v < p.N1 ? __ldcg(p.node_score + v) : 0.0f;
+      pav[k] = v < p.N1 ? __ldcg(p.node_parent + v) : 0;
+      tov[k] = v < p.N1 ? __ldcg(p.node_tok + v) : 0;
+    }
+  }
   cp_async_wait_all();
   cluster_sync();  // no CTA leaves while a peer may read its shared memory
   // the next launch tags its words with a new epoch (also after an abort, so
@@ -1038,7 +1068,7 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
   if (cta == 0 && tid == 0) st_relaxed_u32(p.epoch, E);
 
   // ---- tail: global Top-B and tree/mask (CTA 0, which wrote every node array) ----
-  if (p.fuse_tree && cta == 0 && !aborted) {
+  if (tail) {
     __syncthreads();
     const int S = p.B + 1;
     int* offs = reinterpret_cast<int*>(sm);
@@ -1050,14 +1080,29 @@ __global__ void __launch_bounds__(kT, 1) k_dchain(const DchainParams p) {
     uint64_t* tb_cands = reinterpret_cast<uint64_t*>(t);
     uint32_t* tb_keys = reinterpret_cast<uint32_t*>(t + a16(static_cast<size_t>(p.N1 - 1) * 8));
     uint32_t* hist = tb_keys + a16(static_cast<size_t>(p.N1 - 1) * 4) / 4;
+    const size_t n1b = a16(static_cast<size_t>(p.N1) * 4);
+    float* sc_s = reinterpret_cast<float*>(hist + kNW * 256);                             // [N1]
+    int* pa_s = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(sc_s) + n1b);           // [N1]
+    int* to_s = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(pa_s) + n1b);           // [N1]
+    int* sel_s = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(to_s) + n1b);          // [B]
     for (int k = tid; k <= D + 1; k += kT) offs[k] = p.off[k];
+    if (tail_pre) {
+#pragma unroll
+      for (int k = 0; k < kTailScores; ++k)
+        if (tid + k * kT < p.N1) {
+          sc_s[tid + k * kT] = scv[k];
+          pa_s[tid + k * kT] = pav[k];
+          to_s[tid + k * kT] = tov[k];
+        }
+    }
     __syncthreads();
     DCH_STAMP(0, 6);
-    topb_select(p.node_score, p.N1, p.B, p.beta, D, offs, tb_keys, tb_cands, p.N1 - 1, hist, kNW * 256, s_state,
-                s_tred, s_tscan, p.sel);
+    topb_select(tail_pre ? sc_s : p.node_score, p.N1, p.B, p.beta, D, offs, tb_keys, tb_cands, p.N1 - 1, hist,
+                kNW * 256, s_state, s_tred, s_tscan, p.sel, sel_s);
     DCH_STAMP(0, 7);
-    tree_and_mask(p.sel, p.N1, p.B, D, offs, p.node_tok, p.node_parent, p.node_score, nullptr, nodes, par, dep, anc,
-                  p.tok, p.parent, p.depth, p.logp_cum, p.mask, p.status);
+    tree_and_mask(sel_s, p.N1, p.B, D, offs, tail_pre ? to_s : p.node_tok, tail_pre ? pa_s : p.node_parent,
+                  tail_pre ? sc_s : p.node_score, nullptr, nodes, par, dep, anc, p.tok, p.parent, p.depth, p.logp_cum,
+                  p.mask, p.status);
   }
   DCH_STAMP(0, 2);
 }
@@ -1177,6 +1222,12 @@ extern "C" int dt_dchain_stamps(unsigned long long* out, int n) {
 // The exchange stamps of the last launch, [published / received][depth][CTA]
 // (%globaltimer, ns; CTAs beyond 128 are not recorded).  Returns the number of
 // values copied, or -1.
+// The tail's inner stamps of the last launch (CTA 0, clock64()): Top-B keys,
+// histogram, bound bin, candidates, ranks; tree slots, parents, ancestors.
+extern "C" int dt_dchain_topb_stamps(unsigned long long* out, int n) {
+  if (!out || n < 8) return -1;
+  return cudaMemcpyFromSymbol(out, dt::g_topb_stamps, sizeof(dt::g_topb_stamps)) == cudaSuccess ? 8 : -1;
+}
 extern "C" int dt_dchain_xstamps(unsigned long long* out, int n) {
   const int total = 2 * (dt::kMaxDepth + 2) * dt::kXStampCtas;
   if (!out || n < total) return -1;

@@ -15,6 +15,14 @@
 #include "common.cuh"
 #include "select.cuh"
 
+// Phase stamps of topb_select / tree_and_mask (a timing build of the file that
+// includes this one may define it first).
+#ifndef TOPB_STAMP
+#define TOPB_STAMP(k) \
+  do {                \
+  } while (0)
+#endif
+
 namespace dt {
 
 DT_DEVINL int depth_of(const int* off, int D, int v) {
@@ -33,7 +41,8 @@ constexpr int kTopBCandCap = 8192;
 // score: [N1] node scores of one request (global).  keys: N1-1 uint32 of
 // shared memory; cands: cap uint64 of shared memory; hist: hist_words uint32
 // of shared memory (a multiple of 256); state: 4 uint32; red: 64 floats;
-// scan: 40 ints.  sel: [B] output, ascending node indices.
+// scan: 40 ints.  sel: [B] output, ascending node indices (also written to
+// sel_s, shared memory, when it is not null).
 //   1. key_v = score_v + beta * depth_v for every non-root node; min and max;
 //   2. a 256-bin histogram of the keys between max and min; the bin holding
 //      the B-th largest key bounds the candidates (bins at or above it);
@@ -43,7 +52,7 @@ constexpr int kTopBCandCap = 8192;
 // select of the B-th key with index-ordered compaction runs instead.
 DT_DEVINL void topb_select(const float* score, int N1, int B, float beta, int D, const int* off, uint32_t* keys,
                            uint64_t* cands, int cap, uint32_t* hist, int hist_words, uint32_t* state, float* red,
-                           int* scan, int* sel) {
+                           int* scan, int* sel, int* sel_s = nullptr) {
   const int n = N1 - 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   float* kf = reinterpret_cast<float*>(keys);
@@ -65,8 +74,12 @@ DT_DEVINL void topb_select(const float* score, int N1, int B, float beta, int D,
   for (int b = tid; b < ncopy * 256; b += blockDim.x) hist[b] = 0u;
   if (tid == 0) state[0] = 0u;
   __syncthreads();
+  TOPB_STAMP(0);
   if (B >= n) {
-    for (int e = tid; e < n; e += blockDim.x) sel[e] = e + 1;
+    for (int e = tid; e < n; e += blockDim.x) {
+      sel[e] = e + 1;
+      if (sel_s) sel_s[e] = e + 1;
+    }
     __syncthreads();
     return;
   }
@@ -80,6 +93,7 @@ DT_DEVINL void topb_select(const float* score, int N1, int B, float beta, int D,
   uint32_t* my = hist + (warp % ncopy) * 256;
   for (int e = tid; e < n; e += blockDim.x) atomicAdd(&my[bin_of(kf[e])], 1u);
   __syncthreads();
+  TOPB_STAMP(1);
   for (int b = tid; b < 256; b += blockDim.x) {
     uint32_t c = 0;
     for (int w = 0; w < ncopy; ++w) c += hist[w * 256 + b];
@@ -117,6 +131,7 @@ DT_DEVINL void topb_select(const float* score, int N1, int B, float beta, int D,
     }
   }
   __syncthreads();
+  TOPB_STAMP(2);
   const int bt = static_cast<int>(state[1]);
   for (int e = tid; e < n; e += blockDim.x) {
     const float k = kf[e];
@@ -126,6 +141,7 @@ DT_DEVINL void topb_select(const float* score, int N1, int B, float beta, int D,
     }
   }
   __syncthreads();
+  TOPB_STAMP(3);
   const int c = static_cast<int>(state[0]);
   if (c > cap) {
     // fallback: radix select of the B-th key over all keys, then the winners
@@ -154,7 +170,10 @@ DT_DEVINL void topb_select(const float* score, int N1, int B, float beta, int D,
     for (int e = s0; e < s1; ++e) {
       const uint32_t k = keys[e];
       if (k > t || (k == t && tb++ < need)) {
-        if (o < B) sel[o] = e + 1;
+        if (o < B) {
+          sel[o] = e + 1;
+          if (sel_s) sel_s[o] = e + 1;
+        }
         ++o;
       }
     }
@@ -167,12 +186,14 @@ DT_DEVINL void topb_select(const float* score, int N1, int B, float beta, int D,
     if (rk < B) win[rk] = static_cast<int>(rank_key_id(ke));
   });
   __syncthreads();
+  TOPB_STAMP(4);
   // ascending node order
   for (int a = tid; a < B; a += blockDim.x) {
     const int va = win[a];
     int pos = 0;
     for (int b2 = 0; b2 < B; ++b2) pos += win[b2] < va ? 1 : 0;
     sel[pos] = va;
+    if (sel_s) sel_s[pos] = va;
   }
   __syncthreads();
 }
@@ -203,6 +224,7 @@ DT_DEVINL void tree_and_mask(const int* sel, int N1, int B, int D, const int* of
     nodes[k] = v;
   }
   __syncthreads();
+  TOPB_STAMP(5);
   for (int k = threadIdx.x; k < S; k += blockDim.x) {
     const int v = nodes[k];
     int ps = -1, d = 0;
@@ -234,6 +256,7 @@ DT_DEVINL void tree_and_mask(const int* sel, int N1, int B, int D, const int* of
     logp_cum[k] = node_score[v];
   }
   __syncthreads();
+  TOPB_STAMP(6);
   // each slot walks up to the root once and marks itself and its ancestors
   // in its own bitmask row; the mask bytes are then read off the rows
   const int nw = anc_words(S);
@@ -243,10 +266,28 @@ DT_DEVINL void tree_and_mask(const int* sel, int N1, int B, int D, const int* of
     for (int cur = a, st = 0; cur >= 0 && st <= D; cur = par[cur], ++st) row[cur >> 5] |= 1u << (cur & 31);
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < S * S; idx += blockDim.x) {
+  TOPB_STAMP(7);
+  auto bit = [&](int idx) {
     const int a = idx / S, b = idx - a * S;
-    mask[idx] = static_cast<uint8_t>((anc[static_cast<size_t>(a) * nw + (b >> 5)] >> (b & 31)) & 1u);
+    return (anc[static_cast<size_t>(a) * nw + (b >> 5)] >> (b & 31)) & 1u;
+  };
+  // four mask bytes per 32-bit store where the mask is 4-byte aligned (one
+  // division per word: the next three bytes step along the row)
+  const int n4 = (reinterpret_cast<uintptr_t>(mask) & 3u) == 0 ? S * S / 4 : 0;
+  for (int w = threadIdx.x; w < n4; w += blockDim.x) {
+    int a = (4 * w) / S, b = 4 * w - a * S;
+    uint32_t word = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      word |= ((anc[static_cast<size_t>(a) * nw + (b >> 5)] >> (b & 31)) & 1u) << (8 * k);
+      if (++b == S) {
+        b = 0;
+        ++a;
+      }
+    }
+    reinterpret_cast<uint32_t*>(mask)[w] = word;
   }
+  for (int idx = 4 * n4 + threadIdx.x; idx < S * S; idx += blockDim.x) mask[idx] = static_cast<uint8_t>(bit(idx));
 }
 
 }  // namespace dt
