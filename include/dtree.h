@@ -204,7 +204,10 @@ dt_status dt_base_logits(dt_ctx* ctx, const void* H, float* logits, void* stream
  *              logit descending, token id ascending.
  *   cand_base: [n_req, D, M] fp32 out: base logits of those tokens (not / T).
  *   rest_lse:  [n_req, D] fp32 out: log sum_{v not in C} exp(logit_v / T),
- *              -inf when M == V. */
+ *              -inf when M == V.
+ * Up to one row per SM, each row is split into chunks whose sorted lists are
+ * merged; with more rows (e.g. 32 requests), two CTAs per SM stream whole rows
+ * behind a rising bound (dt_plan_string says which). */
 dt_status dt_topm(dt_ctx* ctx, const float* logits, int32_t* cand_tok, float* cand_base,
                   float* rest_lse, void* stream);
 
@@ -339,7 +342,10 @@ dt_status dt_build_round_host(dt_ctx* ctx, const void* H_host, const int32_t* ro
  * it, where S, the chunks each row is split into, is
  *   S = min(max(SMs / rows, ceil(V / 16384), 1), max(V / (2 M), 1),
  *           max(8192 / M, 1))          (integer divisions, SMs = the device's)
- * and each chunk must hold at most 16384 logits.  Calls beyond the array, with
+ * and each chunk must hold at most 16384 logits.  (With at least one row per
+ * SM, V a multiple of 4 and 16-byte aligned logits, each row is streamed whole
+ * by one CTA instead and the array is not used; the bound above still
+ * applies.)  Calls beyond the array, with
  * rows > 65535, M > 512, or a chunk above 16384 logits (V > 8192 * 16384 / M)
  * are rejected with DT_ERR_SHAPE and a message in dt_last_error(), before any
  * work is queued.
