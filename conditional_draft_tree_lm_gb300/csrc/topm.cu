@@ -45,6 +45,7 @@ constexpr int kSample = 4;            // values per thread in the sample
 constexpr int kRungs = 8;             // threshold ladder
 constexpr int kCandCap = kThreads;    // candidates ranked in the partial phase
 constexpr int kMergeCap = 2048;       // merge candidates ranked among themselves
+constexpr int kPre = 4;               // entries of each list a merge thread loads up front
 
 // Phase stamps (built with -DDT_TOPM_TIMING only): %globaltimer at the phase
 // boundaries of row 0: [0][split][k] for the chunk CTAs, [1][0][k] for the CTA
@@ -283,45 +284,74 @@ DT_DEVINL bool merge_row_tails(const TopmParams& p, int row, const MergeSmem& m,
     const size_t e = (rb + s2) * M + j;
     return rank_key(p.part_val[e], static_cast<uint32_t>(p.part_id[e]));
   };
-  float gmax = -INFINITY;
-  for (int s2 = tid; s2 < S; s2 += kThreads) gmax = fmaxf(gmax, p.part_max[rb + s2]);
-  gmax = block_max(gmax, m.red);
   const int t = min(M, max(1, (M + S - 1) / S));
+  if (t > kPre) return false;
+  // thread s: everything of list s the merge usually needs, loaded at once
+  // (its length, max and rest sum, its first kPre keys and suffix sums)
+  int cnt = 0;
+  float pm = -INFINITY, ps = 0.0f;
+  uint64_t k4[kPre];
+  float t4[kPre + 1];
+  if (tid < S) {
+    cnt = p.part_cnt[rb + tid];
+    pm = p.part_max[rb + tid];
+    ps = p.part_sum[rb + tid];
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      k4[j] = j < cnt ? key_at(tid, j) : 0ull;
+      t4[j] = j < cnt ? p.part_tail[(rb + tid) * M + j] : 0.0f;
+    }
+    t4[kPre] = kPre < cnt ? p.part_tail[(rb + tid) * M + kPre] : 0.0f;
+  }
+  const float gmax = block_max(tid < S ? pm : -INFINITY, m.red);
   const int n1 = S * t;
-  for (int u = tid; u < n1; u += kThreads) {
-    const int s2 = u / t, j = u - s2 * t;
-    m.big[u] = j < p.part_cnt[rb + s2] ? key_at(s2, j) : 0ull;
+  // the lists' first t entries (t <= kPre: from the registers)
+  if (tid < S) {
+#pragma unroll
+    for (int j = 0; j < kPre; ++j)
+      if (j < t) m.big[tid * t + j] = k4[j];
   }
   __syncthreads();
   const uint64_t lb = block_kth_key<1>(m.big, n1, M, m.hist, m.scan, m.cand, m.red4, m.s_lb);
   TOPM_STAMP(1, 1);
-  // thread s: list s's entries at or above the bound (a prefix), read four at
-  // a time; their count, then their place in the candidate list (lists in
-  // order, so the list is the same every run)
+  // thread s: list s's entries at or above the bound (a prefix): the first
+  // kPre from the registers, any further ones four at a time from memory;
+  // their count, then their place in the candidate list (lists in order, so
+  // the list is the same every run)
   int* ncs = reinterpret_cast<int*>(m.hist);  // [S] (the histogram is free again)
-  int cnt = 0, nmine = 0;
+  int nmine = 0;
   if (tid < S) {
-    cnt = p.part_cnt[rb + tid];
-    for (int j0 = 0; j0 < cnt; j0 += 4) {
-      uint64_t k4[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) k4[i] = j0 + i < cnt ? key_at(tid, j0 + i) : 0ull;
-      int more = 0;
+    for (int j = 0; j < kPre; ++j) nmine += (j < cnt && k4[j] >= lb) ? 1 : 0;
+    if (nmine == kPre) {
+      for (int j0 = kPre; j0 < cnt; j0 += 4) {
+        uint64_t q4[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) more += (j0 + i < cnt && k4[i] >= lb) ? 1 : 0;
-      nmine += more;
-      if (more < 4) break;
+        for (int i = 0; i < 4; ++i) q4[i] = j0 + i < cnt ? key_at(tid, j0 + i) : 0ull;
+        int more = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) more += (j0 + i < cnt && q4[i] >= lb) ? 1 : 0;
+        nmine += more;
+        if (more < 4) break;
+      }
     }
   }
   int total;
   const int base = block_exclusive_scan(nmine, m.scan, &total);
   if (total > kMergeCap || total < M) return false;  // (uniform: every thread has the total)
   int* list_of = reinterpret_cast<int*>(m.big);  // [kMergeCap] list of candidate e (big is free again)
-  if (tid < S)
-    for (int j = 0; j < nmine; ++j) {
+  if (tid < S) {
+#pragma unroll
+    for (int j = 0; j < kPre; ++j)
+      if (j < nmine) {
+        m.cand[base + j] = k4[j];
+        list_of[base + j] = tid;
+      }
+    for (int j = kPre; j < nmine; ++j) {
       m.cand[base + j] = key_at(tid, j);
       list_of[base + j] = tid;
     }
+  }
   if (tid < S) ncs[tid] = 0;
   __syncthreads();
   TOPM_STAMP(1, 2);
@@ -340,9 +370,14 @@ DT_DEVINL bool merge_row_tails(const TopmParams& p, int row, const MergeSmem& m,
   float rest = 0.0f;
   if (tid < S) {
     const int c = ncs[tid];
-    const float tail = c < cnt ? p.part_tail[(rb + tid) * M + c] : 0.0f;
-    const float pm = p.part_max[rb + tid];
-    if (pm > -INFINITY) rest = (p.part_sum[rb + tid] + tail) * expf(pm - gmax);
+    float tail = 0.0f;
+    if (c < cnt) {
+      tail = t4[kPre];
+#pragma unroll
+      for (int j = kPre - 1; j >= 0; --j) tail = c == j ? t4[j] : tail;
+      if (c > kPre) tail = p.part_tail[(rb + tid) * M + c];
+    }
+    if (pm > -INFINITY) rest = (ps + tail) * expf(pm - gmax);
   }
   rest = block_sum(rest, m.red);
   if (tid == 0) {
