@@ -311,8 +311,21 @@ DT_DEVINL bool merge_row_tails(const TopmParams& p, int row, const MergeSmem& m,
     for (int j = 0; j < kPre; ++j)
       if (j < t) m.big[tid * t + j] = k4[j];
   }
+  if (tid == 0) *m.s_lb = 0ull;
   __syncthreads();
-  const uint64_t lb = block_kth_key<1>(m.big, n1, M, m.hist, m.scan, m.cand, m.red4, m.s_lb);
+  // the M-th largest head: few heads are ranked directly (the key of rank
+  // M - 1; zero, i.e. every entry, when fewer than M lists hold any), many
+  // through the histogram
+  uint64_t lb;
+  if (n1 <= kThreads) {
+    rank_all(m.big, n1, [&](int, uint64_t ke, int rk) {
+      if (rk == M - 1) *m.s_lb = ke;
+    });
+    __syncthreads();
+    lb = *m.s_lb;
+  } else {
+    lb = block_kth_key<1>(m.big, n1, M, m.hist, m.scan, m.cand, m.red4, m.s_lb);
+  }
   TOPM_STAMP(1, 1);
   // thread s: list s's entries at or above the bound (a prefix): the first
   // kPre from the registers, any further ones four at a time from memory;
