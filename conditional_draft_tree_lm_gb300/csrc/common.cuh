@@ -203,6 +203,13 @@ DT_DEVINL void tc_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+// 32 lanes x 4 consecutive 32-bit columns (as tmem_ld16, a quarter of the columns).
+DT_DEVINL void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 // 32 lanes x 8 consecutive 32-bit columns (as tmem_ld16, half the columns).
 DT_DEVINL void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"

@@ -15,15 +15,16 @@
 //  * the GRU input table (create time): A = E [V, d], B = W_ih [3g, d],
 //    D + b_ih -> X [V, 3g] fp32.
 //
-// Structure: one persistent CTA per SM, 10 warps.  Warp 0 issues TMA loads of
+// Structure: one persistent CTA per SM, 18 warps.  Warp 0 issues TMA loads of
 // A/B k-blocks (64 bf16 = one 128-byte swizzle row) into a ring of shared-memory
 // stages; warp 1 owns the tensor memory and issues tcgen05.mma (M=128, N<=256,
 // K=16) from one thread, committing each stage back to the producer and each
 // finished tile to the epilogue; warps 2..5 drain the accumulator with
 // tcgen05.ld (one TMEM lane quarter each) while the next tile accumulates into
-// the other half of tensor memory.  With the fused Top-M, warps 6..9 join
-// them (the same lane quarters, the other half of the 16 columns), halving
-// each warp's share of the Top-M work; otherwise they have nothing to do.
+// the other half of tensor memory.  With the fused Top-M, warps 6..17 join
+// them (the same lane quarters; each warp takes 4 of the 16 columns), so
+// that each warp's share of the Top-M work is a quarter; otherwise they have
+// nothing to do.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -61,7 +62,7 @@ namespace dt {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 576;
 constexpr uint32_t kABytes = 128 * 128;  // 128 rows x 64 bf16
 
 
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], p.ft ? 8 : 4);  // one arrival per epilogue warp
+      mbar_init(&tempty[a], p.ft ? kFtWarps : 4);  // one arrival per epilogue warp
     }
     fence_mbar_init();
   }
@@ -173,10 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 6 || p.ft) {
-    // epilogue: warps 2..5 (and 6..9 with the fused Top-M); TMEM lanes
+    // epilogue: warps 2..5 (and 6..17 with the fused Top-M); TMEM lanes
     // [32*(warp%4), +32)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;  // fused Top-M: columns 8 half .. 8 half + 7
+    const int grp = (warp - 2) >> 2;  // fused Top-M: columns 4 grp .. 4 grp + 3
     const int row_in_tile = quarter * 32 + lane;
     const int et = (warp - 2) * 32 + lane;
     const bool ft = p.ft != 0;
@@ -199,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * p.BN);
       if (ft && mt < p.m_tiles_a) {
-        // one 16-column tile, half of it per warp: read it, give the
+        // one 16-column tile, a quarter of it per warp: read it, give the
         // accumulator back at once, then the logits (if wanted) and the
         // running Top-M
         uint32_t v[kFtCols];
-        tmem_ld8(tbase + static_cast<uint32_t>(kFtCols * half), v);
+        tmem_ld4(tbase + static_cast<uint32_t>(kFtCols * grp), v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -212,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.logits && valid) {
 #pragma unroll
           for (int j = 0; j < kFtCols; ++j) {
-            const int c = kFtCols * half + j;  // column c: logit row c - 1
+            const int c = kFtCols * grp + j;  // column c: logit row c - 1
             if (c >= 1 && c < p.n_valid) p.logits[static_cast<size_t>(c - 1) * p.rows_a + row] = __uint_as_float(v[j]);
           }
         }
-        ft_tile(fs, fsum, v, p.ft_P, p.ft_M, p.ft_invT, row, valid, quarter, half, warp - 2, ft_tiles);
+        ft_tile(fs, fsum, v, p.ft_P, p.ft_M, p.ft_invT, row, valid, quarter, grp, warp - 2, ft_tiles);
         ++ft_tiles;
         if (warp == 2 && lane == 0) GEMM_STAMP(local, 3);
         continue;
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ft) {
       ft_finish(fs, fsum, p.ft_P, p.ft_M, p.ft_invT, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), et,
-                quarter, half, p.part_id, p.part_val, p.part_max, p.part_sum, p.part_cnt, p.part_kth, p.part_tail);
+                quarter, grp, p.part_id, p.part_val, p.part_max, p.part_sum, p.part_cnt, p.part_kth, p.part_tail);
     }
     if (warp == 2 && lane == 0) GEMM_STAMP(16, 0);
   }

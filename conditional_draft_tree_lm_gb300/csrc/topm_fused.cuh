@@ -7,15 +7,15 @@
 // logit/T, the sum of exp(logit/T - max) over the rest), which a small merge
 // kernel then reduces over the CTAs.
 //
-// Per tile (128 vocabulary rows), with the eight epilogue warps only (named
-// barrier 1, 256 threads): warp e (0..7) reads TMEM lane quarter e % 4 (its
-// vocabulary rows) and columns 8 h .. 8 h + 7, h = e / 4 (half of the logit
-// rows: column c holds row c - 1):
+// Per tile (128 vocabulary rows), with the sixteen epilogue warps only (named
+// barrier 1, 512 threads): warp e (0..15) reads TMEM lane quarter e % 4 (its
+// vocabulary rows) and columns 4 h .. 4 h + 3, h = e / 4 (a quarter of the
+// logit rows: column c holds row c - 1):
 //   1. each thread's logit of each of its rows becomes a key; the keys above
 //      the row's held M-th key are appended to the row's new-key list, warp
 //      by warp (lane quarter order) in lane order (no atomics: the order is
 //      the same every run);
-//   2. warp e updates rows e, e + 8: while nothing is held, a bitonic
+//   2. warp e updates row e: while nothing is held, a bitonic
 //      sort of the (at most 128) new keys; otherwise the held list (sorted)
 //      and the new keys are ranked against each other (a held key moves down
 //      by the new keys above it, a new key counts the held keys above it by
@@ -42,8 +42,8 @@ namespace dt {
 
 constexpr int kFtMaxRows = 16;   // logit rows P (one request, block <= 17)
 constexpr int kFtMaxM = 64;
-constexpr int kFtWarps = 8;      // epilogue warps: two per TMEM lane quarter
-constexpr int kFtCols = 8;       // accumulator columns (block positions) per epilogue thread
+constexpr int kFtWarps = 16;     // epilogue warps: four per TMEM lane quarter
+constexpr int kFtCols = 4;       // accumulator columns (block positions) per epilogue thread
 
 // Shared-memory area of the fused Top-M (byte offsets from a 16-byte aligned base).
 struct FtLayout {
@@ -90,7 +90,7 @@ DT_DEVINL FtState ft_state(uint8_t* base, int P) {
   return s;
 }
 
-DT_DEVINL void ft_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+DT_DEVINL void ft_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 // The epilogue warps' common verdict (all true), so that they leave the tile
 // loop together and no named barrier waits for a warp that has left.
 DT_DEVINL bool ft_all(bool v) {
@@ -98,7 +98,7 @@ DT_DEVINL bool ft_all(bool v) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "bar.red.and.pred q, 1, 512, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(static_cast<uint32_t>(v))
@@ -106,14 +106,14 @@ DT_DEVINL bool ft_all(bool v) {
   return r != 0;
 }
 
-// The running sums of one epilogue thread (registers): per row of its half,
+// The running sums of one epilogue thread (registers): per row of its columns,
 // the sum of exp(logit/T - ref) over its logits that never entered, and ref.
 struct FtSums {
   float rest[kFtCols];
   float ref[kFtCols];
 };
 
-// et: epilogue thread 0..255.
+// et: epilogue thread 0..511.
 DT_DEVINL void ft_init(FtState& s, FtSums& u, int P, int et) {
   if (et < P) {
     s.thr[et] = 0ull;
@@ -156,9 +156,9 @@ DT_DEVINL void ft_sort128(uint64_t (&a)[4], int lane) {
   }
 }
 
-// One logits tile: v[j] is the logit of row 8 h + j - 1 (column 8 h + j;
+// One logits tile: v[j] is the logit of row 4 h + j - 1 (column 4 h + j;
 // rows 0 .. P-1) at vocabulary id `id` (valid: id < V); q: the thread's lane
-// quarter, e: its epilogue warp 0..7.
+// quarter, e: its epilogue warp 0..15.
 DT_DEVINL void ft_tile(FtState& s, FtSums& u, const uint32_t (&v)[kFtCols], int P, int M, float invT, int id,
                        bool valid, int q, int h, int e, int lt) {
   const int lane = threadIdx.x & 31;
@@ -186,7 +186,7 @@ DT_DEVINL void ft_tile(FtState& s, FtSums& u, const uint32_t (&v)[kFtCols], int 
   ft_bar();
   FT_STAMP(lt, 4);
   const int w = e;
-  // the rows' updates, warp e taking rows e, e + 8
+  // the rows' updates, warp e taking row e
   for (int p = w; p < P; p += kFtWarps) {
     const int en = s.wcnt[p] + s.wcnt[kFtMaxRows + p] + s.wcnt[2 * kFtMaxRows + p] + s.wcnt[3 * kFtMaxRows + p];
     if (en == 0) continue;
@@ -285,7 +285,7 @@ DT_DEVINL void ft_tile(FtState& s, FtSums& u, const uint32_t (&v)[kFtCols], int 
 }
 
 // After the CTA's last tile: the partial lists of CTA `cta` (of S) for the P
-// rows.  et: epilogue thread 0..255 (warp e = et / 32); q, h as in ft_tile.
+// rows.  et: epilogue thread 0..511 (warp e = et / 32); q, h as in ft_tile.
 DT_DEVINL void ft_finish(FtState& s, FtSums& u, int P, int M, float invT, int cta, int S, int et, int q, int h,
                          int* part_id, float* part_val, float* part_max, float* part_sum, int* part_cnt,
                          float* part_kth, float* part_tail) {
@@ -300,7 +300,7 @@ DT_DEVINL void ft_finish(FtState& s, FtSums& u, int P, int M, float invT, int ct
   }
   ft_bar();
   FT_STAMP(16, 3);
-  // the lists' suffix sums of exp(logit/T - max), warp e taking rows e, e + 8:
+  // the lists' suffix sums of exp(logit/T - max), warp e taking row e:
   // lane l sums entries 2l, 2l+1, then a suffix scan over the lanes
   if (part_tail) {
     for (int p = w; p < P; p += kFtWarps) {
