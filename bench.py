@@ -548,8 +548,8 @@ def bench_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": "builds/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "us_per_round": us_round,
-        "us_per_round_note": "mean of back-to-back graph replays (pipelined rounds); the 60 % HBM "
-                             "target is judged on it; isolated_round_us_* are single synchronised rounds",
+        "us_per_round_note": "mean of back-to-back graph replays (pipelined rounds), the figure the "
+                             "60 % HBM target is stated for; isolated_round_us_* are single synchronised rounds",
         "isolated_round_us_p10_p50_p90": [float(np.percentile(lat, q)) for q in (10, 50, 90)],
         "isolated_round_hbm_frac_p50": rbytes / (float(np.percentile(lat, 50)) * 1e-6) / 1e9 / peak,
         "round_hbm_gbs": rbytes / (us_round * 1e-6) / 1e9,
