@@ -211,7 +211,7 @@ struct Smem {
   int* surv;        // [n_req][W] survivor child slot
   float* pscore;    // [W] parent scores of the current request
   int* pnode;       // [W] parent node indices of the current request
-  int* tok_all;     // [D][M] candidate tokens of request 0 (when prefetched)
+  int* tok_all;     // [D][M] candidate tokens of the CTA's tok_all request (when prefetched)
   int* ctk_buf;     // the [M] scratch behind ctk when tokens are read per row
   uint16_t* zh;     // [16*ceil(W/16)][r+8] bf16 high part of z (tensor-core phase B)
   uint16_t* zl;     // same, low part
@@ -365,11 +365,15 @@ DT_DEVINL void load_cand_tokens(const ChainParams& p, const Shape& sh, const Sme
   }
 }
 
+// The request whose candidate tokens of every depth a CTA reads once at launch
+// (tok_all): request 0, or with several requests the CTA's own first one.
+DT_DEVINL int tok_all_request(const Shape& sh) { return sh.n_req > 1 ? static_cast<int>(blockIdx.x) : 0; }
+
 // Point s.ctk at the candidate tokens of (request q, depth i): the launch-time
-// prefetch for request 0, else read into the scratch row.  Whole CTA; the
-// caller synchronises before the tokens are used.
+// prefetch for the CTA's tok_all request, else read into the scratch row.
+// Whole CTA; the caller synchronises before the tokens are used.
 DT_DEVINL void select_row_tokens(const ChainParams& p, const Shape& sh, Smem& s, int q, int i) {
-  if (q == 0 && sh.prefetch) {
+  if (q == tok_all_request(sh) && sh.prefetch) {
     s.ctk = s.tok_all + static_cast<size_t>(i - 1) * sh.M;
   } else {
     s.ctk = s.ctk_buf;
@@ -577,10 +581,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     tmem_base = s_tmem;
   }
 
-  // ---- candidate tokens of every depth of request 0, read once ----
-  if (sh.prefetch) {
+  // ---- candidate tokens of every depth of the CTA's tok_all request, read once ----
+  const int tokq = tok_all_request(sh);
+  if (sh.prefetch && tokq < n_req) {
     for (int idx = tid; idx < D * M; idx += kThreads) {
-      int t = p.cand_tok[idx];  // request 0 owns rows 0..D-1
+      int t = p.cand_tok[static_cast<size_t>(tokq) * D * M + idx];  // request q owns rows qD .. qD+D-1
       if (t < 0 || t >= p.V) {
         dt_report(p.status, DT_DEV_BOUNDS);
         t = 0;
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   __syncthreads();
   // W2 rows read from L2 by the scoring (not staged): the first depth's now,
   // every later depth's one depth ahead
-  const bool w2_ahead = !p.marginal && !sh.stage_w2 && sh.prefetch && (sh.r * 2) % 16 == 0;
+  const bool w2_ahead = !p.marginal && n_req == 1 && !sh.stage_w2 && sh.prefetch && (sh.r * 2) % 16 == 0;
   if (w2_ahead) prefetch_w2_rows(p, sh, s.tok_all + static_cast<size_t>(p.depth_first - 1) * M);
   // Several requests: CTA c selects for requests c, c + G, ... (G CTAs) and
   // every CTA then updates its state columns of all requests after one more
@@ -1768,7 +1773,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         // overlap the barrier
         __syncthreads();
         select_row_tokens(p, sh, s, qfirst, i + 1);
-        if (!(qfirst == 0 && sh.prefetch)) __syncthreads();
+        if (!(qfirst == tokq && sh.prefetch)) __syncthreads();
         stage_row(p, sh, buf(i + 1), s.ctk, static_cast<size_t>(qfirst) * D + i, j0, nj,
                   !dist && !bdist && i + 1 != D);
       }
