@@ -236,12 +236,17 @@ DT_HOST_DEVICE_INLINE int pow2_at_least(int n) {
 }
 
 
+// The candidates' GRU-input slices are staged in shared memory only for one
+// request whose branches are not spread and whose phase A is not on tcgen05;
+// otherwise phase C reads them from the table.
+DT_HOST_DEVICE_INLINE bool xs_staged(const Shape& sh) { return !sh.bdist && !sh.tc && sh.n_req == 1; }
+
 // One stage buffer's bytes of each staged array (0 w2s, 1 xs, 2 cbs, 3 h1s,
 // 4 rest), and the region that holds both buffers when double-buffered.
 DT_HOST_DEVICE_INLINE size_t stage_one(const Shape& sh, int which) {
   switch (which) {
     case 0: return sh.stage_w2 ? static_cast<size_t>(sh.M) * (sh.r + 8) * 2 : 0;
-    case 1: return sh.bdist ? 0 : static_cast<size_t>(sh.M) * 3 * sh.jper * 4;
+    case 1: return xs_staged(sh) ? static_cast<size_t>(sh.M) * 3 * sh.jper * 4 : 0;
     case 2: return static_cast<size_t>(sh.M) * 4;
     case 3: return static_cast<size_t>(sh.r) * 4;
     default: return 16;
@@ -626,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
     select_row_tokens(p, sh, s, qfirst, p.depth_first);
     __syncthreads();
     stage_row(p, sh, buf(p.depth_first), s.ctk,
-              static_cast<size_t>(qfirst) * D + (p.depth_first - 1), j0, nj, !dist && !bdist && p.depth_first != D);
+              static_cast<size_t>(qfirst) * D + (p.depth_first - 1), j0, nj, xs_staged(sh) && p.depth_first != D);
   }
 
   unsigned epoch = 0;
@@ -709,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       // depth
       if (sh.dbuf && i < p.depth_last)
         stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
-                  i + 1 != D);
+                  xs_staged(sh) && i + 1 != D);
       // rows 0..7 of the tile carry the high parts and rows 8..15 the low
       // parts of the same states: one MMA per k16 step gives both products
       float acc[kMaxNTiles][4];
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       // frees the slot through the MMAs' commit.
       if (sh.dbuf && i < p.depth_last)
         stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
-                  i + 1 != D);
+                  xs_staged(sh) && i + 1 != D);
       const int KB = g / 64;
       const int ns = sh.ns;
       const uint8_t* abase = reinterpret_cast<const uint8_t*>(p.sfrag) +
@@ -1012,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       // this depth
       if (sh.dbuf && p0 == 0 && i < p.depth_last)
         stage_row(p, sh, buf(i + 1), s.tok_all + static_cast<size_t>(i) * M, static_cast<size_t>(i), j0, nj,
-                  i + 1 != D);
+                  xs_staged(sh) && i + 1 != D);
 #pragma unroll
       for (int j = 0; j < kSLoads; ++j) {
         const int idx = tid + j * kThreads;
@@ -1101,7 +1106,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         __syncthreads();
         select_row_tokens(p, sh, s, q, i);
         __syncthreads();
-        stage_row(p, sh, buf(i), s.ctk, qrow, j0, nj, !dist && !bdist && !last);
+        stage_row(p, sh, buf(i), s.ctk, qrow, j0, nj, xs_staged(sh) && !last);
       }
       {
         const Stage cur = buf(i);
@@ -1668,11 +1673,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           const int jv = idx / nj, jj = idx - jv * nj;
           const int e = s.surv[q * W + jv];
           const int b = e / K;
-          // the GRU-input slice: staged per candidate, or (branches spread)
-          // read from the table by token
-          const int xst = bdist ? g : nj;
-          const float* x = bdist ? p.xtab + static_cast<size_t>(s.ctok[e]) * 3 * g + j0
-                                 : s.xs + static_cast<size_t>(s.cslot[e]) * 3 * sh.jper;
+          // the GRU-input slice: staged per candidate, or read from the
+          // table by token
+          const bool xt = !xs_staged(sh);
+          const int xst = xt ? g : nj;
+          const float* x = xt ? p.xtab + static_cast<size_t>(s.ctok[e]) * 3 * g + j0
+                              : s.xs + static_cast<size_t>(s.cslot[e]) * 3 * sh.jper;
           const float* uu = s.uu + static_cast<size_t>(q * Lp + b) * 3 * sh.jper;
           const float h = Sprev[static_cast<size_t>(q * W + b) * g + j0 + jj];
           const float rg = sigmoidf_(x[jj] + uu[jj]);
@@ -1775,7 +1781,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         select_row_tokens(p, sh, s, qfirst, i + 1);
         if (!(qfirst == tokq && sh.prefetch)) __syncthreads();
         stage_row(p, sh, buf(i + 1), s.ctk, static_cast<size_t>(qfirst) * D + i, j0, nj,
-                  !dist && !bdist && i + 1 != D);
+                  xs_staged(sh) && i + 1 != D);
       }
       if (!grid_barrier(p.bar, epoch, p.status, &s_abort)) {
         drain();
