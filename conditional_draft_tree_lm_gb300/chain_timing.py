@@ -231,7 +231,7 @@ def grid_chain_report(lib, b, cfg, args):
             sub = lambda a, b: (mid[:, :, b] - mid[:, :, a]).mean() * us
             print(f"  B (branches spread): scoring {sub(2, 8):.2f} [to the branch {sub(2, 12):.2f}, z {sub(12, 13):.2f}, "
                   f"logits {sub(13, 14):.2f}, log-partition + keys {sub(14, 15):.2f}, K best {sub(15, 16):.2f}, "
-                  f"children {sub(16, 18):.2f} + {sub(18, 8):.2f}], barrier {sub(8, 9):.2f}, children read back "
+                  f"children: token order {sub(16, 19):.2f}, writes {sub(19, 18):.2f}, + {sub(18, 8):.2f}], barrier {sub(8, 9):.2f}, children read back "
                   f"{sub(9, 10):.2f}, top-W {sub(10, 11):.2f} [threshold {sub(10, 17):.2f}], the rest {sub(11, 3):.2f} us")
         elif (mid[:, :, 10] > 0).all():
             sub = lambda a, b: (mid[:, :, b] - mid[:, :, a]).mean() * us

@@ -354,8 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_best(const BestParams p) {
       const uint64_t xb = __shfl_sync(0xFFFFFFFFu, kb, (lane >> 1) & 31);
       const uint64_t wk = (lane & 1) ? xb : xa;
       const int tok = lane < K ? cand_key_tok(wk) : 0x7FFFFFFF;
-      int trank = 0;
-      for (int m = 0; m < K; ++m) trank += __shfl_sync(0xFFFFFFFFu, tok, m) < tok ? 1 : 0;
+      const int trank = warp_rank_below(tok, K);
       if (lane < K) {
         const float lp = key_f32(static_cast<uint32_t>(wk >> 32)) - logZ;
         const int u = n_nodes + trank;

@@ -207,7 +207,7 @@ struct Smem {
   float* clogp;     // [W*K]
   float* cscore;    // [W*K]
   int* crank;       // [W*K] top-K winners / ranks
-  uint64_t* wkey;   // [max(64, pow2 >= W*K)] top-W keys
+  uint64_t* wkey;   // [wkey_words] top-W keys (and the spread branches' K-best selection)
   int* surv;        // [n_req][W] survivor child slot
   float* pscore;    // [W] parent scores of the current request
   int* pnode;       // [W] parent node indices of the current request
@@ -267,6 +267,14 @@ DT_HOST_DEVICE_INLINE size_t lamkey_bytes(const Shape& sh) {
   return sh.mma_b ? static_cast<size_t>(sh.W) * sh.M * 8 : 0;
 }
 
+// 64-bit words of the top-W keys' region: >= 64 (the one-warp top-W); with the
+// branches spread, also the K-best selection's histogram (128 words) and the
+// keys of its bin (up to M).
+DT_HOST_DEVICE_INLINE int wkey_words(const Shape& sh) {
+  const int a = pow2_at_least(sh.W * sh.K), b = sh.bdist ? 128 + pow2_at_least(sh.M) : 64;
+  return a > b ? a : b;
+}
+
 DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
   const size_t WK = static_cast<size_t>(sh.W) * sh.K;
   const size_t gp = static_cast<size_t>(kstride(sh.g));
@@ -294,7 +302,7 @@ DT_HOST_DEVICE_INLINE SmemSizes smem_sizes(const Shape& sh) {
       WK * 4,
       WK * 4,
       WK * 4,
-      static_cast<size_t>(max(64, pow2_at_least(static_cast<int>(WK)))) * 8,  // >= 64: one-warp top-W
+      static_cast<size_t>(wkey_words(sh)) * 8,
       static_cast<size_t>(sh.n_req) * sh.W * 4,
       static_cast<size_t>(sh.W) * 4,
       static_cast<size_t>(sh.W) * 4,
@@ -1281,8 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
             const uint64_t wk = (lane & 1) ? xb : xa;
             const int tok = cand_key_tok(wk);
             const int wc = cand_key_c(wk);
-            int trank = 0;
-            for (int m = 0; m < K; ++m) trank += __shfl_sync(0xFFFFFFFFu, tok, m) < tok ? 1 : 0;
+            const int trank = warp_rank_below(lane < K ? tok : 0x7FFFFFFF, K);
             if (lane < K) {
               const float lp = key_f32(static_cast<uint32_t>(wk >> 32)) - logZ;
               const int slot = b * K + trank;
@@ -1351,7 +1358,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
       } else if (bdist) {
         float* zv = s.z;           // [r] z of the branch
         float* lamv = s.clogp;     // [M] lambda, then logp
-        uint64_t* keys = s.wkey;   // [M]
+        uint64_t* keys = s.wkey;   // the K best's histogram and bin keys
         int* win = s.crank;        // [K]
         for (int b = blockIdx.x; b < Lp; b += gridDim.x) {
           const float* u = p.uW1 + static_cast<size_t>(b) * r;
@@ -1388,17 +1395,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           float se = expf(rest - lmax);
           for (int w8 = 0; w8 < kWarps; ++w8) se += s_tred[32 + w8];
           const float logZ = lmax + logf(se);
-          for (int c = tid; c < M; c += kThreads) {
-            const float lp = lamv[c] - logZ;
-            lamv[c] = lp;
-            keys[c] = rank_key(lp, static_cast<uint32_t>(s.ctk[c]));
-          }
+          for (int c = tid; c < M; c += kThreads) lamv[c] -= logZ;
           __syncthreads();
           CH_STAMP(i, 15);
-          // the K best (ties to the lower token id), then in token order
-          block_rank_all(keys, M, [&](int e, uint64_t, int rk) {
-            if (rk < K) win[rk] = e;
-          });
+          // the K best (ties to the lower token id) by a value histogram, in
+          // any order (the children are ordered by token below)
+          {
+            uint32_t* hist = reinterpret_cast<uint32_t*>(keys);  // 256 words, then the bin's keys
+            const uint64_t kth = block_kth_rank_key(lamv, M, K, hist, keys + 128, wkey_words(sh) - 128, s_tred,
+                                                    s_tscan, &s_kth, s.ctk);
+            if (tid == 0) s_tscan[0] = 0;
+            __syncthreads();
+            for (int c = tid; c < M; c += kThreads)
+              if (rank_key(lamv[c], static_cast<uint32_t>(s.ctk[c])) >= kth) win[atomicAdd(&s_tscan[0], 1)] = c;
+          }
           __syncthreads();
           CH_STAMP(i, 16);
           if (warp == 0) {
@@ -1408,8 +1418,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
               c = 0;
             }
             const int tok = lane < K ? s.ctk[c] : 0x7FFFFFFF;
+            // the children in token order: each counts the winners' smaller
+            // tokens (read back from shared memory)
+            s_tscan[lane] = tok;
+            __syncwarp();
             int trank = 0;
-            for (int m = 0; m < K; ++m) trank += __shfl_sync(0xFFFFFFFFu, tok, m) < tok ? 1 : 0;
+#pragma unroll 8
+            for (int m = 0; m < K; ++m) trank += s_tscan[m] < tok ? 1 : 0;
+            CH_STAMP(i, 19);
             if (lane < K) {
               const float lp = lamv[c];
               const size_t nidx = static_cast<size_t>(row_off) + b * K + trank;
@@ -1533,11 +1549,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
             }
           }
           // children of branch b, sorted by token id
-          int rank = 0;
-          for (int m = 0; m < K; ++m) {
-            const int t = __shfl_sync(0xFFFFFFFFu, my_tok, m);
-            rank += t < my_tok ? 1 : 0;
-          }
+          const int rank = warp_rank_below(my_tok, K);
           if (lane < K) {
             const int slot = b * K + rank;
             s.ctok[slot] = my_tok;

@@ -14,6 +14,23 @@ constexpr int kWarps = kThreads / 32;
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16
 // mantissa bits, so two bf16 MMAs reproduce an fp32 operand to ~2^-17.
+// For the lanes l < K holding a token each (the others any value): how many of
+// lanes 0 .. K-1 hold a smaller token (the rank that puts a branch's children
+// in token order).  Eight independent shuffles at a time, so that their
+// latencies overlap (a loop of one shuffle per step measured ~290 cycles a
+// step at K = 32).
+DT_DEVINL int warp_rank_below(int tok, int K) {
+  int r = 0;
+  for (int m0 = 0; m0 < K; m0 += 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t2 = __shfl_sync(0xFFFFFFFFu, tok, (m0 + j) & 31);
+      r += (m0 + j < K && t2 < tok) ? 1 : 0;
+    }
+  }
+  return r;
+}
+
 DT_DEVINL uint32_t split_hi_lo(float a, float b, uint32_t& lo) {
   const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
   const __nv_bfloat16 al = __float2bfloat16_rn(a - __bfloat162float(ah));

@@ -135,16 +135,17 @@ DT_DEVINL void block_rank_all(const uint64_t* keys, int c, Fn fn) {
   }
 }
 
-// The m-th largest of the n keys rank_key(v[e], e) (values v in shared
-// memory; 1 <= m <= n; the keys are distinct, a tie in value going to the
-// lower index).  A 256-bin histogram over the value range [lo, hi] (bin 0
+// The m-th largest of the n keys rank_key(v[e], id_e) with id_e = ids[e], or
+// e when ids is null (values and ids in shared memory; 1 <= m <= n; the keys
+// are distinct, a tie in value going to the lower id).  A 256-bin histogram over the value range [lo, hi] (bin 0
 // holds the largest values) locates the bin that holds it; that bin's keys
 // are gathered (at most bnd_cap; beyond that every key of the bin is ranked
 // against the whole bin instead) and ranked exactly.  `hist` holds 256
 // words, `red` 2 x (warps) floats, `sc` 3 ints, `s_key` one key.  Every thread
 // of the block calls it and receives the key.
 DT_DEVINL uint64_t block_kth_rank_key(const float* v, int n, int m, uint32_t* hist, uint64_t* bnd, int bnd_cap,
-                                      float* red, int* sc, uint64_t* s_key) {
+                                      float* red, int* sc, uint64_t* s_key, const int* ids = nullptr) {
+  auto key_of = [&](int e) { return rank_key(v[e], static_cast<uint32_t>(ids ? ids[e] : e)); };
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x, nw = nt >> 5;
   float lo = INFINITY, hi = -INFINITY;
   for (int e = tid; e < n; e += nt) {
@@ -208,7 +209,7 @@ DT_DEVINL uint64_t block_kth_rank_key(const float* v, int n, int m, uint32_t* hi
   for (int e = tid; e < n; e += nt) {
     if (bin_of(v[e]) == bt) {
       const int at = atomicAdd(&sc[2], 1);
-      if (at < bnd_cap) bnd[at] = rank_key(v[e], static_cast<uint32_t>(e));
+      if (at < bnd_cap) bnd[at] = key_of(e);
     }
   }
   __syncthreads();
@@ -220,9 +221,9 @@ DT_DEVINL uint64_t block_kth_rank_key(const float* v, int n, int m, uint32_t* hi
   } else {
     for (int e = tid; e < n; e += nt) {
       if (bin_of(v[e]) != bt) continue;
-      const uint64_t k = rank_key(v[e], static_cast<uint32_t>(e));
+      const uint64_t k = key_of(e);
       int rk = 0;
-      for (int f = 0; f < n; ++f) rk += (bin_of(v[f]) == bt && rank_key(v[f], static_cast<uint32_t>(f)) > k) ? 1 : 0;
+      for (int f = 0; f < n; ++f) rk += (bin_of(v[f]) == bt && key_of(f) > k) ? 1 : 0;
       if (rk == need - 1) *s_key = k;
     }
   }
