@@ -622,6 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
   const bool bdist = sh.bdist;
   const int qfirst = dist ? static_cast<int>(blockIdx.x) : 0;
   const int qstep = dist ? static_cast<int>(gridDim.x) : 1;
+  // a CTA that selects for exactly one request keeps that request's next
+  // parents in shared memory from one depth to the next
+  const bool keep_par = qfirst < n_req && qfirst + qstep >= n_req;
   // stage the first depth's first request of this CTA (overlaps the root
   // step and phase A)
   auto buf = [&](int depth) -> Stage { return (depth & 1) ? s.st1 : s.st0; };
@@ -1150,7 +1153,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
           uv[j] = idx < nz ? ub[idx] : 0.0f;
         }
       }
-      for (int b = tid; b < Lp; b += kThreads) {
+      // the parents (this depth's live branches) and their scores: kept from
+      // this CTA's own top-W of the previous depth, or read back
+      for (int b = tid; b < (keep_par && i > p.depth_first ? 0 : Lp); b += kThreads) {
         const int node = live_prev[static_cast<size_t>(q) * W + b];
         s.pnode[b] = node;
         s.pscore[b] = (node >= 0 && node < p.N1) ? p.node_score[static_cast<size_t>(q) * p.N1 + node] : 0.0f;
@@ -1673,6 +1678,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_chain(const ChainParams p) {
         }
         __syncthreads();
         CH_STAMP(i, 11);
+        if (keep_par) {
+          // the next depth's parents: the survivors, their node indices and
+          // scores (s.pnode / s.pscore are not read again in this depth)
+          for (int j = tid; j < Li; j += kThreads) {
+            const int e = s.surv[q * W + j];
+            s.pnode[j] = row_off + e;
+            s.pscore[j] = s.cscore[e];
+          }
+        }
         if (dist || blockIdx.x == 0) {
           for (int j = tid; j < W; j += kThreads) {
             const int node = j < Li ? row_off + s.surv[q * W + j] : -1;
