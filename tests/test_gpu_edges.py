@@ -13,9 +13,9 @@ scores within 2e-3; a mismatch only excused by an outcome-relevant near-tie):
 * W = 64, K = 32, M = 64, B = 512: wide depths (the sorting-network top-W and
   a large Top-B) at a small vocabulary;
 * d = 72: a hidden size that is not a multiple of the GEMM's 64-wide k-block;
-* g = 128 or 256 with many state rows (5 or 20 requests of 8 branches, or one
-  request of 64 branches): the chain's tcgen05 projection, one row tile or two
-  (the second one ragged);
+* g = 128, 256 or 1024 with many state rows (5 or 20 requests of 8 branches,
+  or one request of 64 branches): the chain's tcgen05 projection, one row tile
+  or two (the second one ragged), 2 to 16 K blocks;
 * the best-first builder with B equal to the whole K-restricted tree (the
   frontier empties exactly at the last pop).
 """
@@ -39,6 +39,7 @@ CASES = {
     "tc_requests": dict(g=256, n_req=5, W=8, K=4, B=32),
     "tc_two_tiles": dict(g=128, n_req=20, W=8, K=4, B=32),
     "tc_wide": dict(g=128, block=4, M=64, K=32, W=64, B=512),
+    "tc_full_width": dict(g=1024, r=256, n_req=20, W=8, K=4, B=32),
 }
 
 
