@@ -763,7 +763,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_topm_merge(const TopmParams p) 
 // running log-partition sum.  When the buffer could overflow with the next
 // tile (and after the row's last), it is cut to its M best (block_kth_key):
 // the cut entries feed a second running sum and tau becomes the M-th key, so
-// later logits enter only when they beat it.  The M kept are ranked among
+// later logits enter only when they beat it.  A row starts from a bound taken
+// from its first tile's lane maxima (for M up to kRowQuota per warp), so that
+// the first tile does not fill the buffer.  The M kept are ranked among
 // themselves; the two sums of every thread give rest_lse.  No partial lists
 // and no merge.
 constexpr int kRowVals = 8;                         // logits per thread and tile
@@ -771,6 +773,14 @@ constexpr int kRowTile = kThreads * kRowVals;       // 4096 logits, 16 KB
 constexpr int kRowSub = 1;                          // tiles per copy
 constexpr int kRowStages = 3;
 constexpr int kRowCap = kRowTile + 2 * kCandCap;    // candidate buffer (keys)
+constexpr int kRowQuota = 8;                        // first-tile bound: up to M = 8 per warp
+
+// 2^x by the SFU's approximation (flushes subnormal results to zero)
+DT_DEVINL float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 DT_DEVINL void row_bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
@@ -878,43 +888,88 @@ __global__ void __launch_bounds__(kThreads, 2) k_topm_rows(const TopmParams p) {
     __syncthreads();
     if (s_abort) return;  // a copy that never landed (reported): nothing more is issued or read
     // logits e = t kRowTile + 4 (h kThreads + tid) + {0..3}, h = 0, 1; -inf
-    // past the row's end (the slot's bytes there are stale)
+    // past the row's end (the slot's bytes there are stale; only the last
+    // tile has such places)
     float v[kRowVals];
+    const bool full = (t + 1) * kRowTile <= V;
 #pragma unroll
     for (int h = 0; h < kRowVals / 4; ++h) {
       const int j = 4 * (h * kThreads + tid);
       const float4 f = *reinterpret_cast<const float4*>(ring + (slot * kRowSub + sub) * kRowTile + j);
-      const int e = t * kRowTile + j;
-      v[4 * h] = e < V ? f.x : -INFINITY;
-      v[4 * h + 1] = e + 1 < V ? f.y : -INFINITY;
-      v[4 * h + 2] = e + 2 < V ? f.z : -INFINITY;
-      v[4 * h + 3] = e + 3 < V ? f.w : -INFINITY;
+      v[4 * h] = f.x;
+      v[4 * h + 1] = f.y;
+      v[4 * h + 2] = f.z;
+      v[4 * h + 3] = f.w;
+      if (!full) {
+        const int e = t * kRowTile + j;
+        if (e >= V) v[4 * h] = -INFINITY;
+        if (e + 1 >= V) v[4 * h + 1] = -INFINITY;
+        if (e + 2 >= V) v[4 * h + 2] = -INFINITY;
+        if (e + 3 >= V) v[4 * h + 3] = -INFINITY;
+      }
     }
     float tm = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kRowVals; ++u) tm = fmaxf(tm, v[u]);
+    if (t == 0 && M <= kWarps * kRowQuota) {
+      // a first bound from the row's first tile: in every warp the q-th
+      // largest lane maximum (q = ceil(M / warps), counted with repeats), and
+      // the smallest of those over the warps.  At least warps x q >= M of the
+      // tile's logits (one per lane taken) reach it, so the row's M-th key
+      // lies above every key of that value's lowest priority: keys at or
+      // below the bound are losers from the start
+      const int qw = (M + kWarps - 1) / kWarps;
+      uint32_t mk = f32_key(tm), kq = 0u;
+      for (int rr = 0; rr < qw; ++rr) {
+        kq = __reduce_max_sync(0xFFFFFFFFu, mk);
+        const unsigned who = __ballot_sync(0xFFFFFFFFu, mk == kq);
+        if (lane == __ffs(who) - 1) mk = 0u;  // (every real key is above 0)
+      }
+      uint32_t* wq = reinterpret_cast<uint32_t*>(red4);
+      if (lane == 0) wq[tid >> 5] = kq;
+      __syncthreads();
+      uint32_t kmin = wq[0];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) kmin = min(kmin, wq[w]);
+      if (kmin > f32_key(-INFINITY)) {
+        tau = (static_cast<uint64_t>(kmin) << 32) - 1ull;
+        tauv = key_f32(kmin);
+      }
+      __syncthreads();  // (red4 is the cuts' scratch)
+    }
     tm *= invT;
     if (tm > mt) {
       st = mt > -INFINITY ? st * __expf(mt - tm) : 0.0f;
       mt = tm;
     }
-    // the losers' exponentials in four independent sums; a logit at or
-    // above tau's value (rare once the bound has risen) is checked by its
-    // exact key, and the warp's appends take one atomic (a prefix sum of the
-    // lanes' counts)
+    // the losers' exponentials in four independent sums, as 2^(v c - m c)
+    // with c = log2(e) / T; a logit at or above tau's value (rare once the
+    // bound has risen) is checked by its exact key, a loser then after all,
+    // and the warp's appends take one atomic (a prefix sum of the lanes'
+    // counts)
     float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const float mref = mt > -INFINITY ? mt : 0.0f;  // (past the row's end: -inf, adds 0)
+    const float c2 = invT * 1.4426950408889634f, b2 = -mref * 1.4426950408889634f;
     uint32_t fl = 0u;
 #pragma unroll
     for (int u = 0; u < kRowVals; ++u) {
-      const int e = t * kRowTile + 4 * ((u >> 2) * kThreads + tid) + (u & 3);
-      if (v[u] >= tauv && e < V && rank_key(v[u], static_cast<uint32_t>(e)) > tau)
-        fl |= 1u << u;
-      else
-        s4[u & 3] += __expf(v[u] * invT - mref);
+      const bool hi = v[u] >= tauv;
+      fl |= hi ? 1u << u : 0u;
+      const float y = ex2_approx(fmaf(v[u], c2, b2));
+      s4[u & 3] += hi ? 0.0f : y;
     }
     if (__any_sync(0xFFFFFFFFu, fl != 0u)) {
-      const int cnt = __popc(fl);
+      uint32_t ap = 0u;
+#pragma unroll
+      for (int u = 0; u < kRowVals; ++u)
+        if ((fl >> u) & 1u) {
+          const int e = t * kRowTile + 4 * ((u >> 2) * kThreads + tid) + (u & 3);
+          if (e < V && rank_key(v[u], static_cast<uint32_t>(e)) > tau)
+            ap |= 1u << u;
+          else
+            s4[u & 3] += ex2_approx(fmaf(v[u], c2, b2));
+        }
+      const int cnt = __popc(ap);
       int incl = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -923,11 +978,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_topm_rows(const TopmParams p) {
       }
       const int wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
       int base = 0;
-      if (lane == 31) base = atomicAdd(&s_cnt, wtot);
+      if (lane == 31 && wtot > 0) base = atomicAdd(&s_cnt, wtot);
       base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
 #pragma unroll
       for (int u = 0; u < kRowVals; ++u)
-        if ((fl >> u) & 1u) {
+        if ((ap >> u) & 1u) {
           const int e = t * kRowTile + 4 * ((u >> 2) * kThreads + tid) + (u & 3);
           buf[base++] = rank_key(v[u], static_cast<uint32_t>(e));
         }

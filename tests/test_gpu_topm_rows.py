@@ -90,3 +90,35 @@ def test_row_streaming_topm_matches_oracle_and_chunked_kernel():
     finally:
         big.close()
         small.close()
+
+
+@pytest.mark.parametrize("M", [128, 200])
+def test_row_streaming_topm_other_m_matches_oracle(M):
+    """M = 128 (the first tile's bound taken as the 8th-largest lane maximum
+    of every warp) and M = 200 (above what that bound covers: the row starts
+    unbounded), through the context-free entry point, which streams rows the
+    same way when there are at least as many rows as SMs."""
+    import torch
+    from conditional_draft_tree_lm_gb300.dtree import topm_noalloc
+    from oracle.dartree import top_m
+    torch.cuda.set_device(0)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, V, T = n_sm + 8, 151936, 1.0
+    x = _logits(rows, V, 1)
+    xd = torch.from_numpy(x).cuda()
+    tok = torch.full((rows, M), -7, dtype=torch.int32, device="cuda")
+    base = torch.full((rows, M), float("nan"), dtype=torch.float32, device="cuda")
+    rest = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+    topm_noalloc(xd, M, T, tok, base, rest)
+    torch.cuda.synchronize()
+    tok, base, rest = tok.cpu().numpy(), base.cpu().numpy(), rest.cpu().numpy()
+    checked = 0
+    for row in range(rows):
+        ids, vals, rho = top_m(x[row].astype(np.float64), M, T)
+        s = np.sort(x[row].astype(np.float64))[::-1]
+        if s[M - 1] - s[M] > 1e-3 or row == 1:
+            assert tok[row].tolist() == ids.tolist(), f"M={M} row {row}: ids differ from the oracle"
+            assert np.array_equal(base[row].astype(np.float64), vals), f"M={M} row {row}: logits"
+            checked += 1
+        assert abs(float(rest[row]) - rho) <= REST_TOL, f"M={M} row {row}: rest vs the oracle"
+    assert checked >= rows // 2
