@@ -1,9 +1,10 @@
 """Top-M over many rows: the row-streaming kernel against the fp64 oracle and
 against the chunked kernel.
 
-With at least one row per SM, dt_topm runs the kernel that streams each whole
-row in one CTA (a candidate buffer behind a rising bound, cut to its M best
-whenever it could overflow) instead of the chunked kernel and its merge.  The
+With at least one row per SM, dt_topm runs the kernel that streams rows (a
+candidate buffer behind a rising bound, cut to its M best whenever it could
+overflow) instead of the chunked kernel and its merge; with more rows than
+CTAs, some CTAs stream two rows.  The
 two must agree: candidate ids and their logits bit-exact, the rest
 log-partition within 1e-4 (the two sum in different orders).  Every row is
 also checked against the oracle's Top-M ("Resumen Técnico: DominoTree",
@@ -92,18 +93,21 @@ def test_row_streaming_topm_matches_oracle_and_chunked_kernel():
         small.close()
 
 
-@pytest.mark.parametrize("M", [128, 200])
-def test_row_streaming_topm_other_m_matches_oracle(M):
+@pytest.mark.parametrize("M,extra_rows", [(128, 8), (200, 8), (64, None), (136, None)])
+def test_row_streaming_topm_other_m_matches_oracle(M, extra_rows):
     """M = 128 (the first tile's bound taken as the 8th-largest lane maximum
-    of every warp) and M = 200 (above what that bound covers: the row starts
+    of every warp) and M = 200 (above what that bound covers: a segment starts
     unbounded), through the context-free entry point, which streams rows the
-    same way when there are at least as many rows as SMs."""
+    same way when there are at least as many rows as SMs.  With more rows than
+    two per SM (extra_rows None: 2 SMs + 37 rows) some CTAs stream a second
+    row after their first."""
     import torch
     from conditional_draft_tree_lm_gb300.dtree import topm_noalloc
     from oracle.dartree import top_m
     torch.cuda.set_device(0)
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    rows, V, T = n_sm + 8, 151936, 1.0
+    rows = n_sm + extra_rows if extra_rows is not None else 2 * n_sm + 37
+    V, T = 151936, 1.0
     x = _logits(rows, V, 1)
     xd = torch.from_numpy(x).cuda()
     tok = torch.full((rows, M), -7, dtype=torch.int32, device="cuda")
