@@ -944,9 +944,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_topm_rows(const TopmParams p) {
     }
     // the losers' exponentials in four independent sums, as 2^(v c - m c)
     // with c = log2(e) / T; a logit at or above tau's value (rare once the
-    // bound has risen) is checked by its exact key, a loser then after all,
-    // and the warp's appends take one atomic (a prefix sum of the lanes'
-    // counts)
+    // bound has risen) is checked by its exact key and appended with one
+    // shared atomic, or is a loser after all
     float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const float mref = mt > -INFINITY ? mt : 0.0f;  // (past the row's end: -inf, adds 0)
     const float c2 = invT * 1.4426950408889634f, b2 = -mref * 1.4426950408889634f;
@@ -959,32 +958,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_topm_rows(const TopmParams p) {
       s4[u & 3] += hi ? 0.0f : y;
     }
     if (__any_sync(0xFFFFFFFFu, fl != 0u)) {
-      uint32_t ap = 0u;
 #pragma unroll
       for (int u = 0; u < kRowVals; ++u)
         if ((fl >> u) & 1u) {
           const int e = t * kRowTile + 4 * ((u >> 2) * kThreads + tid) + (u & 3);
-          if (e < V && rank_key(v[u], static_cast<uint32_t>(e)) > tau)
-            ap |= 1u << u;
+          const uint64_t k = rank_key(v[u], static_cast<uint32_t>(e));
+          if (e < V && k > tau)
+            buf[atomicAdd(&s_cnt, 1)] = k;
           else
             s4[u & 3] += ex2_approx(fmaf(v[u], c2, b2));
-        }
-      const int cnt = __popc(ap);
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      int base = 0;
-      if (lane == 31 && wtot > 0) base = atomicAdd(&s_cnt, wtot);
-      base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
-#pragma unroll
-      for (int u = 0; u < kRowVals; ++u)
-        if ((ap >> u) & 1u) {
-          const int e = t * kRowTile + 4 * ((u >> 2) * kThreads + tid) + (u & 3);
-          buf[base++] = rank_key(v[u], static_cast<uint32_t>(e));
         }
     }
     st += (s4[0] + s4[1]) + (s4[2] + s4[3]);
